@@ -1,0 +1,158 @@
+"""fp64 CPU oracle for the mLSTM matrix-memory cell -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
+import this package.  The product path (the CUDA library and its Python binding) never
+imports, links or calls it, and it shares no code with them: the two meet only through the
+seeded input generator in ``mlstm_matrix_memory_02_b300.workloads``, which holds none of the
+method's arithmetic.
+
+The arithmetic lives in ``mlstm_oracle.c`` (plain C, fp64, one POSIX thread per
+(batch, head) pair at a time).  It follows "xLSTM: How Exponential Gating and Matrix Memory
+Scale Recurrent Neural Networks" (llms.blog): section 2 "The Normalizer State and Numerical
+Stabilization" for the log-space max stabiliser, section 3 "Associative Matrix Cell State"
+for the key scale, the C_t / n_t updates and the retrieval, and section 3 "The Parallel
+Dual Form" for the quadratic form.  Pins against closed forms, exact rational arithmetic and
+library routines are in ``tests/test_oracle_pins.py``.
+
+Parity pinning: every routine here is pinned (no routine is "parity unpinned").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mlstm_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle_mlstm.so")
+_lib = None
+
+# -ffp-contract=off: no fused multiply-adds, so every product and sum rounds as written.
+CFLAGS = ["-O2", "-fPIC", "-shared", "-pthread", "-ffp-contract=off", "-std=c11"]
+
+
+def build(src: str = _SRC, out: str = _LIB_PATH, quiet: bool = True) -> str:
+    """Compile the oracle with gcc into a shared library; returns its path."""
+    cmd = ["gcc", *CFLAGS, "-o", out, src, "-lm"]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError(f"oracle build failed: {' '.join(cmd)}\n{res.stderr}")
+    if not quiet and res.stderr:
+        print(res.stderr)
+    return out
+
+
+def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
+    dp = ctypes.POINTER(ctypes.c_double)
+    i = ctypes.c_int
+    lib.oracle_mlstm_recurrent.restype = i
+    lib.oracle_mlstm_recurrent.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, dp, dp, dp,
+                                           dp, dp, dp, dp, dp, i, dp, dp, dp, i]
+    lib.oracle_mlstm_unstabilised.restype = i
+    lib.oracle_mlstm_unstabilised.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, dp, dp, dp, i]
+    lib.oracle_mlstm_parallel.restype = i
+    lib.oracle_mlstm_parallel.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, dp, i]
+    return lib
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the compiled oracle (building it first if the library is missing or stale)."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    if _lib is None:
+        if (not os.path.exists(_LIB_PATH)
+                or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
+            build()
+        _lib = _declare(ctypes.CDLL(_LIB_PATH))
+    return _lib
+
+
+def _f64(x):
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _shapes(q, k, v, ig, fg):
+    if q.ndim != 4 or k.shape != q.shape or v.ndim != 4 or v.shape[:3] != q.shape[:3]:
+        raise ValueError("q,k must be [B,NH,S,DQK] and v [B,NH,S,DV]")
+    if ig.shape != q.shape[:3] or fg.shape != q.shape[:3]:
+        raise ValueError("gate pre-activations must be [B,NH,S]")
+    B, NH, S, DQK = q.shape
+    return B, NH, S, DQK, v.shape[3]
+
+
+def recurrent(q, k, v, ig, fg, C0=None, n0=None, m0=None, snap_every=0, want_h=True,
+              want_m_tok=False, nthreads=0, lib=None):
+    """Stabilised step-by-step mLSTM in fp64.
+
+    Returns a dict with ``h`` [B,NH,S,DV] (unless want_h is False), the final state ``C``
+    [B,NH,DV,DQK], ``n`` [B,NH,DQK], ``m`` [B,NH]; ``m_tok`` [B,NH,S] if asked; and, when
+    ``snap_every`` > 0, ``C_snap``/``n_snap``/``m_snap`` holding the state at
+    t = 0, snap_every, ..., S (the state entering each chunk, then the final one).
+    """
+    lib = lib or load()
+    q, k, v, ig, fg = (_f64(x) for x in (q, k, v, ig, fg))
+    B, NH, S, DQK, DV = _shapes(q, k, v, ig, fg)
+    C0 = None if C0 is None else _f64(C0).reshape(B, NH, DV, DQK)
+    n0 = None if n0 is None else _f64(n0).reshape(B, NH, DQK)
+    m0 = None if m0 is None else _f64(m0).reshape(B, NH)
+    out = {
+        "C": np.empty((B, NH, DV, DQK)),
+        "n": np.empty((B, NH, DQK)),
+        "m": np.empty((B, NH)),
+    }
+    if want_h:
+        out["h"] = np.empty((B, NH, S, DV))
+    if want_m_tok:
+        out["m_tok"] = np.empty((B, NH, S))
+    if snap_every > 0:
+        if S % snap_every:
+            raise ValueError("snap_every must divide S")
+        ns = S // snap_every + 1
+        out["C_snap"] = np.empty((B, NH, ns, DV, DQK))
+        out["n_snap"] = np.empty((B, NH, ns, DQK))
+        out["m_snap"] = np.empty((B, NH, ns))
+    rc = lib.oracle_mlstm_recurrent(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(ig), _ptr(fg), B, NH, S, DQK, DV,
+        _ptr(C0), _ptr(n0), _ptr(m0), _ptr(out.get("h")), _ptr(out["C"]), _ptr(out["n"]),
+        _ptr(out["m"]), _ptr(out.get("m_tok")), int(snap_every), _ptr(out.get("C_snap")),
+        _ptr(out.get("n_snap")), _ptr(out.get("m_snap")), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_mlstm_recurrent rejected its arguments (code {rc})")
+    return out
+
+
+def unstabilised(q, k, v, ig, fg, nthreads=0, lib=None):
+    """Unstabilised recurrent mLSTM (f = sigmoid, i = exp, floor 1) in fp64."""
+    lib = lib or load()
+    q, k, v, ig, fg = (_f64(x) for x in (q, k, v, ig, fg))
+    B, NH, S, DQK, DV = _shapes(q, k, v, ig, fg)
+    out = {"h": np.empty((B, NH, S, DV)), "C": np.empty((B, NH, DV, DQK)),
+           "n": np.empty((B, NH, DQK))}
+    rc = lib.oracle_mlstm_unstabilised(_ptr(q), _ptr(k), _ptr(v), _ptr(ig), _ptr(fg), B, NH, S,
+                                       DQK, DV, _ptr(out["h"]), _ptr(out["C"]), _ptr(out["n"]),
+                                       int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_mlstm_unstabilised rejected its arguments (code {rc})")
+    return out
+
+
+def parallel(q, k, v, ig, fg, nthreads=0, lib=None):
+    """Fully parallel quadratic (dual) form from the zero state, fp64, O(S^2) per head."""
+    lib = lib or load()
+    q, k, v, ig, fg = (_f64(x) for x in (q, k, v, ig, fg))
+    B, NH, S, DQK, DV = _shapes(q, k, v, ig, fg)
+    h = np.empty((B, NH, S, DV))
+    rc = lib.oracle_mlstm_parallel(_ptr(q), _ptr(k), _ptr(v), _ptr(ig), _ptr(fg), B, NH, S, DQK,
+                                   DV, _ptr(h), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_mlstm_parallel rejected its arguments (code {rc})")
+    return h

@@ -1,0 +1,240 @@
+"""Pins for the fp64 oracle: properties fixed by the mathematics of the mLSTM cell, each
+computed by a route other than the oracle's own loop.
+
+Page: "xLSTM: How Exponential Gating and Matrix Memory Scale Recurrent Neural Networks"
+(llms.blog).  Section 2 "The Normalizer State and Numerical Stabilization" (max
+stabiliser), section 3 "Associative Matrix Cell State" (updates, retrieval, key scale) and
+"The Parallel Dual Form" (unrolled sum, causal decay matrix).
+
+Each pin takes the loaded oracle library so that the mutation test can run the same pins
+against deliberately broken copies of the oracle.
+"""
+from __future__ import annotations
+
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+
+import oracle
+from golden.exact_case import exact_rational_case
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def rand_inputs(B, NH, S, DQK, DV, seed, ig=(0.0, 1.0), fg=(1.0, 1.5)):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, NH, S, DQK))
+    k = rng.standard_normal((B, NH, S, DQK))
+    v = rng.standard_normal((B, NH, S, DV))
+    igp = ig[0] + ig[1] * rng.standard_normal((B, NH, S))
+    fgp = fg[0] + fg[1] * rng.standard_normal((B, NH, S))
+    return q, k, v, igp, fgp
+
+
+def rel(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300))
+
+
+def log_sigmoid_np(x):
+    # library route: log sigma(x) = -log(1 + e^{-x}) via numpy's logaddexp
+    return -np.logaddexp(0.0, -np.asarray(x, np.float64))
+
+
+# ---------------------------------------------------------------- the pins
+def pin_recurrent_equals_parallel(lib):
+    """Recurrent form == the parallel dual form H = ((Q K^T) o S) V, row-normalised
+    (section 3 "The Parallel Dual Form"); DQK != DV so a transposed operand shows."""
+    worst = 0.0
+    for seed, fg in ((1, (1.0, 1.5)), (2, (-1.0, 2.0)), (3, (4.0, 0.5))):
+        q, k, v, ig, fgp = rand_inputs(2, 2, 20, 6, 5, seed, fg=fg)
+        h_rec = oracle.recurrent(q, k, v, ig, fgp, lib=lib)["h"]
+        h_par = oracle.parallel(q, k, v, ig, fgp, lib=lib)
+        worst = max(worst, rel(h_rec, h_par))
+    return worst <= 1e-11, f"recurrent vs parallel rel err {worst:.3e}"
+
+
+def pin_stabiliser_is_a_rescaling(lib):
+    """The max stabiliser rescales C and n by exp(-m_t) and leaves h unchanged
+    (section 2): stabilised h == unstabilised h, C_stab e^m == C_unstab, n likewise."""
+    worst = 0.0
+    for seed in (4, 5):
+        q, k, v, ig, fg = rand_inputs(2, 3, 40, 7, 4, seed, ig=(0.0, 1.5), fg=(0.5, 2.0))
+        st = oracle.recurrent(q, k, v, ig, fg, lib=lib)
+        un = oracle.unstabilised(q, k, v, ig, fg, lib=lib)
+        e = np.exp(st["m"])
+        worst = max(worst, rel(st["h"], un["h"]), rel(st["C"] * e[..., None, None], un["C"]),
+                    rel(st["n"] * e[..., None], un["n"]))
+    return worst <= 1e-11, f"stabilised vs unstabilised rel err {worst:.3e}"
+
+
+def pin_single_token_closed_form(lib):
+    """From the zero state (m_0 = 0) one token gives m_1 = max(log sigma(f~), i~),
+    C_1 = e^{i~ - m_1} v k^T/sqrt(d), n_1 = e^{i~ - m_1} k/sqrt(d) and
+    h_1 = e^{i~} (k.q/sqrt(d)) v / max(e^{i~} |k.q/sqrt(d)|, 1)."""
+    rng = np.random.default_rng(6)
+    worst = 0.0
+    both_branches = set()
+    for trial in range(12):
+        d, dv = 8, 3
+        q = rng.standard_normal((1, 1, 1, d))
+        k = rng.standard_normal((1, 1, 1, d))
+        v = rng.standard_normal((1, 1, 1, dv))
+        ig = np.array([[[rng.uniform(-4, 4)]]])
+        fg = np.array([[[rng.uniform(-4, 4)]]])
+        out = oracle.recurrent(q, k, v, ig, fg, lib=lib)
+        s = float(k[0, 0, 0] @ q[0, 0, 0]) / np.sqrt(d)
+        i = float(np.exp(ig[0, 0, 0]))
+        den = max(i * abs(s), 1.0)
+        both_branches.add(i * abs(s) >= 1.0)
+        h = i * s * v[0, 0, 0] / den
+        m1 = max(float(log_sigmoid_np(fg[0, 0, 0])), float(ig[0, 0, 0]))
+        w = np.exp(float(ig[0, 0, 0]) - m1)
+        C1 = w * np.outer(v[0, 0, 0], k[0, 0, 0] / np.sqrt(d))
+        n1 = w * k[0, 0, 0] / np.sqrt(d)
+        worst = max(worst, rel(out["h"][0, 0, 0], h), rel(out["C"][0, 0], C1),
+                    rel(out["n"][0, 0], n1), abs(float(out["m"][0, 0]) - m1))
+    ok = worst <= 1e-12 and both_branches == {True, False}
+    return ok, f"single-token closed form err {worst:.3e}, branches {sorted(both_branches)}"
+
+
+def pin_linear_attention_limit(lib):
+    """f~ -> +inf (f = 1) with i~ = 0 reduces the cell to causal linear attention
+    (section 3, last paragraph): h_t = sum_{j<=t} (q_t.k_j) v_j / max(|sum_{j<=t} q_t.k_j|, 1),
+    evaluated with a masked matrix product."""
+    q, k, v, _, _ = rand_inputs(1, 2, 32, 6, 5, 7)
+    ig = np.zeros(q.shape[:3])
+    fg = np.full(q.shape[:3], 60.0)  # log sigma(60) = -8.8e-27: the decay is 1 to fp64
+    h = oracle.recurrent(q, k, v, ig, fg, lib=lib)["h"]
+    kh = k / np.sqrt(q.shape[-1])
+    A = np.tril(np.einsum("bhtc,bhjc->bhtj", q, kh))
+    num = np.einsum("bhtj,bhja->bhta", A, v)
+    den = np.maximum(np.abs(A.sum(-1)), 1.0)
+    err = rel(h, num / den[..., None])
+    return err <= 1e-12, f"linear-attention limit rel err {err:.3e}"
+
+
+def pin_stabiliser_max_plus_form(lib):
+    """Unrolling m_t = max(log f_t + m_{t-1}, i~_t) gives
+    m_t = F_t + max(m_0, max_{j<=t}(i~_j - F_j)) with F_t = sum_{tau<=t} log f_tau;
+    checked with cumulative sums and running maxima, also from a nonzero m_0."""
+    q, k, v, ig, fg = rand_inputs(2, 2, 50, 4, 4, 8, ig=(0.0, 3.0), fg=(0.0, 2.0))
+    m0 = np.array([[0.0, 2.5], [-1.0, 7.0]])
+    C0 = np.zeros((2, 2, 4, 4))
+    n0 = np.zeros((2, 2, 4))
+    out = oracle.recurrent(q, k, v, ig, fg, C0=C0, n0=n0, m0=m0, want_m_tok=True, lib=lib)
+    F = np.cumsum(log_sigmoid_np(fg), axis=-1)
+    run = np.maximum.accumulate(ig - F, axis=-1)
+    m_ref = F + np.maximum(m0[..., None], run)
+    err = float(np.max(np.abs(out["m_tok"] - m_ref) / (1 + np.abs(m_ref))))
+    err = max(err, float(np.max(np.abs(out["m"] - m_ref[..., -1]))))
+    return err <= 1e-12, f"max-plus stabiliser err {err:.3e}"
+
+
+def pin_exact_rational(lib):
+    """Exact rational evaluation of the unrolled sum (section 3) on integer inputs;
+    the stabiliser stays at m = 0 here, so the stabilised oracle is compared as is."""
+    (q, k, v, ig, fg), h, C, n = exact_rational_case()
+    out = oracle.recurrent(q, k, v, ig, fg, lib=lib)
+    hx = np.array([[float(x) for x in row] for row in h])
+    Cx = np.array([[float(x) for x in row] for row in C])
+    nx = np.array([float(x) for x in n])
+    err = max(rel(out["h"][0, 0], hx), rel(out["C"][0, 0], Cx), rel(out["n"][0, 0], nx),
+              abs(float(out["m"][0, 0])))
+    # both sides of max(|n.q|, 1) and both signs of n.q must occur in this case
+    nq_vals = []
+    for t in range(q.shape[2]):
+        kk = k[0, 0, : t + 1] / 2.0
+        w = 2.0 ** -(t - np.arange(t + 1))
+        nq_vals.append(float((w[:, None] * kk).sum(0) @ q[0, 0, t]))
+    nq_vals = np.array(nq_vals)
+    covered = (np.any(np.abs(nq_vals) < 1) and np.any(np.abs(nq_vals) > 1)
+               and np.any(nq_vals < -1))
+    return err <= 1e-14 and covered, f"exact rational err {err:.3e}, branches covered {covered}"
+
+
+def pin_golden_fixture(lib):
+    """Stored exact values (tests/golden/exact_rational_case.json, written by
+    tests/golden/make_golden.py from the unrolled sum in exact arithmetic)."""
+    with open(os.path.join(GOLDEN, "exact_rational_case.json")) as f:
+        g = json.load(f)
+    q, k, v = (np.array(g[x], np.float64) for x in ("q", "k", "v"))
+    ig, fg = np.array(g["ig"], np.float64), np.array(g["fg"], np.float64)
+    out = oracle.recurrent(q, k, v, ig, fg, lib=lib)
+    hx = np.array([[float(Fraction(x)) for x in row] for row in g["h"]])
+    Cx = np.array([[float(Fraction(x)) for x in row] for row in g["C_last"]])
+    err = max(rel(out["h"][0, 0], hx), rel(out["C"][0, 0], Cx))
+    return err <= 1e-14, f"golden fixture err {err:.3e}"
+
+
+def pin_split_sequence(lib):
+    """The state (C, n, m) carries everything (section 5 "Inference Memory and Throughput
+    Trade-Offs"): running S1 tokens, then S2 more from that state, equals running S1+S2."""
+    q, k, v, ig, fg = rand_inputs(2, 2, 36, 5, 6, 10, ig=(0.0, 2.0), fg=(1.0, 2.0))
+    full = oracle.recurrent(q, k, v, ig, fg, lib=lib)
+    s1 = 13
+    a = oracle.recurrent(q[:, :, :s1], k[:, :, :s1], v[:, :, :s1], ig[:, :, :s1], fg[:, :, :s1],
+                         lib=lib)
+    b = oracle.recurrent(q[:, :, s1:], k[:, :, s1:], v[:, :, s1:], ig[:, :, s1:], fg[:, :, s1:],
+                         C0=a["C"], n0=a["n"], m0=a["m"], lib=lib)
+    err = max(rel(np.concatenate([a["h"], b["h"]], axis=2), full["h"]), rel(b["C"], full["C"]),
+              rel(b["n"], full["n"]), float(np.max(np.abs(b["m"] - full["m"]))))
+    return err <= 1e-12, f"split-sequence err {err:.3e}"
+
+
+def pin_snapshots(lib):
+    """Chunk-boundary snapshots equal the final state of the prefix runs."""
+    q, k, v, ig, fg = rand_inputs(1, 2, 24, 4, 3, 11)
+    out = oracle.recurrent(q, k, v, ig, fg, snap_every=8, lib=lib)
+    err = float(np.max(np.abs(out["C_snap"][:, :, 0]))) + float(np.max(np.abs(out["m_snap"][:, :, 0])))
+    for s, t in enumerate((8, 16, 24), start=1):
+        pre = oracle.recurrent(q[:, :, :t], k[:, :, :t], v[:, :, :t], ig[:, :, :t], fg[:, :, :t],
+                               lib=lib)
+        err = max(err, rel(out["C_snap"][:, :, s], pre["C"]), rel(out["n_snap"][:, :, s], pre["n"]),
+                  float(np.max(np.abs(out["m_snap"][:, :, s] - pre["m"]))))
+    return err <= 1e-13, f"snapshot err {err:.3e}"
+
+
+def pin_causality_and_linearity(lib):
+    """Causal decay matrix: S_ij = 0 for i < j (token t' cannot change h_t, t < t');
+    H = ((Q K^T) o S) V is linear in V."""
+    q, k, v, ig, fg = rand_inputs(1, 2, 30, 4, 4, 12)
+    base = oracle.recurrent(q, k, v, ig, fg, lib=lib)
+    tp = 17
+    q2, k2, v2, ig2, fg2 = (x.copy() for x in (q, k, v, ig, fg))
+    q2[:, :, tp] += 1.0; k2[:, :, tp] -= 2.0; v2[:, :, tp] *= 3.0; ig2[:, :, tp] += 5.0; fg2[:, :, tp] -= 1.0
+    pert = oracle.recurrent(q2, k2, v2, ig2, fg2, lib=lib)
+    causal = np.array_equal(base["h"][:, :, :tp], pert["h"][:, :, :tp])
+    changed = not np.allclose(base["h"][:, :, tp:], pert["h"][:, :, tp:])
+    scaled = oracle.recurrent(q, k, 2.5 * v, ig, fg, lib=lib)
+    lin = max(rel(scaled["h"], 2.5 * base["h"]), rel(scaled["C"], 2.5 * base["C"]))
+    ok = causal and changed and lin <= 1e-14
+    return ok, f"causal {causal}, later rows changed {changed}, linearity err {lin:.3e}"
+
+
+ALL_PINS = [
+    pin_recurrent_equals_parallel,
+    pin_stabiliser_is_a_rescaling,
+    pin_single_token_closed_form,
+    pin_linear_attention_limit,
+    pin_stabiliser_max_plus_form,
+    pin_exact_rational,
+    pin_golden_fixture,
+    pin_split_sequence,
+    pin_snapshots,
+    pin_causality_and_linearity,
+]
+
+
+def run_all(lib):
+    """[(name, ok, message)] for every pin (exceptions count as failures)."""
+    res = []
+    for pin in ALL_PINS:
+        try:
+            ok, msg = pin(lib)
+        except Exception as e:  # a broken oracle may fail loudly instead of numerically
+            ok, msg = False, f"raised {type(e).__name__}: {e}"
+        res.append((pin.__name__, bool(ok), msg))
+    return res
