@@ -1,0 +1,384 @@
+"""Benchmark of the mLSTM cell forward on one B300 (or N, one process per GPU).
+
+A step is one chunkwise forward of the 1.3B-style layer (B=4, NH=4, S=2048, d=512, chunk 64,
+bf16 q/k/v, fp32 gates, fp32 h) through the library: gate preprocessing, then the state
+passing and output stage.  The decode step (B=256, NH=8, d=256, fp32 state) is timed in its
+own loop and reported under "decode".  Inputs are synthetic (seeded) and resident in HBM;
+L2 is flushed between timed iterations (a 256 MiB write) outside the timed events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle on a bounded
+sample of the same workload instead (the reference arm of this build).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mlstm_matrix_memory_02_b300 import workloads as W  # noqa: E402
+
+FWD = W.LAYER_1P3B
+DEC = W.DECODE
+
+
+def fwd_flops(w) -> float:
+    """Algorithmic flops of one chunkwise forward: per head and chunk, L(L+1)(dqk+dv) for the
+    causal Q K^T and (S o D) V, plus 4 L dqk dv for Q C^T and the state update."""
+    L = w.chunk
+    per_chunk = L * (L + 1) * (w.DQK + w.DV) + 4 * L * w.DQK * w.DV
+    return float(per_chunk * (w.S // L) * w.B * w.NH)
+
+
+def fwd_bytes(w, h_bytes=4) -> float:
+    """Algorithmic HBM bytes: q, k, v read once (bf16), gates read once, h written once,
+    final state written once."""
+    P = w.B * w.NH
+    qkv = P * w.S * (2 * w.DQK + w.DV) * 2
+    gates = P * w.S * 2 * 4
+    h = P * w.S * w.DV * h_bytes
+    state = P * (w.DV * w.DQK + w.DQK + 1) * 4
+    return float(qkv + gates + h + state)
+
+
+def dec_bytes(w, h_bytes=4) -> float:
+    """Algorithmic bytes of one decode step: C and n read and written, m read and written,
+    q, k, v (bf16) and the gates read, h written."""
+    P = w.B * w.NH
+    return float(P * (2 * w.DV * w.DQK * 4 + 2 * w.DQK * 4 + 2 * 4
+                      + (2 * w.DQK + w.DV) * 2 + 2 * 4 + w.DV * h_bytes))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, local, world
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------------ CPU oracle arm
+def oracle_sample(w, heads: int):
+    """The first `heads` (batch, head) pairs of the workload, for the CPU oracle."""
+    inp = W.make_inputs(w.with_(B=1, NH=heads) if heads <= w.NH else w)
+    if heads > w.NH:
+        inp = {k: v.reshape(1, -1, *v.shape[2:])[:, :heads] for k, v in inp.items()}
+    return inp
+
+
+def time_oracle(w, heads: int, reps: int = 1):
+    """Wall time of the oracle over `heads` head-sequences of workload w; tokens/s of the full
+    layer (each layer token needs NH head-tokens)."""
+    import oracle
+    inp = oracle_sample(w, heads)
+    oracle.load()
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.recurrent(**inp)
+        times.append(time.perf_counter() - t0)
+    cores = min(os.cpu_count() or 1, heads)
+    tps = heads * w.S / w.NH / statistics.median(times)
+    return tps, cores, times
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    heads = max(1, min(os.cpu_count() or 1, FWD.B * FWD.NH))
+    for _ in range(args.warmup):
+        time_oracle(FWD, 1)
+    tps, cores, times = time_oracle(FWD, heads, reps=args.steps)
+    value = tps
+    sample = (f"{heads} of {FWD.B * FWD.NH} (batch, head) sequences of the {FWD.name}, full "
+              f"S={FWD.S}, per step; tokens/s scaled to the whole layer (x 1/NH)")
+    line = {
+        "metric": "mLSTM chunkwise forward tokens/s (1.3B-style layer)", "value": value,
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": FWD.name, "B": FWD.B, "NH": FWD.NH, "S": FWD.S, "DQK": FWD.DQK,
+                   "DV": FWD.DV, "chunk": FWD.chunk, "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------ GPU arm
+def run_ours(args, rank, local, world):
+    import torch
+    from mlstm_matrix_memory_02_b300 import binding as B
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+    w = FWD
+
+    inp = W.make_inputs(w)
+    q = torch.from_numpy(inp["q"]).to(dev).to(torch.bfloat16)
+    k = torch.from_numpy(inp["k"]).to(dev).to(torch.bfloat16)
+    v = torch.from_numpy(inp["v"]).to(dev).to(torch.bfloat16)
+    ig = torch.from_numpy(inp["ig"]).to(dev)
+    fg = torch.from_numpy(inp["fg"]).to(dev)
+    P = w.B * w.NH
+    h = torch.empty((w.B, w.NH, w.S, w.DV), dtype=torch.float32, device=dev)
+    C = torch.empty((w.B, w.NH, w.DV, w.DQK), dtype=torch.float32, device=dev)
+    n = torch.empty((w.B, w.NH, w.DQK), dtype=torch.float32, device=dev)
+    m = torch.empty((w.B, w.NH), dtype=torch.float32, device=dev)
+    ws = B.alloc_workspace(w.B, w.NH, w.S, w.DQK, w.DV, w.chunk, torch.bfloat16, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        B.mlstm_fwd_gates(ig, fg, w.chunk, workspace=ws, outputs=False)
+        ev_mid.record(stream)
+        B.mlstm_fwd_from_gates(q, k, v, w.chunk, ws, (h, C, n, m))
+
+    ev_mid = torch.cuda.Event(enable_timing=True)
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = B.mlstm_kernel_launches()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()  # evict the inputs from L2 (outside the timed events)
+            starts[i].record(stream)
+            B.mlstm_fwd_gates(ig, fg, w.chunk, workspace=ws, outputs=False)
+            mids[i].record(stream)
+            B.mlstm_fwd_from_gates(q, k, v, w.chunk, ws, (h, C, n, m))
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    launches_fwd = B.mlstm_kernel_launches() - launches0
+    barrier(world)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    main_ms = [s.elapsed_time(e) for s, e in zip(mids, ends)]
+    ms = statistics.mean(step_ms)
+    ms_max = max_over_ranks(ms, world)
+    tokens = w.B * w.S
+    value = tokens * world / (ms_max * 1e-3)
+
+    flops = fwd_flops(w)
+    main_mean = statistics.mean(main_ms)
+    achieved_tf = flops / (main_mean * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved_tf, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved_tf / peaks["bf16_tflops"], "traffic": None,
+                "kernel": "state passing + output stage (mlstm_fwd_from_gates)",
+                "algorithmic_flops_per_launch": flops, "ms_per_launch": main_mean,
+                "peak_source": f"{peaks['source']} bf16 dense (burst); fp16 operands run at the same rate",
+                "hbm_gbs_of_algorithmic_bytes": fwd_bytes(w) / (main_mean * 1e-3) / 1e9}
+
+    # ---- decode step: B=256, NH=8, d=256 state from a 512-token prefill through the library
+    dw = DEC
+    prior, steps = W.make_decode_inputs(dw.with_(S=max(args.steps, 1)))
+    dq = torch.from_numpy(prior["q"]).to(dev).to(torch.bfloat16)
+    dk = torch.from_numpy(prior["k"]).to(dev).to(torch.bfloat16)
+    dv = torch.from_numpy(prior["v"]).to(dev).to(torch.bfloat16)
+    _, Cd, nd, md = B.mlstm_fwd_chunkwise(dq, dk, dv, torch.from_numpy(prior["ig"]).to(dev),
+                                          torch.from_numpy(prior["fg"]).to(dev), 64,
+                                          h_dtype=torch.float32)
+    del dq, dk, dv
+    sq = torch.from_numpy(steps["q"]).to(dev).to(torch.bfloat16)
+    sk = torch.from_numpy(steps["k"]).to(dev).to(torch.bfloat16)
+    sv = torch.from_numpy(steps["v"]).to(dev).to(torch.bfloat16)
+    sig = torch.from_numpy(steps["ig"]).to(dev)
+    sfg = torch.from_numpy(steps["fg"]).to(dev)
+    per_step = [tuple(x[:, :, t].contiguous() for x in (sq, sk, sv, sig, sfg)) for t in range(sq.shape[2])]
+    hd = torch.empty((dw.B, dw.NH, dw.DV), dtype=torch.float32, device=dev)
+    for t in range(max(args.warmup, 3)):
+        B.mlstm_step(*per_step[t % len(per_step)], Cd, nd, md, h=hd)
+    torch.cuda.synchronize()
+    d0 = torch.cuda.Event(enable_timing=True)
+    d1 = torch.cuda.Event(enable_timing=True)
+    launches1 = B.mlstm_kernel_launches()
+    d0.record(stream)
+    for t in range(args.steps):  # the 512 MiB state is far larger than L2
+        B.mlstm_step(*per_step[t % len(per_step)], Cd, nd, md, h=hd)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    launches_dec = B.mlstm_kernel_launches() - launches1
+    dec_ms = d0.elapsed_time(d1) / max(args.steps, 1)
+    dec_gbs = dec_bytes(dw) / (dec_ms * 1e-3) / 1e9
+    decode = {"metric": "mLSTM decode step GB/s (B=256, NH=8, d=256, fp32 state)",
+              "value": dec_gbs, "unit": "GB/s", "us_per_step": dec_ms * 1e3,
+              "tokens_per_s": dw.B / (dec_ms * 1e-3),
+              "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"],
+                           "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"], "traffic": None,
+                           "kernel": "mlstm_step", "algorithmic_bytes_per_launch": dec_bytes(dw),
+                           "peak_source": peaks["source"] + " HBM copy"},
+              "frac_of_nominal_8tbs": dec_gbs / 8000.0}
+    del Cd, nd, md
+
+    # ---- end to end through the public API: pinned host inputs in, h back to the host
+    pin = {key: torch.from_numpy(inp[key]).to(torch.bfloat16 if key in "qkv" else torch.float32).pin_memory()
+           for key in ("q", "k", "v", "ig", "fg")}
+    h_host = torch.empty(h.shape, dtype=torch.float32).pin_memory()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = h_host.numel() * h_host.element_size()
+    e2e_ms = []
+    for i in range(max(args.warmup, 3) + args.steps):
+        flush.zero_()
+        e0.record(stream)
+        dd = {key: t.to(dev, non_blocking=True) for key, t in pin.items()}
+        hh, _, _, _ = B.mlstm_fwd_chunkwise(dd["q"], dd["k"], dd["v"], dd["ig"], dd["fg"], w.chunk,
+                                            h_dtype=torch.float32, out=(h, C, n, m), workspace=ws)
+        h_host.copy_(hh, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= max(args.warmup, 3):
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_val = tokens * world / (max_over_ranks(statistics.mean(e2e_ms), world) * 1e-3)
+
+    if rank != 0:
+        return
+    line = {
+        "metric": "mLSTM chunkwise forward tokens/s (1.3B-style layer)",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "NH": w.NH, "S": w.S, "DQK": w.DQK, "DV": w.DV,
+                   "chunk": w.chunk, "qkv": "bf16", "gates": "fp32", "h": "fp32",
+                   "l2": "flushed between timed iterations (256 MiB write, outside the events)",
+                   "per_rank": "each rank runs the full layer batch (weak scaling)"},
+        "roofline": roofline,
+        "decode": decode,
+        "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches_fwd + launches_dec),
+        "clocks": clk.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        heads = max(1, min(os.cpu_count() or 1, P))
+        tps, cores, times = time_oracle(w, heads)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": f"{heads} of {P} (batch, head) sequences of the {w.name}, "
+                                          f"full S={w.S}; tokens/s scaled to the layer (x 1/NH)",
+                                "seconds": times[0]}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, local, world = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, local, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

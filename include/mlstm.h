@@ -1,0 +1,143 @@
+/*
+ * mlstm.h -- C ABI of the B300 (sm_103a) mLSTM matrix-memory cell library.
+ *
+ * The cell (page "xLSTM: How Exponential Gating and Matrix Memory Scale Recurrent Neural
+ * Networks", llms.blog):
+ *   section 3 "Associative Matrix Cell State":  k_t is scaled by 1/sqrt(d_qk);
+ *       C_t = f_t C_{t-1} + i_t v_t k_t^T,  n_t = f_t n_{t-1} + i_t k_t,
+ *       h_t = C_t q_t / max(|n_t^T q_t|, exp(-m_t))          (stabilised form);
+ *   section 2 "The Normalizer State and Numerical Stabilization": the log-space max
+ *       stabiliser m_t = max(log f_t + m_{t-1}, i~_t), with i_t = exp(i~_t) and the
+ *       sigmoid forget gate used in log space, log f_t = log sigmoid(f~_t);
+ *   section 3 "The Parallel Dual Form" and section 5 (chunkwise scans): the forward is
+ *       computed chunk by chunk -- the quadratic form inside each chunk, the recurrent
+ *       state (C, n, m) passed across chunks;
+ *   section 5 "Inference Memory and Throughput Trade-Offs": decoding carries only the
+ *       constant-size state (C, n, m), updated in place one token at a time.
+ *
+ * Conventions for every entry point
+ *   - Every array pointer is DEVICE memory owned by the caller; the library allocates
+ *     nothing and keeps no state between calls.
+ *   - All arrays are contiguous row-major with the layouts given below; every pointer
+ *     must be 16-byte aligned.
+ *   - q, k, v are given in `dt` (MLSTM_F32 or MLSTM_BF16); k is passed UNSCALED and the
+ *     library applies 1/sqrt(DQK).  The gate pre-activations and every state array are
+ *     float32.  h is written in `h_dt`.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream) and
+ *     the call returns without synchronising.  Argument errors are detected on the host
+ *     and returned before anything is launched; a failed launch returns MLSTM_ERR_LAUNCH.
+ *   - Layout of the state: C[b][h][a][c] accumulates v_a * k_c (d_v rows, d_qk columns),
+ *     n[b][h][c], m[b][h].  (C, n) are stored relative to the stabiliser: the
+ *     unstabilised state is C * exp(m).
+ *
+ * Supported sizes: B, NH >= 1; S >= 0 with S % chunk == 0; chunk in {16, 32, 64, 128};
+ * DQK and DV multiples of 32 in [32, 512].
+ */
+#ifndef MLSTM_B300_H
+#define MLSTM_B300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLSTM_OK = 0,
+  MLSTM_ERR_NULL = 1,      /* a required pointer is NULL */
+  MLSTM_ERR_ALIGN = 2,     /* a pointer is not 16-byte aligned */
+  MLSTM_ERR_SHAPE = 3,     /* a size is outside the supported set, or S % chunk != 0 */
+  MLSTM_ERR_DTYPE = 4,     /* unsupported dtype code */
+  MLSTM_ERR_WORKSPACE = 5, /* workspace smaller than mlstm_fwd_workspace_bytes() */
+  MLSTM_ERR_LAUNCH = 6,    /* a kernel launch failed (see mlstm_last_cuda_error) */
+  MLSTM_ERR_TIMEOUT = 7,   /* a bounded device-side wait gave up (reported by a kernel) */
+  MLSTM_ERR_DEVICE = 8     /* no usable device, or the device is not sm_103 */
+} mlstm_status;
+
+typedef enum { MLSTM_F32 = 0, MLSTM_BF16 = 1 } mlstm_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *mlstm_status_str(mlstm_status s);
+
+/* The cudaError_t value (as int) behind the last MLSTM_ERR_LAUNCH returned on the calling
+ * host thread, 0 if there was none.  The CUDA error itself has been consumed. */
+int mlstm_last_cuda_error(void);
+
+/* Number of kernels this library has launched in the process so far (all host threads);
+ * the difference across a region counts the library's launches inside it. */
+unsigned long long mlstm_kernel_launches(void);
+
+/* Bytes of device workspace mlstm_fwd_chunkwise / mlstm_fwd_chunk_states need for these
+ * sizes (0 if the sizes are unsupported).  The workspace holds the per-token gate
+ * prefix sums, the per-chunk stabiliser and, on paths that materialise them, the
+ * chunk-boundary states.  Its contents are scratch: nothing is read back by the caller. */
+size_t mlstm_fwd_workspace_bytes(int B, int NH, int S, int DQK, int DV, int chunk,
+                                 mlstm_dtype dt);
+
+/* Chunkwise forward of the mLSTM cell over a whole sequence (section 3 "The Parallel Dual
+ * Form", chunked; section 2 stabiliser).
+ *   q, k     [B, NH, S, DQK]  (dt)          v        [B, NH, S, DV]   (dt)
+ *   igate_pre, fgate_pre  [B, NH, S] float32: the gate pre-activations i~_t and f~_t
+ *   C_init [B,NH,DV,DQK], n_init [B,NH,DQK], m_init [B,NH] float32: the state the
+ *       sequence continues from; all three NULL = the zero state with m_0 = 0 (either
+ *       all NULL or none).
+ *   h      [B, NH, S, DV]  (h_dt) output: h~_t for every token
+ *   C_last [B,NH,DV,DQK], n_last [B,NH,DQK], m_last [B,NH] float32 outputs: the state
+ *       after the last token (may alias C_init/n_init/m_init for an in-place update).
+ *   workspace: at least mlstm_fwd_workspace_bytes(...) bytes of device memory.
+ * S == 0 copies the initial state to the outputs. */
+mlstm_status mlstm_fwd_chunkwise(const void *q, const void *k, const void *v,
+                                 const float *igate_pre, const float *fgate_pre, int B, int NH,
+                                 int S, int DQK, int DV, int chunk, mlstm_dtype dt,
+                                 const float *C_init, const float *n_init, const float *m_init,
+                                 void *h, mlstm_dtype h_dt, float *C_last, float *n_last,
+                                 float *m_last, void *workspace, size_t ws_bytes, void *stream);
+
+/* The two stages of mlstm_fwd_chunkwise, for callers that time or schedule them apart:
+ * mlstm_fwd_gates (below) runs the gate preprocessing into `workspace`; then
+ * mlstm_fwd_from_gates runs everything after it (state passing and output) on that
+ * workspace.  Both calls must use the same sizes, chunk, workspace and m_init, in stream
+ * order; C_init and n_init (both NULL or both given) belong to this second call.  Arguments
+ * and outputs are those of mlstm_fwd_chunkwise. */
+mlstm_status mlstm_fwd_from_gates(const void *q, const void *k, const void *v, int B, int NH,
+                                  int S, int DQK, int DV, int chunk, mlstm_dtype dt,
+                                  const float *C_init, const float *n_init, void *h,
+                                  mlstm_dtype h_dt, float *C_last, float *n_last, float *m_last,
+                                  void *workspace, size_t ws_bytes, void *stream);
+
+/* The inter-chunk recurrence alone (gate preprocessing + state passing), materialising
+ * the state at every chunk boundary:
+ *   C_states [B, NH, NC+1, DV, DQK], n_states [B, NH, NC+1, DQK], m_states [B, NH, NC+1]
+ * with NC = S / chunk; entry j is the state after j*chunk tokens (entry 0 = the initial
+ * state, entry NC = the final state).  Other arguments as for mlstm_fwd_chunkwise. */
+mlstm_status mlstm_fwd_chunk_states(const void *k, const void *v, const float *igate_pre,
+                                    const float *fgate_pre, int B, int NH, int S, int DQK,
+                                    int DV, int chunk, mlstm_dtype dt, const float *C_init,
+                                    const float *n_init, const float *m_init, float *C_states,
+                                    float *n_states, float *m_states, void *workspace,
+                                    size_t ws_bytes, void *stream);
+
+/* Gate preprocessing alone (kernel a): fills `workspace` with the per-token gate prefix
+ * quantities and the per-chunk stabiliser (the input of mlstm_fwd_from_gates), and writes
+ * the stabiliser m_t of every token, m_tok [B, NH, S], and of every chunk boundary,
+ * m_states [B, NH, NC+1] (entry 0 = m_init or 0).  Either output may be NULL.  The
+ * workspace must hold at least mlstm_fwd_workspace_bytes(B, NH, S, 32, 32, chunk, dt). */
+mlstm_status mlstm_fwd_gates(const float *igate_pre, const float *fgate_pre, int B, int NH,
+                             int S, int chunk, const float *m_init, float *m_tok,
+                             float *m_states, void *workspace, size_t ws_bytes, void *stream);
+
+/* One recurrent decode step for every (batch, head), in place (section 5 "Inference
+ * Memory and Throughput Trade-Offs"; section 2 stabiliser; section 3 updates):
+ *   q, k [B, NH, DQK] (dt), v [B, NH, DV] (dt), ig, fg [B, NH] float32 pre-activations
+ *   C [B, NH, DV, DQK], n [B, NH, DQK], m [B, NH] float32: read, then overwritten with
+ *       the state after this token
+ *   h [B, NH, DV] (h_dt) output. */
+mlstm_status mlstm_step(const void *q, const void *k, const void *v, const float *ig,
+                        const float *fg, float *C, float *n, float *m, void *h, int B, int NH,
+                        int DQK, int DV, mlstm_dtype dt, mlstm_dtype h_dt, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLSTM_B300_H */

@@ -1,0 +1,66 @@
+"""Build step of the CUDA library: compiles csrc/*.cu for sm_103a with nvcc into
+libmlstm_b300.so inside the package (in-tree, so it travels with the source tree).
+
+    python -m mlstm_matrix_memory_02_b300.build        # incremental
+    python -m mlstm_matrix_memory_02_b300.build --clean
+"""
+from __future__ import annotations
+
+import glob
+import os
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+OBJ = os.path.join(ROOT, "_build", "obj")
+LIB = os.path.join(PKG, "libmlstm_b300.so")
+NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
+         "--expt-relaxed-constexpr", f"-I{os.path.join(ROOT, 'include')}"]
+
+
+def _headers():
+    return glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(ROOT, "include", "*.h"))
+
+
+def _compile(src: str, verbose_ptxas: bool) -> str:
+    obj = os.path.join(OBJ, os.path.basename(src)[:-3] + ".o")
+    newest_dep = max(os.path.getmtime(p) for p in [src, __file__, *_headers()])
+    if os.path.exists(obj) and os.path.getmtime(obj) >= newest_dep and not verbose_ptxas:
+        return obj
+    cmd = [NVCC, *ARCH, *FLAGS, "-c", src, "-o", obj]
+    if verbose_ptxas:
+        cmd += ["-Xptxas", "-v"]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError(f"nvcc failed for {src}:\n{' '.join(cmd)}\n{res.stdout}\n{res.stderr}")
+    if verbose_ptxas:
+        sys.stderr.write(res.stderr)
+    return obj
+
+
+def build(verbose_ptxas: bool = False, clean: bool = False) -> str:
+    """Compile every kernel source and link the shared library; returns its path."""
+    os.makedirs(OBJ, exist_ok=True)
+    if clean:
+        for f in glob.glob(os.path.join(OBJ, "*.o")):
+            os.remove(f)
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), srcs))
+    if (not os.path.exists(LIB) or clean
+            or max(os.path.getmtime(o) for o in objs) > os.path.getmtime(LIB)):
+        cmd = [NVCC, *ARCH, "-shared", "-cudart", "shared", "-Xlinker",
+               "-rpath,/usr/local/cuda/lib64", "-o", LIB, *objs]
+        res = subprocess.run(cmd, capture_output=True, text=True)
+        if res.returncode != 0:
+            raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{res.stdout}\n{res.stderr}")
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(verbose_ptxas="-v" in sys.argv, clean="--clean" in sys.argv))

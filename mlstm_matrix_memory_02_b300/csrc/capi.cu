@@ -1,0 +1,279 @@
+// capi.cu -- the extern "C" boundary of the mLSTM library: argument checks, workspace
+// layout and kernel launches.  Declarations and their contracts are in include/mlstm.h.
+#include <stdint.h>
+
+#include "../../include/mlstm.h"
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace mlstm {
+
+__global__ void copy_chunk_m_kernel(const float *__restrict__ cm, int P, int NC, float *__restrict__ m_last) {
+  const int p = blockIdx.x * blockDim.x + threadIdx.x;
+  if (p < P) m_last[p] = cm[(size_t)p * (NC + 1) + NC];
+}
+
+cudaError_t launch_copy_chunk_m(const float *cm, int P, int NC, float *m_last, cudaStream_t stream) {
+  if (P == 0) return cudaSuccess;
+  copy_chunk_m_kernel<<<(P + 255) / 256, 256, 0, stream>>>(cm, P, NC, m_last);
+  return cudaGetLastError();
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxPairs = 65535;  // grid.z limit of the output kernel
+
+inline size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+  size_t gb, gx, gu, cm, Cs, ns, gates_end, total;
+};
+
+bool sizes_ok(int B, int NH, int S, int DQK, int DV, int chunk) {
+  if (B < 1 || NH < 1 || S < 0) return false;
+  if ((long long)B * NH > kMaxPairs) return false;
+  if (chunk != 16 && chunk != 32 && chunk != 64 && chunk != 128) return false;
+  if (S % chunk != 0) return false;
+  if (DQK < 32 || DQK > 512 || DQK % 32 != 0) return false;
+  if (DV < 32 || DV > 512 || DV % 32 != 0) return false;
+  if ((long long)B * NH * S > (1LL << 40)) return false;
+  return true;
+}
+
+Layout layout(int B, int NH, int S, int DQK, int DV, int chunk) {
+  const size_t P = (size_t)B * NH, NC = (size_t)S / chunk;
+  Layout L{};
+  size_t off = 0;
+  L.gb = off; off = round_up(off + P * S * sizeof(float));
+  L.gx = off; off = round_up(off + P * S * sizeof(float));
+  L.gu = off; off = round_up(off + P * S * sizeof(float));
+  L.cm = off; off = round_up(off + P * (NC + 1) * sizeof(float));
+  L.gates_end = off;
+  L.Cs = off; off = round_up(off + P * (NC + 1) * DV * DQK * sizeof(float));
+  L.ns = off; off = round_up(off + P * (NC + 1) * DQK * sizeof(float));
+  L.total = off;
+  return L;
+}
+
+inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+thread_local int g_last_cuda_error = 0;
+unsigned long long g_launches = 0;  // kernels launched by this library (all host threads)
+
+mlstm_status launch_status(cudaError_t e, int kernels = 1) {
+  if (e == cudaSuccess) {
+    __atomic_fetch_add(&g_launches, (unsigned long long)kernels, __ATOMIC_RELAXED);
+    return MLSTM_OK;
+  }
+  g_last_cuda_error = (int)e;
+  return MLSTM_ERR_LAUNCH;
+}
+
+mlstm_status check_device() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return MLSTM_ERR_DEVICE; }
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MLSTM_ERR_DEVICE;
+  }
+  if (major != 10 || minor != 3) return MLSTM_ERR_DEVICE;
+  return MLSTM_OK;
+}
+
+}  // namespace
+}  // namespace mlstm
+
+using namespace mlstm;
+
+extern "C" {
+
+const char *mlstm_status_str(mlstm_status s) {
+  switch (s) {
+    case MLSTM_OK: return "MLSTM_OK";
+    case MLSTM_ERR_NULL: return "MLSTM_ERR_NULL: a required pointer is NULL";
+    case MLSTM_ERR_ALIGN: return "MLSTM_ERR_ALIGN: a pointer is not 16-byte aligned";
+    case MLSTM_ERR_SHAPE: return "MLSTM_ERR_SHAPE: unsupported sizes (S % chunk, chunk, DQK/DV range)";
+    case MLSTM_ERR_DTYPE: return "MLSTM_ERR_DTYPE: unsupported dtype code";
+    case MLSTM_ERR_WORKSPACE: return "MLSTM_ERR_WORKSPACE: workspace too small";
+    case MLSTM_ERR_LAUNCH: return "MLSTM_ERR_LAUNCH: a kernel launch failed";
+    case MLSTM_ERR_TIMEOUT: return "MLSTM_ERR_TIMEOUT: a bounded device-side wait gave up";
+    case MLSTM_ERR_DEVICE: return "MLSTM_ERR_DEVICE: no usable sm_103 device";
+  }
+  return "MLSTM_ERR_UNKNOWN";
+}
+
+// CUDA error code of the last failed launch on this host thread (0 if none).
+int mlstm_last_cuda_error(void) { return g_last_cuda_error; }
+
+unsigned long long mlstm_kernel_launches(void) { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
+
+size_t mlstm_fwd_workspace_bytes(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) {
+  if (dt != MLSTM_F32 && dt != MLSTM_BF16) return 0;
+  if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return 0;
+  return layout(B, NH, S, DQK, DV, chunk).total;
+}
+
+static mlstm_status check_init(const float *C_init, const float *n_init, const float *m_init) {
+  const int given = (C_init != nullptr) + (n_init != nullptr) + (m_init != nullptr);
+  if (given != 0 && given != 3) return MLSTM_ERR_NULL;
+  if (given && (!aligned16(C_init) || !aligned16(n_init) || !aligned16(m_init))) return MLSTM_ERR_ALIGN;
+  return MLSTM_OK;
+}
+
+static mlstm_status check_fwd_args(const void *q, const void *k, const void *v, int B, int NH, int S,
+                                   int DQK, int DV, int chunk, mlstm_dtype dt, const float *C_init,
+                                   const float *n_init, const void *h, mlstm_dtype h_dt,
+                                   const float *C_last, const float *n_last, const float *m_last,
+                                   const void *workspace, size_t ws_bytes) {
+  if (dt != MLSTM_F32 && dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
+  if (h_dt != MLSTM_F32 && h_dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
+  if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return MLSTM_ERR_SHAPE;
+  // per-token arrays may be NULL for an empty sequence (zero-size tensors have no storage)
+  if (S > 0 && (!q || !k || !v || !h)) return MLSTM_ERR_NULL;
+  if (!C_last || !n_last || !m_last || !workspace) return MLSTM_ERR_NULL;
+  if ((C_init == nullptr) != (n_init == nullptr)) return MLSTM_ERR_NULL;
+  for (const void *ptr : {q, k, v, h, (const void *)C_last, (const void *)n_last, (const void *)m_last, workspace})
+    if (!aligned16(ptr)) return MLSTM_ERR_ALIGN;
+  if ((C_init && !aligned16(C_init)) || (n_init && !aligned16(n_init))) return MLSTM_ERR_ALIGN;
+  if (ws_bytes < layout(B, NH, S, DQK, DV, chunk).total) return MLSTM_ERR_WORKSPACE;
+  return MLSTM_OK;
+}
+
+// Everything after kernel (a), on a workspace that kernel (a) has filled for these sizes.
+static mlstm_status run_from_gates(const void *q, const void *k, const void *v, int B, int NH, int S,
+                                   int DQK, int DV, int chunk, mlstm_dtype dt, const float *C_init,
+                                   const float *n_init, void *h, mlstm_dtype h_dt, float *C_last,
+                                   float *n_last, float *m_last, void *workspace, cudaStream_t s) {
+  const Layout Lw = layout(B, NH, S, DQK, DV, chunk);
+  char *ws = (char *)workspace;
+  float *gb = (float *)(ws + Lw.gb), *gx = (float *)(ws + Lw.gx), *gu = (float *)(ws + Lw.gu);
+  float *cm = (float *)(ws + Lw.cm), *Cs = (float *)(ws + Lw.Cs), *ns = (float *)(ws + Lw.ns);
+  const int P = B * NH, NC = S / chunk;
+  const bool bf16 = dt == MLSTM_BF16;
+  if (mlstm_status st = launch_status(launch_states_simt(k, v, bf16, gb, gx, cm, P, S, chunk, DQK, DV, C_init,
+                                                         n_init, Cs, ns, C_last, n_last, s)))
+    return st;
+  if (S > 0) {
+    if (mlstm_status st = launch_status(launch_output_simt(q, k, v, bf16, h_dt == MLSTM_BF16, gb, gx, gu, cm,
+                                                           Cs, ns, P, S, chunk, DQK, DV, h, s)))
+      return st;
+  }
+  return launch_status(launch_copy_chunk_m(cm, P, NC, m_last, s));
+}
+
+mlstm_status mlstm_fwd_from_gates(const void *q, const void *k, const void *v, int B, int NH, int S,
+                                  int DQK, int DV, int chunk, mlstm_dtype dt, const float *C_init,
+                                  const float *n_init, void *h, mlstm_dtype h_dt, float *C_last,
+                                  float *n_last, float *m_last, void *workspace, size_t ws_bytes,
+                                  void *stream) {
+  if (mlstm_status st = check_fwd_args(q, k, v, B, NH, S, DQK, DV, chunk, dt, C_init, n_init, h, h_dt,
+                                       C_last, n_last, m_last, workspace, ws_bytes))
+    return st;
+  if (mlstm_status st = check_device()) return st;
+  return run_from_gates(q, k, v, B, NH, S, DQK, DV, chunk, dt, C_init, n_init, h, h_dt, C_last, n_last,
+                        m_last, workspace, (cudaStream_t)stream);
+}
+
+mlstm_status mlstm_fwd_chunkwise(const void *q, const void *k, const void *v, const float *igate_pre,
+                                 const float *fgate_pre, int B, int NH, int S, int DQK, int DV,
+                                 int chunk, mlstm_dtype dt, const float *C_init, const float *n_init,
+                                 const float *m_init, void *h, mlstm_dtype h_dt, float *C_last,
+                                 float *n_last, float *m_last, void *workspace, size_t ws_bytes,
+                                 void *stream) {
+  if (mlstm_status st = check_fwd_args(q, k, v, B, NH, S, DQK, DV, chunk, dt, C_init, n_init, h, h_dt,
+                                       C_last, n_last, m_last, workspace, ws_bytes))
+    return st;
+  if (S > 0 && (!igate_pre || !fgate_pre)) return MLSTM_ERR_NULL;
+  if (mlstm_status st = check_init(C_init, n_init, m_init)) return st;
+  if (!aligned16(igate_pre) || !aligned16(fgate_pre)) return MLSTM_ERR_ALIGN;
+  if (mlstm_status st = check_device()) return st;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  const Layout Lw = layout(B, NH, S, DQK, DV, chunk);
+  char *ws = (char *)workspace;
+  const int P = B * NH;
+  if (mlstm_status st = launch_status(launch_gates(igate_pre, fgate_pre, P, S, chunk, m_init, (float *)(ws + Lw.gb),
+                                                   (float *)(ws + Lw.gx), (float *)(ws + Lw.gu),
+                                                   (float *)(ws + Lw.cm), nullptr, s)))
+    return st;
+  return run_from_gates(q, k, v, B, NH, S, DQK, DV, chunk, dt, C_init, n_init, h, h_dt, C_last, n_last,
+                        m_last, workspace, s);
+}
+
+mlstm_status mlstm_fwd_chunk_states(const void *k, const void *v, const float *igate_pre,
+                                    const float *fgate_pre, int B, int NH, int S, int DQK, int DV,
+                                    int chunk, mlstm_dtype dt, const float *C_init, const float *n_init,
+                                    const float *m_init, float *C_states, float *n_states,
+                                    float *m_states, void *workspace, size_t ws_bytes, void *stream) {
+  if (dt != MLSTM_F32 && dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
+  if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return MLSTM_ERR_SHAPE;
+  if (S > 0 && (!k || !v || !igate_pre || !fgate_pre)) return MLSTM_ERR_NULL;
+  if (!C_states || !n_states || !m_states || !workspace) return MLSTM_ERR_NULL;
+  if (mlstm_status st = check_init(C_init, n_init, m_init)) return st;
+  for (const void *ptr : {(const void *)k, (const void *)v, (const void *)igate_pre, (const void *)fgate_pre,
+                          (const void *)C_states, (const void *)n_states, (const void *)m_states,
+                          (const void *)workspace})
+    if (!aligned16(ptr)) return MLSTM_ERR_ALIGN;
+  const Layout Lw = layout(B, NH, S, DQK, DV, chunk);
+  if (ws_bytes < Lw.total) return MLSTM_ERR_WORKSPACE;
+  if (mlstm_status st = check_device()) return st;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  char *ws = (char *)workspace;
+  float *gb = (float *)(ws + Lw.gb), *gx = (float *)(ws + Lw.gx), *gu = (float *)(ws + Lw.gu);
+  float *cm = (float *)(ws + Lw.cm);
+  const int P = B * NH, NC = S / chunk;
+  if (mlstm_status st = launch_status(launch_gates(igate_pre, fgate_pre, P, S, chunk, m_init, gb, gx, gu, cm, nullptr, s)))
+    return st;
+  if (mlstm_status st = launch_status(launch_states_simt(k, v, dt == MLSTM_BF16, gb, gx, cm, P, S, chunk, DQK,
+                                                         DV, C_init, n_init, C_states, n_states, nullptr,
+                                                         nullptr, s)))
+    return st;
+  return launch_status(cudaMemcpyAsync(m_states, cm, sizeof(float) * (size_t)P * (NC + 1),
+                                       cudaMemcpyDeviceToDevice, s));
+}
+
+mlstm_status mlstm_fwd_gates(const float *igate_pre, const float *fgate_pre, int B, int NH, int S,
+                             int chunk, const float *m_init, float *m_tok, float *m_states,
+                             void *workspace, size_t ws_bytes, void *stream) {
+  if (!sizes_ok(B, NH, S, 32, 32, chunk)) return MLSTM_ERR_SHAPE;
+  if ((S > 0 && (!igate_pre || !fgate_pre)) || !workspace) return MLSTM_ERR_NULL;
+  for (const void *ptr : {(const void *)igate_pre, (const void *)fgate_pre, (const void *)workspace})
+    if (!aligned16(ptr)) return MLSTM_ERR_ALIGN;
+  if ((m_init && !aligned16(m_init)) || (m_tok && !aligned16(m_tok)) || (m_states && !aligned16(m_states)))
+    return MLSTM_ERR_ALIGN;
+  const Layout Lw = layout(B, NH, S, 32, 32, chunk);
+  if (ws_bytes < Lw.gates_end) return MLSTM_ERR_WORKSPACE;
+  if (mlstm_status st = check_device()) return st;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  char *ws = (char *)workspace;
+  float *gb = (float *)(ws + Lw.gb), *gx = (float *)(ws + Lw.gx), *gu = (float *)(ws + Lw.gu);
+  float *cm = (float *)(ws + Lw.cm);
+  const int P = B * NH, NC = S / chunk;
+  if (mlstm_status st = launch_status(launch_gates(igate_pre, fgate_pre, P, S, chunk, m_init, gb, gx, gu, cm, m_tok, s)))
+    return st;
+  if (m_states)
+    return launch_status(cudaMemcpyAsync(m_states, cm, sizeof(float) * (size_t)P * (NC + 1),
+                                         cudaMemcpyDeviceToDevice, s));
+  return MLSTM_OK;
+}
+
+mlstm_status mlstm_step(const void *q, const void *k, const void *v, const float *ig, const float *fg,
+                        float *C, float *n, float *m, void *h, int B, int NH, int DQK, int DV,
+                        mlstm_dtype dt, mlstm_dtype h_dt, void *stream) {
+  if (dt != MLSTM_F32 && dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
+  if (h_dt != MLSTM_F32 && h_dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
+  if (!sizes_ok(B, NH, 0, DQK, DV, 16)) return MLSTM_ERR_SHAPE;
+  if (!q || !k || !v || !ig || !fg || !C || !n || !m || !h) return MLSTM_ERR_NULL;
+  for (const void *ptr : {(const void *)q, (const void *)k, (const void *)v, (const void *)ig, (const void *)fg,
+                          (const void *)C, (const void *)n, (const void *)m, (const void *)h})
+    if (!aligned16(ptr)) return MLSTM_ERR_ALIGN;
+  if (mlstm_status st = check_device()) return st;
+  return launch_status(launch_step(q, k, v, dt == MLSTM_BF16, h_dt == MLSTM_BF16, ig, fg, C, n, m, h,
+                                   B * NH, DQK, DV, (cudaStream_t)stream));
+}
+
+}  // extern "C"

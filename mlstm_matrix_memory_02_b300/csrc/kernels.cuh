@@ -1,0 +1,33 @@
+// kernels.cuh -- launch wrappers of the mLSTM kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace mlstm {
+
+// (a) gate preprocessing: per-token b, x, u [P, S] and per-chunk m [P, NC+1].
+cudaError_t launch_gates(const float *ig, const float *fg, int P, int S, int L, const float *m_init,
+                         float *gb, float *gx, float *gu, float *cm, float *m_tok,
+                         cudaStream_t stream);
+
+// (b) inter-chunk recurrence on CUDA cores; Cs/ns [P, NC+1, ...] (optional) and the final state.
+cudaError_t launch_states_simt(const void *k, const void *v, bool bf16, const float *gb,
+                               const float *gx, const float *cm, int P, int S, int L, int DQK,
+                               int DV, const float *C_init, const float *n_init, float *Cs,
+                               float *ns, float *C_last, float *n_last, cudaStream_t stream);
+
+// (c) intra-chunk output on CUDA cores, reading the entering states Cs/ns.
+cudaError_t launch_output_simt(const void *q, const void *k, const void *v, bool bf16, bool out_bf16,
+                               const float *gb, const float *gx, const float *gu, const float *cm,
+                               const float *Cs, const float *ns, int P, int S, int L, int DQK, int DV,
+                               void *h, cudaStream_t stream);
+
+// (d) single decode step, in place.
+cudaError_t launch_step(const void *q, const void *k, const void *v, bool bf16, bool out_bf16,
+                        const float *ig, const float *fg, float *C, float *n, float *m, void *h,
+                        int P, int DQK, int DV, cudaStream_t stream);
+
+// small helpers
+cudaError_t launch_copy_chunk_m(const float *cm, int P, int NC, float *m_last, cudaStream_t stream);
+
+}  // namespace mlstm

@@ -49,7 +49,7 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     i = ctypes.c_int
     lib.oracle_mlstm_recurrent.restype = i
     lib.oracle_mlstm_recurrent.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, dp, dp, dp,
-                                           dp, dp, dp, dp, dp, i, dp, dp, dp, i]
+                                           dp, dp, dp, dp, dp, dp, dp, i, dp, dp, dp, i]
     lib.oracle_mlstm_unstabilised.restype = i
     lib.oracle_mlstm_unstabilised.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, dp, dp, dp, i]
     lib.oracle_mlstm_parallel.restype = i
@@ -90,13 +90,14 @@ def _shapes(q, k, v, ig, fg):
 
 
 def recurrent(q, k, v, ig, fg, C0=None, n0=None, m0=None, snap_every=0, want_h=True,
-              want_m_tok=False, nthreads=0, lib=None):
+              want_m_tok=False, want_den=False, nthreads=0, lib=None):
     """Stabilised step-by-step mLSTM in fp64.
 
     Returns a dict with ``h`` [B,NH,S,DV] (unless want_h is False), the final state ``C``
     [B,NH,DV,DQK], ``n`` [B,NH,DQK], ``m`` [B,NH]; ``m_tok`` [B,NH,S] if asked; and, when
     ``snap_every`` > 0, ``C_snap``/``n_snap``/``m_snap`` holding the state at
     t = 0, snap_every, ..., S (the state entering each chunk, then the final one).
+    ``want_den`` adds ``den_tok`` (n_t.q_t) and ``dabs_tok`` (sum_c |q_c| nabs_c) [B,NH,S].
     """
     lib = lib or load()
     q, k, v, ig, fg = (_f64(x) for x in (q, k, v, ig, fg))
@@ -113,6 +114,9 @@ def recurrent(q, k, v, ig, fg, C0=None, n0=None, m0=None, snap_every=0, want_h=T
         out["h"] = np.empty((B, NH, S, DV))
     if want_m_tok:
         out["m_tok"] = np.empty((B, NH, S))
+    if want_den:
+        out["den_tok"] = np.empty((B, NH, S))
+        out["dabs_tok"] = np.empty((B, NH, S))
     if snap_every > 0:
         if S % snap_every:
             raise ValueError("snap_every must divide S")
@@ -123,7 +127,8 @@ def recurrent(q, k, v, ig, fg, C0=None, n0=None, m0=None, snap_every=0, want_h=T
     rc = lib.oracle_mlstm_recurrent(
         _ptr(q), _ptr(k), _ptr(v), _ptr(ig), _ptr(fg), B, NH, S, DQK, DV,
         _ptr(C0), _ptr(n0), _ptr(m0), _ptr(out.get("h")), _ptr(out["C"]), _ptr(out["n"]),
-        _ptr(out["m"]), _ptr(out.get("m_tok")), int(snap_every), _ptr(out.get("C_snap")),
+        _ptr(out["m"]), _ptr(out.get("m_tok")), _ptr(out.get("den_tok")),
+        _ptr(out.get("dabs_tok")), int(snap_every), _ptr(out.get("C_snap")),
         _ptr(out.get("n_snap")), _ptr(out.get("m_snap")), int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_mlstm_recurrent rejected its arguments (code {rc})")

@@ -38,7 +38,7 @@
 typedef struct {
   const double *q, *k, *v, *ig, *fg;
   const double *C0, *n0, *m0;
-  double *h, *C_out, *n_out, *m_out, *m_tok;
+  double *h, *C_out, *n_out, *m_out, *m_tok, *den_tok, *dabs_tok;
   double *C_snap, *n_snap, *m_snap;
   int B, NH, S, DQK, DV, snap_every;
   int kind; /* 0 = stabilised recurrent, 1 = unstabilised recurrent, 2 = parallel dual form */
@@ -66,12 +66,15 @@ static void recurrent_pair(const job_t *J, int pair) {
 
   double *C = (double *)malloc(sizeof(double) * (size_t)DV * DQK);
   double *n = (double *)malloc(sizeof(double) * DQK);
+  double *nabs = (double *)calloc(DQK, sizeof(double)); /* same recurrence with |k_t| */
   double *khat = (double *)malloc(sizeof(double) * DQK);
   double m;
   if (J->C0) memcpy(C, J->C0 + (size_t)pair * DV * DQK, sizeof(double) * (size_t)DV * DQK);
   else memset(C, 0, sizeof(double) * (size_t)DV * DQK);
   if (J->n0) memcpy(n, J->n0 + (size_t)pair * DQK, sizeof(double) * DQK);
   else memset(n, 0, sizeof(double) * DQK);
+  if (J->n0)
+    for (int c = 0; c < DQK; ++c) nabs[c] = fabs(n[c]);
   m = J->m0 ? J->m0[pair] : 0.0;
 
   const int nsnap = J->snap_every > 0 ? S / J->snap_every + 1 : 0;
@@ -109,6 +112,8 @@ static void recurrent_pair(const job_t *J, int pair) {
     }
     /* n_t = f_t n_{t-1} + i_t k_t */
     for (int c = 0; c < DQK; ++c) n[c] = fgate * n[c] + igate * khat[c];
+    /* the same weights applied to |k_t|: sum_c nabs_c |q_c| bounds the terms of n_t^T q_t */
+    for (int c = 0; c < DQK; ++c) nabs[c] = fgate * nabs[c] + igate * fabs(khat[c]);
 
     if (J->m_tok) J->m_tok[(size_t)pair * S + t] = m;
 
@@ -118,6 +123,12 @@ static void recurrent_pair(const job_t *J, int pair) {
       for (int c = 0; c < DQK; ++c) nq += n[c] * qt[c];
       const double floor_ = (J->kind == 0) ? exp(-m) : 1.0;
       const double den = fmax(fabs(nq), floor_);
+      if (J->den_tok) J->den_tok[(size_t)pair * S + t] = nq;
+      if (J->dabs_tok) {
+        double da = 0.0;
+        for (int c = 0; c < DQK; ++c) da += nabs[c] * fabs(qt[c]);
+        J->dabs_tok[(size_t)pair * S + t] = da;
+      }
       for (int a = 0; a < DV; ++a) {
         const double *row = C + (size_t)a * DQK;
         double acc = 0.0;
@@ -131,6 +142,7 @@ static void recurrent_pair(const job_t *J, int pair) {
   if (J->m_out) J->m_out[pair] = (J->kind == 0) ? m : 0.0;
   free(C);
   free(n);
+  free(nabs);
   free(khat);
 }
 
@@ -199,6 +211,9 @@ static int run(job_t *J, int nthreads) {
 
 /* Stabilised recurrent mLSTM (the definition).  C0/n0/m0 may be NULL for the zero state
  * (m_0 = 0).  Any output pointer may be NULL.  m_tok [B,NH,S] receives m_t per token.
+ * den_tok [B,NH,S] receives n_t^T q_t and dabs_tok [B,NH,S] receives sum_c |q_c| nabs_c,
+ * where nabs follows the n recurrence with |k_t| (and |n_0|): the magnitude of the terms
+ * the denominator sums, so dabs / max(|den|, exp(-m)) is its condition number.
  * If snap_every > 0 (must divide S), C_snap [B,NH,S/snap_every+1,DV,DQK], n_snap and
  * m_snap receive the state at t = 0, snap_every, 2*snap_every, ..., S.
  * Returns 0 on success, nonzero on a bad argument.  nthreads <= 0 uses every core. */
@@ -206,13 +221,14 @@ int oracle_mlstm_recurrent(const double *q, const double *k, const double *v, co
                            const double *fg, int B, int NH, int S, int DQK, int DV,
                            const double *C0, const double *n0, const double *m0, double *h,
                            double *C_out, double *n_out, double *m_out, double *m_tok,
-                           int snap_every, double *C_snap, double *n_snap, double *m_snap,
-                           int nthreads) {
+                           double *den_tok, double *dabs_tok, int snap_every, double *C_snap,
+                           double *n_snap, double *m_snap, int nthreads) {
   job_t J;
   memset(&J, 0, sizeof(J));
   J.q = q; J.k = k; J.v = v; J.ig = ig; J.fg = fg;
   J.C0 = C0; J.n0 = n0; J.m0 = m0;
   J.h = h; J.C_out = C_out; J.n_out = n_out; J.m_out = m_out; J.m_tok = m_tok;
+  J.den_tok = den_tok; J.dabs_tok = dabs_tok;
   J.C_snap = C_snap; J.n_snap = n_snap; J.m_snap = m_snap;
   J.B = B; J.NH = NH; J.S = S; J.DQK = DQK; J.DV = DV; J.snap_every = snap_every;
   J.kind = 0;

@@ -214,6 +214,28 @@ def pin_causality_and_linearity(lib):
     return ok, f"causal {causal}, later rows changed {changed}, linearity err {lin:.3e}"
 
 
+def pin_denominator_brute_force(lib):
+    """n_t.q_t and its absolute-term sum, brute force from the unrolled sum (section 3):
+    n_t q_t = e^{-m_t} sum_{j<=t} (prod_{tau=j+1..t} f_tau) i_j (q_t . k_j) and the same
+    with |q_t| . |k_j|; m_t from the pinned stabiliser output."""
+    q, k, v, ig, fg = rand_inputs(1, 2, 18, 5, 3, 13, ig=(0.0, 1.5), fg=(0.5, 1.5))
+    out = oracle.recurrent(q, k, v, ig, fg, want_m_tok=True, want_den=True, lib=lib)
+    kh = k / np.sqrt(q.shape[-1])
+    f = 1.0 / (1.0 + np.exp(-fg))
+    err = 0.0
+    for h_ in range(2):
+        for t in range(q.shape[2]):
+            den = dab = 0.0
+            for j in range(t + 1):
+                w = np.exp(ig[0, h_, j]) * np.prod(f[0, h_, j + 1: t + 1])
+                den += w * float(q[0, h_, t] @ kh[0, h_, j])
+                dab += w * float(np.abs(q[0, h_, t]) @ np.abs(kh[0, h_, j]))
+            e = np.exp(-out["m_tok"][0, h_, t])
+            err = max(err, abs(out["den_tok"][0, h_, t] - den * e) / (dab * e),
+                      abs(out["dabs_tok"][0, h_, t] - dab * e) / (dab * e))
+    return err <= 1e-13, f"denominator brute force err {err:.3e}"
+
+
 ALL_PINS = [
     pin_recurrent_equals_parallel,
     pin_stabiliser_is_a_rescaling,
@@ -225,6 +247,7 @@ ALL_PINS = [
     pin_split_sequence,
     pin_snapshots,
     pin_causality_and_linearity,
+    pin_denominator_brute_force,
 ]
 
 

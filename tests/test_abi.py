@@ -1,0 +1,134 @@
+"""CPU tests of the C ABI: the library builds for sm_103a, loads, exports every entry point
+declared in include/mlstm.h, and rejects bad arguments on the host before any launch.
+
+No GPU is needed and no kernel is launched: every call here fails argument validation,
+which runs before the library touches the device.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mlstm.h")
+
+OK, ERR_NULL, ERR_ALIGN, ERR_SHAPE, ERR_DTYPE, ERR_WS, ERR_LAUNCH, ERR_TIMEOUT, ERR_DEVICE = range(9)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mlstm_matrix_memory_02_b300 import build
+    build.build()
+    from mlstm_matrix_memory_02_b300 import binding
+    return binding.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mlstm_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("mlstm_fwd_chunkwise", "mlstm_step", "mlstm_fwd_workspace_bytes",
+                     "mlstm_status_str"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from mlstm_matrix_memory_02_b300 import binding
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in mlstm.h but not exported"
+    assert sorted(binding.EXPORTED) == declared_functions()
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        s = lib.mlstm_status_str(code)
+        assert s and s.startswith(b"MLSTM_")
+    assert lib.mlstm_status_str(99) == b"MLSTM_ERR_UNKNOWN"
+
+
+def test_workspace_bytes(lib):
+    ws = lib.mlstm_fwd_workspace_bytes
+    assert ws(4, 4, 2048, 512, 512, 64, 1) > 0
+    # gate arrays (3 x P x S fp32) + chunk m + boundary states (P x (NC+1) x DV x DQK fp32)
+    P, S, NC = 16, 2048, 32
+    need = 3 * P * S * 4 + P * (NC + 1) * 4 + P * (NC + 1) * 512 * 512 * 4 + P * (NC + 1) * 512 * 4
+    assert ws(4, 4, 2048, 512, 512, 64, 1) >= need
+    assert ws(1, 1, 100, 64, 64, 64, 1) == 0      # S % chunk != 0
+    assert ws(1, 1, 128, 48, 64, 64, 1) == 0      # DQK not a multiple of 32
+    assert ws(1, 1, 128, 64, 1024, 64, 1) == 0    # DV above 512
+    assert ws(1, 1, 128, 64, 64, 48, 1) == 0      # chunk not in {16,32,64,128}
+    assert ws(1, 1, 128, 64, 64, 64, 7) == 0      # bad dtype code
+    assert ws(1, 1, 0, 64, 64, 64, 0) > 0         # empty sequence is allowed
+
+
+FAKE = 0x100000  # 16-byte aligned, never dereferenced: every call below fails validation
+
+
+def _fwd(lib, q=FAKE, ws=FAKE, ws_bytes=1 << 40, S=128, DQK=64, DV=64, chunk=64, dt=1, hdt=0,
+         init=(None, None, None), last=(FAKE, FAKE, FAKE)):
+    p = ctypes.c_void_p
+    return lib.mlstm_fwd_chunkwise(p(q), p(FAKE), p(FAKE), p(FAKE), p(FAKE), 1, 2, S, DQK, DV,
+                                   chunk, dt, p(init[0]), p(init[1]), p(init[2]), p(FAKE), hdt,
+                                   p(last[0]), p(last[1]), p(last[2]), p(ws),
+                                   ctypes.c_size_t(ws_bytes), p(None))
+
+
+def test_fwd_argument_errors(lib):
+    assert _fwd(lib, dt=5) == ERR_DTYPE
+    assert _fwd(lib, hdt=9) == ERR_DTYPE
+    assert _fwd(lib, S=100) == ERR_SHAPE
+    assert _fwd(lib, DQK=40) == ERR_SHAPE
+    assert _fwd(lib, chunk=256) == ERR_SHAPE
+    assert _fwd(lib, q=None) == ERR_NULL
+    assert _fwd(lib, last=(FAKE, None, FAKE)) == ERR_NULL
+    assert _fwd(lib, init=(FAKE, None, None)) == ERR_NULL  # all three or none
+    assert _fwd(lib, q=FAKE + 4) == ERR_ALIGN
+    assert _fwd(lib, init=(FAKE, FAKE + 8, FAKE)) == ERR_ALIGN
+    assert _fwd(lib, ws_bytes=16) == ERR_WS
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device status")
+def test_fwd_without_device(lib):
+    assert _fwd(lib) == ERR_DEVICE
+
+
+def test_step_argument_errors(lib):
+    p = ctypes.c_void_p
+
+    def step(q=FAKE, DQK=64, DV=64, dt=1, hdt=1):
+        return lib.mlstm_step(p(q), p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE), p(FAKE),
+                              p(FAKE), 2, 2, DQK, DV, dt, hdt, p(None))
+
+    assert step(dt=3) == ERR_DTYPE
+    assert step(DQK=16) == ERR_SHAPE
+    assert step(DV=544) == ERR_SHAPE
+    assert step(q=None) == ERR_NULL
+    assert step(q=FAKE + 2) == ERR_ALIGN
+
+
+def test_states_and_gates_argument_errors(lib):
+    p = ctypes.c_void_p
+    r = lib.mlstm_fwd_chunk_states(p(FAKE), p(FAKE), p(FAKE), p(FAKE), 1, 1, 96, 64, 64, 64, 1,
+                                   p(None), p(None), p(None), p(FAKE), p(FAKE), p(FAKE), p(FAKE),
+                                   ctypes.c_size_t(1 << 40), p(None))
+    assert r == ERR_SHAPE
+    r = lib.mlstm_fwd_gates(p(FAKE), p(None), 1, 1, 128, 64, p(None), p(FAKE), p(FAKE), p(FAKE),
+                            ctypes.c_size_t(1 << 40), p(None))
+    assert r == ERR_NULL
+    r = lib.mlstm_fwd_gates(p(FAKE), p(FAKE), 1, 1, 128, 64, p(None), p(FAKE), p(FAKE), p(FAKE),
+                            ctypes.c_size_t(8), p(None))
+    assert r == ERR_WS
+
+
+def test_binding_rejects_cpu_tensors(lib):
+    from mlstm_matrix_memory_02_b300 import binding
+    x = torch.zeros(1, 1, 64, 32)
+    g = torch.zeros(1, 1, 64)
+    with pytest.raises(TypeError):
+        binding.mlstm_fwd_chunkwise(x, x, x, g, g, 16)

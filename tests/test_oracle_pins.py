@@ -35,6 +35,8 @@ MUTANTS = [
     ("retrieval with k instead of q", "acc += row[c] * qt[c];", "acc += row[c] * kt[c];"),
     ("dual-form decay off by one", "for (int tau = j + 1; tau <= t; ++tau)", "for (int tau = j; tau <= t; ++tau)"),
     ("dual-form missing i_j", "double Stj = exp(ig[j]); /* i_j */", "double Stj = 1.0;"),
+    ("abs normaliser drops |k|", "igate * fabs(khat[c]);", "igate * khat[c];"),
+    ("abs denominator drops |q|", "da += nabs[c] * fabs(qt[c]);", "da += nabs[c] * qt[c];"),
     ("snapshot after the update", "if (J->snap_every > 0 && t % J->snap_every == 0) {",
      "if (J->snap_every > 0 && t % J->snap_every == 0 && t > 0) {"),
 ]

@@ -1,0 +1,362 @@
+"""GPU parity: the CUDA path (called through the C ABI via the thin binding) against the
+fp64 oracle on identical seeded inputs, at every workload's full size and on edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mlstm_matrix_memory_02_b300 import workloads as W
+from parity import (TOL_BF16, TOL_F32, bf16_out_ok, conditioned_ok, rel_err, state_errs)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from mlstm_matrix_memory_02_b300 import binding
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return binding
+
+
+def dev(inp, dtype):
+    """numpy inputs -> CUDA tensors: q, k, v in `dtype`, gates fp32 (values are exact)."""
+    out = {}
+    for key in ("q", "k", "v"):
+        out[key] = torch.from_numpy(inp[key]).to("cuda").to(dtype).contiguous()
+    for key in ("ig", "fg"):
+        out[key] = torch.from_numpy(inp[key]).to("cuda").contiguous()
+    return out
+
+
+def tdt(w):
+    return torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+
+def npy(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def tol_for(w):
+    return TOL_BF16 if w.dtype == "bf16" else TOL_F32
+
+
+def run_fwd(B, w, inp, chunk=None, h_dtype=torch.float32, init=None):
+    d = dev(inp, tdt(w))
+    kw = {}
+    if init is not None:
+        kw = dict(C_init=init[0], n_init=init[1], m_init=init[2])
+    h, C, n, m = B.mlstm_fwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"],
+                                       chunk or w.chunk, h_dtype=h_dtype, **kw)
+    torch.cuda.synchronize()
+    return npy(h), npy(C), npy(n), npy(m)
+
+
+# ----------------------------------------------------------------------------- tiny fp32
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+def test_tiny_fp32_forward(B, chunk):
+    w = W.TINY_F32
+    inp = W.make_inputs(w)
+    ora = oracle.recurrent(**inp)
+    h, C, n, m = run_fwd(B, w, inp, chunk=chunk)
+    assert rel_err(h, ora["h"]) <= TOL_F32
+    eC, en, em = state_errs(C, n, m, ora["C"], ora["n"], ora["m"])
+    assert eC <= TOL_F32 and en <= TOL_F32 and em <= 1e-4, (eC, en, em)
+
+
+# ----------------------------------------------------------------------------- gates
+@pytest.mark.parametrize("name", ["tiny", "350m", "1p3b", "stress"])
+def test_gate_stabiliser(B, name):
+    w = W.WORKLOADS[name]
+    inp = W.make_inputs(w)
+    nh = min(w.NH, 2)
+    sub = {k_: v_[:1, :nh] for k_, v_ in inp.items()}
+    ora = oracle.recurrent(**sub, want_h=False, want_m_tok=True, snap_every=w.chunk)
+    ig = torch.from_numpy(inp["ig"]).cuda()
+    fg = torch.from_numpy(inp["fg"]).cuda()
+    m_tok, m_states = B.mlstm_fwd_gates(ig, fg, w.chunk)
+    torch.cuda.synchronize()
+    m_tok = npy(m_tok)[:1, :nh]
+    m_states = npy(m_states)[:1, :nh]
+    assert np.max(np.abs(m_tok - ora["m_tok"]) / (1 + np.abs(ora["m_tok"]))) <= 1e-4
+    assert np.max(np.abs(m_states - ora["m_snap"]) / (1 + np.abs(ora["m_snap"]))) <= 1e-4
+
+
+# ----------------------------------------------------------------------------- boundary states
+@pytest.mark.parametrize("name", ["tiny", "350m", "stress"])
+def test_chunk_states(B, name):
+    w = W.WORKLOADS[name]
+    inp = W.make_inputs(w)
+    d = dev(inp, tdt(w))
+    Cs, ns, ms = B.mlstm_fwd_chunk_states(d["k"], d["v"], d["ig"], d["fg"], w.chunk)
+    torch.cuda.synchronize()
+    nh = min(w.NH, 2)  # the oracle snapshots two heads of the first batch row
+    sub = {k_: v_[:1, :nh] for k_, v_ in inp.items()}
+    ora = oracle.recurrent(**sub, want_h=False, snap_every=w.chunk)
+    Cs, ns, ms = npy(Cs[:1, :nh]), npy(ns[:1, :nh]), npy(ms[:1, :nh])
+    tol = tol_for(w)
+    for j in range(1, Cs.shape[2]):
+        eC, en, em = state_errs(Cs[:, :, j], ns[:, :, j], ms[:, :, j], ora["C_snap"][:, :, j],
+                                ora["n_snap"][:, :, j], ora["m_snap"][:, :, j])
+        assert eC <= tol and en <= tol and em <= 1e-4, (j, eC, en, em)
+    assert np.all(Cs[:, :, 0] == 0) and np.all(ms[:, :, 0] == 0)
+
+
+# ----------------------------------------------------------------------------- full size
+@pytest.mark.parametrize("name", ["350m", "1p3b"])
+def test_layer_forward_full_size(B, name):
+    w = W.WORKLOADS[name]
+    inp = W.make_inputs(w)
+    ora = oracle.recurrent(**inp)
+    h, C, n, m = run_fwd(B, w, inp)
+    e = rel_err(h, ora["h"])
+    assert e <= TOL_BF16, f"h max-abs/RMS {e:.4g}"
+    eC, en, em = state_errs(C, n, m, ora["C"], ora["n"], ora["m"])
+    assert eC <= TOL_BF16 and en <= TOL_BF16 and em <= 1e-4, (eC, en, em)
+    assert np.all(np.isfinite(h))
+
+
+def test_bf16_output_350m(B):
+    w = W.LAYER_350M
+    inp = W.make_inputs(w)
+    ora = oracle.recurrent(**inp)
+    h, _, _, _ = run_fwd(B, w, inp, h_dtype=torch.bfloat16)
+    ok, worst = bf16_out_ok(h, ora["h"])
+    assert ok, f"bf16 h exceeds its bound by x{worst:.3g}"
+
+
+def test_stress_forward_full_size(B):
+    w = W.STRESS_16K
+    inp = W.make_inputs(w)
+    ora = oracle.recurrent(**inp, want_m_tok=True, want_den=True)
+    h, C, n, m = run_fwd(B, w, inp)
+    assert np.all(np.isfinite(h)), "NaN/Inf in h"
+    # fp32 CUDA-core arithmetic: relative error per summed term <= (terms) * 2^-24
+    u = (w.DQK + w.chunk) * 2.0 ** -24
+    ok, worst, stats = conditioned_ok(h, ora, inp["v"], TOL_BF16, u, u)
+    assert ok, (worst, stats)
+    assert stats["rel_err_kappa_le_100"] <= TOL_BF16, stats
+    eC, en, em = state_errs(C, n, m, ora["C"], ora["n"], ora["m"])
+    assert eC <= TOL_BF16 and en <= TOL_BF16 and em <= 1e-4, (eC, en, em)
+
+
+# ----------------------------------------------------------------------------- decode
+def test_decode_full_size_sampled_heads(B):
+    """B=256, NH=8, d=256, 64 steps on the full batch; the oracle checks 12 sampled heads
+    whose starting state it computed itself (512 prior tokens)."""
+    w = W.DECODE
+    prior, steps = W.make_decode_inputs(w)
+    P = w.B * w.NH
+    rng = np.random.default_rng(123)
+    sample = np.sort(rng.choice(P, 12, replace=False))
+    bi, hi = sample // w.NH, sample % w.NH
+
+    def pick(x):
+        return x[bi, hi][:, None]  # [12, 1, ...] as a batch of 12 single-head rows
+
+    o_prior = oracle.recurrent(**{k_: pick(v_) for k_, v_ in prior.items()}, want_h=False)
+    o_steps = oracle.recurrent(**{k_: pick(v_) for k_, v_ in steps.items()},
+                               C0=o_prior["C"], n0=o_prior["n"], m0=o_prior["m"])
+    # GPU state: prefill every head with the library, then overwrite the sampled heads with
+    # the oracle's fp32-rounded state (the state the oracle starts from).
+    d = dev(prior, torch.bfloat16)
+    _, C, n, m = B.mlstm_fwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], 64)
+    Ct = torch.from_numpy(o_prior["C"][:, 0].astype(np.float32)).cuda()
+    nt = torch.from_numpy(o_prior["n"][:, 0].astype(np.float32)).cuda()
+    mt = torch.from_numpy(o_prior["m"][:, 0].astype(np.float32)).cuda()
+    bt, ht = torch.from_numpy(bi).cuda(), torch.from_numpy(hi).cuda()
+    C[bt, ht], n[bt, ht], m[bt, ht] = Ct, nt, mt
+    s = dev(steps, torch.bfloat16)
+    hs = []
+    for t in range(w.S):
+        h = B.mlstm_step(s["q"][:, :, t].contiguous(), s["k"][:, :, t].contiguous(),
+                         s["v"][:, :, t].contiguous(), s["ig"][:, :, t].contiguous(),
+                         s["fg"][:, :, t].contiguous(), C, n, m, h_dtype=torch.float32)
+        hs.append(h[bt, ht])
+    torch.cuda.synchronize()
+    h_gpu = npy(torch.stack(hs, dim=1))  # [12, S, DV]
+    assert rel_err(h_gpu, o_steps["h"][:, 0]) <= TOL_BF16
+    eC, en, em = state_errs(npy(C[bt, ht]), npy(n[bt, ht]), npy(m[bt, ht]), o_steps["C"][:, 0],
+                            o_steps["n"][:, 0], o_steps["m"][:, 0])
+    assert eC <= TOL_BF16 and en <= TOL_BF16 and em <= 1e-4, (eC, en, em)
+
+
+def test_decode_step_fp32_matches_oracle(B):
+    w = W.DECODE.with_(B=3, NH=2, S=5, prior=32, DQK=64, DV=96, dtype="f32")
+    prior, steps = W.make_decode_inputs(w)
+    o_prior = oracle.recurrent(**prior, want_h=False)
+    o = oracle.recurrent(**steps, C0=o_prior["C"], n0=o_prior["n"], m0=o_prior["m"])
+    C = torch.from_numpy(o_prior["C"].astype(np.float32)).cuda()
+    n = torch.from_numpy(o_prior["n"].astype(np.float32)).cuda()
+    m = torch.from_numpy(o_prior["m"].astype(np.float32)).cuda()
+    s = dev(steps, torch.float32)
+    hs = [B.mlstm_step(*(s[k_][:, :, t].contiguous() for k_ in ("q", "k", "v", "ig", "fg")),
+                       C, n, m) for t in range(w.S)]
+    torch.cuda.synchronize()
+    assert rel_err(npy(torch.stack(hs, 2)), o["h"]) <= TOL_F32
+    eC, en, em = state_errs(npy(C), npy(n), npy(m), o["C"], o["n"], o["m"])
+    assert eC <= TOL_F32 and en <= TOL_F32 and em <= 1e-5
+
+
+def test_prefill_then_decode_handoff(B):
+    """Chunkwise prefill over S1 tokens, then single steps, equals the oracle over S1+S2."""
+    w = W.LAYER_350M.with_(B=2, NH=2, S=192, DQK=128, DV=128)
+    inp = W.make_inputs(w)
+    ora = oracle.recurrent(**inp)
+    S1 = 128
+    d = dev(inp, torch.bfloat16)
+    h1, C, n, m = B.mlstm_fwd_chunkwise(*(d[k_][:, :, :S1].contiguous() for k_ in ("q", "k", "v", "ig", "fg")),
+                                        64, h_dtype=torch.float32)
+    hs = [B.mlstm_step(*(d[k_][:, :, t].contiguous() for k_ in ("q", "k", "v", "ig", "fg")), C, n, m,
+                       h_dtype=torch.float32) for t in range(S1, w.S)]
+    torch.cuda.synchronize()
+    h = np.concatenate([npy(h1), npy(torch.stack(hs, 2))], axis=2)
+    assert rel_err(h, ora["h"]) <= TOL_BF16
+    eC, en, em = state_errs(npy(C), npy(n), npy(m), ora["C"], ora["n"], ora["m"])
+    assert eC <= TOL_BF16 and en <= TOL_BF16 and em <= 1e-4
+
+
+# ----------------------------------------------------------------------------- properties
+def test_split_sequence_with_initial_state(B):
+    w = W.TINY_F32.with_(B=2, NH=3, S=96, DQK=64, DV=32)
+    inp = W.make_inputs(w)
+    ora = oracle.recurrent(**inp)
+    d = dev(inp, torch.float32)
+    part = lambda a, b_: [d[k_][:, :, a:b_].contiguous() for k_ in ("q", "k", "v", "ig", "fg")]
+    h1, C, n, m = B.mlstm_fwd_chunkwise(*part(0, 32), 16)
+    h2, C2, n2, m2 = B.mlstm_fwd_chunkwise(*part(32, 96), 32, C_init=C, n_init=n, m_init=m)
+    torch.cuda.synchronize()
+    h = np.concatenate([npy(h1), npy(h2)], axis=2)
+    assert rel_err(h, ora["h"]) <= TOL_F32
+    eC, en, em = state_errs(npy(C2), npy(n2), npy(m2), ora["C"], ora["n"], ora["m"])
+    assert eC <= TOL_F32 and en <= TOL_F32 and em <= 1e-5
+
+
+def test_in_place_state_update(B):
+    w = W.TINY_F32.with_(S=32)
+    inp = W.make_inputs(w)
+    d = dev(inp, torch.float32)
+    _, C, n, m = B.mlstm_fwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], 16)
+    C0, n0, m0 = C.clone(), n.clone(), m.clone()
+    h_ref, C_ref, n_ref, m_ref = B.mlstm_fwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], 16,
+                                                       C_init=C0, n_init=n0, m_init=m0)
+    h = torch.empty_like(h_ref)
+    B.mlstm_fwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], 16, C_init=C, n_init=n,
+                          m_init=m, out=(h, C, n, m))
+    torch.cuda.synchronize()
+    assert torch.equal(h, h_ref) and torch.equal(C, C_ref) and torch.equal(n, n_ref) and torch.equal(m, m_ref)
+
+
+@pytest.mark.parametrize("chunk", [16, 32, 64, 128])
+def test_chunk_size_invariance(B, chunk):
+    w = W.LAYER_350M.with_(B=1, NH=2, S=256, DQK=64, DV=64)
+    inp = W.make_inputs(w)
+    ora = oracle.recurrent(**inp)
+    h, C, n, m = run_fwd(B, w, inp, chunk=chunk)
+    assert rel_err(h, ora["h"]) <= TOL_BF16
+    eC, en, em = state_errs(C, n, m, ora["C"], ora["n"], ora["m"])
+    assert eC <= TOL_BF16 and en <= TOL_BF16 and em <= 1e-4
+
+
+def test_causality(B):
+    w = W.LAYER_350M.with_(B=1, NH=2, S=256, DQK=64, DV=64)
+    inp = W.make_inputs(w)
+    h0, *_ = run_fwd(B, w, inp)
+    tp = 150
+    for key, delta in (("q", 1.0), ("k", -2.0), ("v", 3.0), ("ig", 4.0), ("fg", -1.0)):
+        inp[key][:, :, tp] += delta
+    h1, *_ = run_fwd(B, w, inp)
+    assert np.array_equal(h0[:, :, :tp], h1[:, :, :tp])
+    assert not np.allclose(h0[:, :, tp:], h1[:, :, tp:])
+
+
+def test_linearity_in_v(B):
+    w = W.TINY_F32.with_(S=64)
+    inp = W.make_inputs(w)
+    h0, C0, _, _ = run_fwd(B, w, inp)
+    inp["v"] = inp["v"] * 2.0  # exact scaling
+    h1, C1, _, _ = run_fwd(B, w, inp)
+    assert np.allclose(h1, 2.0 * h0, rtol=1e-6, atol=1e-6) and np.allclose(C1, 2.0 * C0, rtol=1e-6, atol=1e-6)
+
+
+# ----------------------------------------------------------------------------- edge cases
+@pytest.mark.parametrize("dqk,dv,chunk,dtype", [(96, 160, 32, "f32"), (32, 512, 16, "bf16"),
+                                                (512, 32, 128, "bf16"), (512, 512, 128, "bf16"),
+                                                (224, 64, 64, "f32")])
+def test_shapes(B, dqk, dv, chunk, dtype):
+    w = W.LAYER_350M.with_(B=2, NH=1, S=2 * chunk + (256 if chunk < 128 else 0), DQK=dqk, DV=dv,
+                           chunk=chunk, dtype=dtype)
+    inp = W.make_inputs(w)
+    ora = oracle.recurrent(**inp)
+    h, C, n, m = run_fwd(B, w, inp)
+    tol = tol_for(w)
+    assert rel_err(h, ora["h"]) <= tol
+    eC, en, em = state_errs(C, n, m, ora["C"], ora["n"], ora["m"])
+    assert eC <= tol and en <= tol and em <= 1e-4
+
+
+def test_empty_sequence_copies_state(B):
+    C0 = torch.randn(2, 3, 32, 64, device="cuda")
+    n0 = torch.randn(2, 3, 64, device="cuda")
+    m0 = torch.randn(2, 3, device="cuda")
+    e = torch.empty(2, 3, 0, 64, device="cuda")
+    ev = torch.empty(2, 3, 0, 32, device="cuda")
+    g = torch.empty(2, 3, 0, device="cuda")
+    h, C, n, m = B.mlstm_fwd_chunkwise(e, e, ev, g, g, 16, C_init=C0, n_init=n0, m_init=m0)
+    torch.cuda.synchronize()
+    assert h.numel() == 0 and torch.equal(C, C0) and torch.equal(n, n0) and torch.equal(m, m0)
+    _, C, n, m = B.mlstm_fwd_chunkwise(e, e, ev, g, g, 16)
+    torch.cuda.synchronize()
+    assert not C.any() and not n.any() and not m.any()
+
+
+@pytest.mark.parametrize("case", ["no_forget", "no_input", "spikes", "zero_q", "large_m_init"])
+def test_degenerate_gates(B, case):
+    w = W.TINY_F32.with_(B=1, NH=2, S=128, DQK=64, DV=64, chunk=32)
+    inp = W.make_inputs(w)
+    init = None
+    if case == "no_forget":
+        inp["fg"][:] = 30.0   # f = 1 to fp32: causal linear attention
+    elif case == "no_input":
+        inp["ig"][:, :, 40:] = -60.0  # exp(-60): later tokens barely write
+    elif case == "spikes":
+        inp["ig"][:, :, ::17] = 80.0
+    elif case == "zero_q":
+        inp["q"][:, :, 10:30] = 0.0   # n.q = 0: the floor exp(-m) decides
+    ora_kw = {}
+    if case == "large_m_init":
+        rng = np.random.default_rng(5)
+        C0 = rng.standard_normal((1, 2, 64, 64)).astype(np.float32)
+        n0 = rng.standard_normal((1, 2, 64)).astype(np.float32)
+        m0 = np.array([[40.0, -25.0]], np.float32)
+        ora_kw = dict(C0=C0, n0=n0, m0=m0)
+        init = tuple(torch.from_numpy(x).cuda() for x in (C0, n0, m0))
+    ora = oracle.recurrent(**inp, **ora_kw)
+    h, C, n, m = run_fwd(B, w, inp, init=init)
+    assert np.all(np.isfinite(h))
+    assert rel_err(h, ora["h"]) <= TOL_F32 * 10, rel_err(h, ora["h"])
+    eC, en, em = state_errs(C, n, m, ora["C"], ora["n"], ora["m"])
+    assert eC <= TOL_F32 * 10 and en <= TOL_F32 * 10 and em <= 1e-5
+
+
+# ----------------------------------------------------------------------------- error codes
+def test_error_codes_do_not_launch(B):
+    w = W.TINY_F32
+    inp = W.make_inputs(w)
+    d = dev(inp, torch.float32)
+    h = torch.full((1, 2, 64, 32), 7.0, device="cuda")
+    C = torch.full((1, 2, 32, 32), 7.0, device="cuda")
+    n = torch.full((1, 2, 32), 7.0, device="cuda")
+    m = torch.full((1, 2), 7.0, device="cuda")
+    small = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(B.MlstmError) as e:
+        B.mlstm_fwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], 16, out=(h, C, n, m),
+                              workspace=small)
+    assert e.value.code == 5
+    flat = torch.empty(1 + 2 * 64 * 32, device="cuda")
+    q_mis = flat[1:].view(1, 2, 64, 32)  # 4-byte offset: misaligned
+    q_mis.copy_(d["q"])
+    with pytest.raises(B.MlstmError) as e:
+        B.mlstm_fwd_chunkwise(q_mis, d["k"], d["v"], d["ig"], d["fg"], 16, out=(h, C, n, m))
+    assert e.value.code == 2
+    torch.cuda.synchronize()
+    assert bool((h == 7).all() and (C == 7).all() and (n == 7).all() and (m == 7).all())
