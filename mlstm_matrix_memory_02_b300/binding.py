@@ -234,7 +234,7 @@ def mlstm_step(q, k, v, ig, fg, C, n, m, h=None, h_dtype=None, stream=None):
     _dev(C, "C", torch.float32, (B, NH, DV, DQK))
     _dev(n, "n", torch.float32, (B, NH, DQK))
     _dev(m, "m", torch.float32, (B, NH))
-    h_dtype = h_dtype or dt
+    h_dtype = h_dtype or (h.dtype if h is not None else dt)
     if h is None:
         h = torch.empty((B, NH, DV), dtype=h_dtype, device=q.device)
     _dev(h, "h", h_dtype, (B, NH, DV))

@@ -330,10 +330,13 @@ def test_degenerate_gates(B, case):
         m0 = np.array([[40.0, -25.0]], np.float32)
         ora_kw = dict(C0=C0, n0=n0, m0=m0)
         init = tuple(torch.from_numpy(x).cuda() for x in (C0, n0, m0))
-    ora = oracle.recurrent(**inp, **ora_kw)
+    ora = oracle.recurrent(**inp, **ora_kw, want_m_tok=True, want_den=True)
     h, C, n, m = run_fwd(B, w, inp, init=init)
     assert np.all(np.isfinite(h))
-    assert rel_err(h, ora["h"]) <= TOL_F32 * 10, rel_err(h, ora["h"])
+    # fp32 arithmetic: rows with a cancelling denominator get the conditioned bound
+    u = (w.DQK + w.chunk) * 2.0 ** -24
+    ok, worst, stats = conditioned_ok(h, ora, inp["v"], TOL_F32, u, u)
+    assert ok, (worst, stats)
     eC, en, em = state_errs(C, n, m, ora["C"], ora["n"], ora["m"])
     assert eC <= TOL_F32 * 10 and en <= TOL_F32 * 10 and em <= 1e-5
 
