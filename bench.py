@@ -354,12 +354,14 @@ def run_ours(args, rank, local, world):
     if rank != 0:
         return
     line = {
-        "metric": "mLSTM chunkwise forward tokens/s (1.3B-style layer)",
+        "metric": f"mLSTM chunkwise forward tokens/s ({w.name})",
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "NH": w.NH, "S": w.S, "DQK": w.DQK, "DV": w.DV,
                    "chunk": w.chunk, "qkv": "bf16", "gates": "fp32", "h": "fp32",
+                   "kernel_path": "tensor cores (tcgen05, fused)" if B.mlstm_fwd_path(
+                       w.B, w.NH, w.S, w.DQK, w.DV, w.chunk) == 1 else "CUDA cores",
                    "l2": "flushed between timed iterations (256 MiB write, outside the events)",
                    "per_rank": "each rank runs the full layer batch (weak scaling)"},
         "roofline": roofline,
@@ -382,7 +384,7 @@ def run_ours(args, rank, local, world):
 def run_profile(kind: str):
     """Small, self-contained launches for ncu captures: one warm-up and one timed-shape call.
 
-    fwd:    the 1.3B-style layer forward (gates, then the state passing and output stage)
+    fwd:    the --workload forward (gates, then the state passing and output stage)
     decode: one decode step of the B=256, NH=8, d=256 state (state initialised randomly)"""
     import torch
     from mlstm_matrix_memory_02_b300 import binding as B
@@ -418,9 +420,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["1p3b", "350m", "stress"], default="1p3b",
+                    help="forward workload (default: the 1.3B-style layer)")
     ap.add_argument("--profile", choices=["fwd", "decode"], default=None,
                     help="run one small forward or decode step for ncu captures and exit")
     args = ap.parse_args()
+    global FWD
+    FWD = W.WORKLOADS[args.workload]
     if args.profile:
         run_profile(args.profile)
         return

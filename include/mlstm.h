@@ -67,6 +67,12 @@ int mlstm_last_cuda_error(void);
  * the difference across a region counts the library's launches inside it. */
 unsigned long long mlstm_kernel_launches(void);
 
+/* Which kernels mlstm_fwd_chunkwise / mlstm_fwd_from_gates run for these sizes:
+ * 1 = the fused tensor-core kernel (bf16 inputs, chunk 64, d_qk in {64, 128, 256},
+ * d_v a multiple of 128), 0 = the CUDA-core kernels (every other supported size),
+ * -1 = unsupported sizes or dtype. */
+int mlstm_fwd_path(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt);
+
 /* Bytes of device workspace mlstm_fwd_chunkwise / mlstm_fwd_chunk_states need for these
  * sizes (0 if the sizes are unsupported).  The workspace holds the per-token gate
  * prefix sums, the per-chunk stabiliser and, on paths that materialise them, the
@@ -125,6 +131,12 @@ mlstm_status mlstm_fwd_chunk_states(const void *k, const void *v, const float *i
 mlstm_status mlstm_fwd_gates(const float *igate_pre, const float *fgate_pre, int B, int NH,
                              int S, int chunk, const float *m_init, float *m_tok,
                              float *m_states, void *workspace, size_t ws_bytes, void *stream);
+
+/* Synchronises `stream` and reports whether the last forward that used `workspace` (with
+ * these sizes) completed every bounded device-side wait: MLSTM_OK, or MLSTM_ERR_TIMEOUT when a
+ * kernel gave up waiting (mlstm_last_cuda_error() then returns the kernel's wait code). */
+mlstm_status mlstm_fwd_check(const void *workspace, size_t ws_bytes, int B, int NH, int S, int DQK,
+                             int DV, int chunk, mlstm_dtype dt, void *stream);
 
 /* One recurrent decode step for every (batch, head), in place (section 5 "Inference
  * Memory and Throughput Trade-Offs"; section 2 stabiliser; section 3 updates):

@@ -46,13 +46,18 @@ _lib.mlstm_fwd_chunk_states.argtypes = [_vp, _vp, _fp, _fp, _i, _i, _i, _i, _i, 
                                         _fp, _fp, _fp, _fp, _fp, _fp, _vp, _sz, _vp]
 _lib.mlstm_fwd_gates.restype = _i
 _lib.mlstm_fwd_gates.argtypes = [_fp, _fp, _i, _i, _i, _i, _fp, _fp, _fp, _vp, _sz, _vp]
+_lib.mlstm_fwd_path.restype = _i
+_lib.mlstm_fwd_path.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+_lib.mlstm_fwd_check.restype = _i
+_lib.mlstm_fwd_check.argtypes = [_vp, _sz, _i, _i, _i, _i, _i, _i, _i, _vp]
 _lib.mlstm_step.restype = _i
 _lib.mlstm_step.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _vp, _i, _i, _i, _i,
                             _i, _i, _vp]
 
 EXPORTED = ["mlstm_status_str", "mlstm_last_cuda_error", "mlstm_kernel_launches",
             "mlstm_fwd_workspace_bytes", "mlstm_fwd_chunkwise", "mlstm_fwd_from_gates",
-            "mlstm_fwd_chunk_states", "mlstm_fwd_gates", "mlstm_step"]
+            "mlstm_fwd_chunk_states", "mlstm_fwd_gates", "mlstm_fwd_check", "mlstm_fwd_path",
+            "mlstm_step"]
 
 
 class MlstmError(RuntimeError):
@@ -98,6 +103,11 @@ def _dev(t, name, dtype=None, shape=None):
 
 def mlstm_fwd_workspace_bytes(B, NH, S, DQK, DV, chunk, dtype=torch.bfloat16) -> int:
     return int(_lib.mlstm_fwd_workspace_bytes(B, NH, S, DQK, DV, chunk, _DT[dtype]))
+
+
+def mlstm_fwd_path(B, NH, S, DQK, DV, chunk, dtype=torch.bfloat16) -> int:
+    """1: fused tensor-core kernel, 0: CUDA-core kernels, -1: unsupported."""
+    return int(_lib.mlstm_fwd_path(B, NH, S, DQK, DV, chunk, _DT[dtype]))
 
 
 def alloc_workspace(B, NH, S, DQK, DV, chunk, dtype=torch.bfloat16, device=None):
@@ -219,6 +229,14 @@ def mlstm_fwd_gates(igate_pre, fgate_pre, chunk, m_init=None, workspace=None, st
                                 _stream(stream))
     _check(code, "mlstm_fwd_gates")
     return m_tok, m_states
+
+
+def mlstm_fwd_check(workspace, B, NH, S, DQK, DV, chunk, dtype=torch.bfloat16, stream=None):
+    """Synchronise and raise MlstmError if the last forward on ``workspace`` reported a
+    device-side wait that gave up."""
+    code = _lib.mlstm_fwd_check(_ptr(workspace), workspace.numel(), B, NH, S, DQK, DV, chunk,
+                                _DT[dtype], _stream(stream))
+    _check(code, "mlstm_fwd_check")
 
 
 def mlstm_step(q, k, v, ig, fg, C, n, m, h=None, h_dtype=None, stream=None):

@@ -27,8 +27,13 @@ constexpr int kMaxPairs = 65535;  // grid.z limit of the output kernel
 inline size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t gb, gx, gu, cm, Cs, ns, gates_end, total;
+  size_t gb, gx, gu, cm, err, Cs, ns, gates_end, total;
+  bool tc;  // the forward runs on the fused tensor-core kernel (no materialised states)
 };
+
+bool use_tc(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) {
+  return fused_tc_supported(S, chunk, DQK, DV, dt == MLSTM_BF16) && (long long)B * NH * S < (1LL << 31);
+}
 
 bool sizes_ok(int B, int NH, int S, int DQK, int DV, int chunk) {
   if (B < 1 || NH < 1 || S < 0) return false;
@@ -41,17 +46,20 @@ bool sizes_ok(int B, int NH, int S, int DQK, int DV, int chunk) {
   return true;
 }
 
-Layout layout(int B, int NH, int S, int DQK, int DV, int chunk) {
+Layout layout(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) {
   const size_t P = (size_t)B * NH, NC = (size_t)S / chunk;
   Layout L{};
+  L.tc = use_tc(B, NH, S, DQK, DV, chunk, dt);
   size_t off = 0;
   L.gb = off; off = round_up(off + P * S * sizeof(float));
   L.gx = off; off = round_up(off + P * S * sizeof(float));
   L.gu = off; off = round_up(off + P * S * sizeof(float));
   L.cm = off; off = round_up(off + P * (NC + 1) * sizeof(float));
+  L.err = off; off = round_up(off + sizeof(int));
   L.gates_end = off;
-  L.Cs = off; off = round_up(off + P * (NC + 1) * DV * DQK * sizeof(float));
-  L.ns = off; off = round_up(off + P * (NC + 1) * DQK * sizeof(float));
+  const size_t states = L.tc ? 0 : P * (NC + 1);
+  L.Cs = off; off = round_up(off + states * DV * DQK * sizeof(float));
+  L.ns = off; off = round_up(off + states * DQK * sizeof(float));
   L.total = off;
   return L;
 }
@@ -109,10 +117,16 @@ int mlstm_last_cuda_error(void) { return g_last_cuda_error; }
 
 unsigned long long mlstm_kernel_launches(void) { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
 
+int mlstm_fwd_path(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) {
+  if (dt != MLSTM_F32 && dt != MLSTM_BF16) return -1;
+  if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return -1;
+  return use_tc(B, NH, S, DQK, DV, chunk, dt) ? 1 : 0;
+}
+
 size_t mlstm_fwd_workspace_bytes(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) {
   if (dt != MLSTM_F32 && dt != MLSTM_BF16) return 0;
   if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return 0;
-  return layout(B, NH, S, DQK, DV, chunk).total;
+  return layout(B, NH, S, DQK, DV, chunk, dt).total;
 }
 
 static mlstm_status check_init(const float *C_init, const float *n_init, const float *m_init) {
@@ -137,7 +151,7 @@ static mlstm_status check_fwd_args(const void *q, const void *k, const void *v, 
   for (const void *ptr : {q, k, v, h, (const void *)C_last, (const void *)n_last, (const void *)m_last, workspace})
     if (!aligned16(ptr)) return MLSTM_ERR_ALIGN;
   if ((C_init && !aligned16(C_init)) || (n_init && !aligned16(n_init))) return MLSTM_ERR_ALIGN;
-  if (ws_bytes < layout(B, NH, S, DQK, DV, chunk).total) return MLSTM_ERR_WORKSPACE;
+  if (ws_bytes < layout(B, NH, S, DQK, DV, chunk, dt).total) return MLSTM_ERR_WORKSPACE;
   return MLSTM_OK;
 }
 
@@ -146,12 +160,18 @@ static mlstm_status run_from_gates(const void *q, const void *k, const void *v, 
                                    int DQK, int DV, int chunk, mlstm_dtype dt, const float *C_init,
                                    const float *n_init, void *h, mlstm_dtype h_dt, float *C_last,
                                    float *n_last, float *m_last, void *workspace, cudaStream_t s) {
-  const Layout Lw = layout(B, NH, S, DQK, DV, chunk);
+  const Layout Lw = layout(B, NH, S, DQK, DV, chunk, dt);
   char *ws = (char *)workspace;
   float *gb = (float *)(ws + Lw.gb), *gx = (float *)(ws + Lw.gx), *gu = (float *)(ws + Lw.gu);
   float *cm = (float *)(ws + Lw.cm), *Cs = (float *)(ws + Lw.Cs), *ns = (float *)(ws + Lw.ns);
+  int *err = (int *)(ws + Lw.err);
   const int P = B * NH, NC = S / chunk;
   const bool bf16 = dt == MLSTM_BF16;
+  if (Lw.tc) {
+    if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return launch_status(cudaGetLastError());
+    return launch_status(launch_fused_tc(q, k, v, h_dt == MLSTM_BF16, gb, gx, gu, cm, P, S, DQK, DV, C_init,
+                                         n_init, h, C_last, n_last, m_last, err, s));
+  }
   if (mlstm_status st = launch_status(launch_states_simt(k, v, bf16, gb, gx, cm, P, S, chunk, DQK, DV, C_init,
                                                          n_init, Cs, ns, C_last, n_last, s)))
     return st;
@@ -191,7 +211,7 @@ mlstm_status mlstm_fwd_chunkwise(const void *q, const void *k, const void *v, co
   if (mlstm_status st = check_device()) return st;
 
   cudaStream_t s = (cudaStream_t)stream;
-  const Layout Lw = layout(B, NH, S, DQK, DV, chunk);
+  const Layout Lw = layout(B, NH, S, DQK, DV, chunk, dt);
   char *ws = (char *)workspace;
   const int P = B * NH;
   if (mlstm_status st = launch_status(launch_gates(igate_pre, fgate_pre, P, S, chunk, m_init, (float *)(ws + Lw.gb),
@@ -216,8 +236,8 @@ mlstm_status mlstm_fwd_chunk_states(const void *k, const void *v, const float *i
                           (const void *)C_states, (const void *)n_states, (const void *)m_states,
                           (const void *)workspace})
     if (!aligned16(ptr)) return MLSTM_ERR_ALIGN;
-  const Layout Lw = layout(B, NH, S, DQK, DV, chunk);
-  if (ws_bytes < Lw.total) return MLSTM_ERR_WORKSPACE;
+  const Layout Lw = layout(B, NH, S, DQK, DV, chunk, dt);
+  if (ws_bytes < Lw.gates_end) return MLSTM_ERR_WORKSPACE;
   if (mlstm_status st = check_device()) return st;
 
   cudaStream_t s = (cudaStream_t)stream;
@@ -244,7 +264,7 @@ mlstm_status mlstm_fwd_gates(const float *igate_pre, const float *fgate_pre, int
     if (!aligned16(ptr)) return MLSTM_ERR_ALIGN;
   if ((m_init && !aligned16(m_init)) || (m_tok && !aligned16(m_tok)) || (m_states && !aligned16(m_states)))
     return MLSTM_ERR_ALIGN;
-  const Layout Lw = layout(B, NH, S, 32, 32, chunk);
+  const Layout Lw = layout(B, NH, S, 32, 32, chunk, MLSTM_F32);
   if (ws_bytes < Lw.gates_end) return MLSTM_ERR_WORKSPACE;
   if (mlstm_status st = check_device()) return st;
 
@@ -258,6 +278,28 @@ mlstm_status mlstm_fwd_gates(const float *igate_pre, const float *fgate_pre, int
   if (m_states)
     return launch_status(cudaMemcpyAsync(m_states, cm, sizeof(float) * (size_t)P * (NC + 1),
                                          cudaMemcpyDeviceToDevice, s));
+  return MLSTM_OK;
+}
+
+mlstm_status mlstm_fwd_check(const void *workspace, size_t ws_bytes, int B, int NH, int S, int DQK, int DV,
+                             int chunk, mlstm_dtype dt, void *stream) {
+  if (dt != MLSTM_F32 && dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
+  if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return MLSTM_ERR_SHAPE;
+  if (!workspace) return MLSTM_ERR_NULL;
+  const Layout Lw = layout(B, NH, S, DQK, DV, chunk, dt);
+  if (ws_bytes < Lw.gates_end) return MLSTM_ERR_WORKSPACE;
+  if (mlstm_status st = check_device()) return st;
+  int word = 0;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(&word, (const char *)workspace + Lw.err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    g_last_cuda_error = (int)cudaGetLastError();
+    return MLSTM_ERR_LAUNCH;
+  }
+  if (word != 0) {
+    g_last_cuda_error = word;  // the code of the wait that gave up
+    return MLSTM_ERR_TIMEOUT;
+  }
   return MLSTM_OK;
 }
 

@@ -363,3 +363,65 @@ def test_error_codes_do_not_launch(B):
     assert e.value.code == 2
     torch.cuda.synchronize()
     assert bool((h == 7).all() and (C == 7).all() and (n == 7).all() and (m == 7).all())
+
+
+# ----------------------------------------------------------------------------- tensor-core path
+TC_CASES = [
+    # (DQK, DV, B, NH, S, gates, init)
+    (64, 128, 1, 1, 64, "layer", False),
+    (128, 128, 1, 2, 256, "layer", False),
+    (256, 256, 2, 1, 512, "layer", True),
+    (256, 384, 1, 2, 512, "stress", False),
+    (128, 512, 2, 1, 320, "layer", True),
+    (64, 256, 3, 1, 192, "stress", True),
+]
+
+
+@pytest.mark.parametrize("dqk,dv,b,nh,s,gates,init", TC_CASES)
+def test_tensor_core_path(B, dqk, dv, b, nh, s, gates, init):
+    """The fused tensor-core kernel (fp16 operands, fp32 accumulation in tensor memory)
+    against the oracle: plain 2e-2 tolerance where the denominators are well conditioned,
+    the first-order conditioned bound on every row (operands rounded to fp16: 2^-11 per
+    term in the numerator, fp32 sums in the denominator)."""
+    w = W.LAYER_350M.with_(B=b, NH=nh, S=s, DQK=dqk, DV=dv)
+    if gates == "stress":
+        w = w.with_(ig=("student_t", 4.0, 3.0), fg=("normal", 0.0, 2.0))
+    assert B.mlstm_fwd_path(b, nh, s, dqk, dv, 64) == 1
+    inp = W.make_inputs(w)
+    ora_kw, init_t = {}, None
+    if init:
+        rng = np.random.default_rng(11)
+        C0 = (0.3 * rng.standard_normal((b, nh, dv, dqk))).astype(np.float32)
+        n0 = (0.3 * rng.standard_normal((b, nh, dqk))).astype(np.float32)
+        m0 = rng.uniform(-2, 3, (b, nh)).astype(np.float32)
+        ora_kw = dict(C0=C0, n0=n0, m0=m0)
+        init_t = tuple(torch.from_numpy(x).cuda() for x in (C0, n0, m0))
+    ora = oracle.recurrent(**inp, **ora_kw, want_m_tok=True, want_den=True)
+    d = dev(inp, torch.bfloat16)
+    ws = B.alloc_workspace(b, nh, s, dqk, dv, 64)
+    kw = {} if init_t is None else dict(C_init=init_t[0], n_init=init_t[1], m_init=init_t[2])
+    h, C, n, m = B.mlstm_fwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], 64,
+                                       h_dtype=torch.float32, workspace=ws, **kw)
+    B.mlstm_fwd_check(ws, b, nh, s, dqk, dv, 64)
+    h = npy(h)
+    assert np.all(np.isfinite(h))
+    ok, worst, stats = conditioned_ok(h, ora, inp["v"], TOL_BF16, 4 * 2.0 ** -11,
+                                      (dqk + 64) * 2.0 ** -24)
+    assert ok, (worst, stats)
+    assert stats["rel_err_kappa_le_100"] <= TOL_BF16, stats
+    if gates == "layer":
+        assert rel_err(h, ora["h"]) <= TOL_BF16
+    eC, en, em = state_errs(npy(C), npy(n), npy(m), ora["C"], ora["n"], ora["m"])
+    assert eC <= TOL_BF16 and en <= TOL_BF16 and em <= 1e-4, (eC, en, em)
+
+
+def test_tensor_core_path_matches_cuda_core_path(B):
+    """Same inputs through both kernel families (the CUDA-core family reached with fp32
+    inputs holding the same bf16 values): outputs agree to the fp16-operand tolerance."""
+    w = W.LAYER_350M.with_(B=1, NH=2, S=256, DQK=128, DV=256)
+    inp = W.make_inputs(w)
+    assert B.mlstm_fwd_path(1, 2, 256, 128, 256, 64, torch.bfloat16) == 1
+    assert B.mlstm_fwd_path(1, 2, 256, 128, 256, 64, torch.float32) == 0
+    h16, C16, _, _ = run_fwd(B, w, inp)
+    h32, C32, _, _ = run_fwd(B, w.with_(dtype="f32"), inp)
+    assert rel_err(h16, h32) <= TOL_BF16 and rel_err(C16, C32) <= TOL_BF16
