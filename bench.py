@@ -360,8 +360,9 @@ def run_ours(args, rank, local, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "NH": w.NH, "S": w.S, "DQK": w.DQK, "DV": w.DV,
                    "chunk": w.chunk, "qkv": "bf16", "gates": "fp32", "h": "fp32",
-                   "kernel_path": "tensor cores (tcgen05, fused)" if B.mlstm_fwd_path(
-                       w.B, w.NH, w.S, w.DQK, w.DV, w.chunk) == 1 else "CUDA cores",
+                   "kernel_path": {0: "CUDA cores", 1: "tensor cores (tcgen05, fused, one CTA per d_v tile)",
+                                   2: "tensor cores (tcgen05, fused, d_qk split over a CTA pair)"}[
+                       B.mlstm_fwd_path(w.B, w.NH, w.S, w.DQK, w.DV, w.chunk)],
                    "l2": "flushed between timed iterations (256 MiB write, outside the events)",
                    "per_rank": "each rank runs the full layer batch (weak scaling)"},
         "roofline": roofline,

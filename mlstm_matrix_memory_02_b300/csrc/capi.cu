@@ -27,12 +27,12 @@ constexpr int kMaxPairs = 65535;  // grid.z limit of the output kernel
 inline size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t gb, gx, gu, cm, err, Cs, ns, gates_end, total;
+  size_t gb, gx, gu, cm, err, Cs, ns, ncopy, gates_end, total;
   bool tc;  // the forward runs on the fused tensor-core kernel (no materialised states)
 };
 
 bool use_tc(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) {
-  return fused_tc_supported(S, chunk, DQK, DV, dt == MLSTM_BF16) && (long long)B * NH * S < (1LL << 31);
+  return fwd_tc_supported(S, chunk, DQK, DV, dt == MLSTM_BF16) && (long long)B * NH * S < (1LL << 31);
 }
 
 bool sizes_ok(int B, int NH, int S, int DQK, int DV, int chunk) {
@@ -60,6 +60,9 @@ Layout layout(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) 
   const size_t states = L.tc ? 0 : P * (NC + 1);
   L.Cs = off; off = round_up(off + states * DV * DQK * sizeof(float));
   L.ns = off; off = round_up(off + states * DQK * sizeof(float));
+  // tensor-core path: a copy of n_init (every d_v tile reads it; one of them writes n_last,
+  // which may alias n_init)
+  L.ncopy = off; off = round_up(off + (L.tc ? P * DQK : 0) * sizeof(float));
   L.total = off;
   return L;
 }
@@ -120,7 +123,8 @@ unsigned long long mlstm_kernel_launches(void) { return __atomic_load_n(&g_launc
 int mlstm_fwd_path(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) {
   if (dt != MLSTM_F32 && dt != MLSTM_BF16) return -1;
   if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return -1;
-  return use_tc(B, NH, S, DQK, DV, chunk, dt) ? 1 : 0;
+  if (!use_tc(B, NH, S, DQK, DV, chunk, dt)) return 0;
+  return fwd_tc_pair(B * NH, DQK, DV) ? 2 : 1;
 }
 
 size_t mlstm_fwd_workspace_bytes(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) {
@@ -169,7 +173,13 @@ static mlstm_status run_from_gates(const void *q, const void *k, const void *v, 
   const bool bf16 = dt == MLSTM_BF16;
   if (Lw.tc) {
     if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return launch_status(cudaGetLastError());
-    return launch_status(launch_fused_tc(q, k, v, h_dt == MLSTM_BF16, gb, gx, gu, cm, P, S, DQK, DV, C_init,
+    if (n_init) {
+      float *ncopy = (float *)(ws + Lw.ncopy);
+      if (cudaMemcpyAsync(ncopy, n_init, sizeof(float) * (size_t)P * DQK, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return launch_status(cudaGetLastError());
+      n_init = ncopy;
+    }
+    return launch_status(launch_fwd_tc(q, k, v, h_dt == MLSTM_BF16, gb, gx, gu, cm, P, S, DQK, DV, C_init,
                                          n_init, h, C_last, n_last, m_last, err, s));
   }
   if (mlstm_status st = launch_status(launch_states_simt(k, v, bf16, gb, gx, cm, P, S, chunk, DQK, DV, C_init,

@@ -27,12 +27,14 @@ cudaError_t launch_step(const void *q, const void *k, const void *v, bool bf16, 
                         const float *ig, const float *fg, float *C, float *n, float *m, void *h,
                         int P, int DQK, int DV, cudaStream_t stream);
 
-// (b)+(c) fused on tensor cores: bf16 inputs, chunk 64, d_qk in {64, 128, 256}, d_v % 128 == 0.
-bool fused_tc_supported(int S, int L, int D, int DV, bool bf16);
-cudaError_t launch_fused_tc(const void *q, const void *k, const void *v, bool out_bf16, const float *gb,
-                            const float *gx, const float *gu, const float *cm, int P, int S, int D, int DV,
-                            const float *C_init, const float *n_init, void *h, float *C_last, float *n_last,
-                            float *m_last, int *err, cudaStream_t stream);
+// (b)+(c) fused on tensor cores (fwd_tc.cu): bf16 inputs, chunk 64, d_qk in {64, 128, 256, 512},
+// d_v a multiple of 128.  fwd_tc_pair says whether a head's d_qk is split over a CTA pair.
+bool fwd_tc_supported(int S, int L, int D, int DV, bool bf16);
+bool fwd_tc_pair(int P, int D, int DV);
+cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, bool out_bf16, const float *gb,
+                          const float *gx, const float *gu, const float *cm, int P, int S, int D, int DV,
+                          const float *C_init, const float *n_init, void *h, float *C_last, float *n_last,
+                          float *m_last, int *err, cudaStream_t stream);
 
 // small helpers
 cudaError_t launch_copy_chunk_m(const float *cm, int P, int NC, float *m_last, cudaStream_t stream);

@@ -2,9 +2,9 @@
 // features the tensor-core kernels use: mbarriers, TMA tiled loads, tcgen05 tensor memory
 // (alloc / mma / commit / ld / st) and the shared-memory matrix descriptors.
 //
-// Every wait here is bounded: a wait that gives up records a code in the caller-supplied
-// error word and returns false, so a kernel can free its tensor memory and exit instead of
-// hanging.
+// Every wait here is bounded in time: a wait that gives up records a code in the
+// caller-supplied error word and returns false, so a kernel can free its tensor memory and exit
+// instead of hanging.
 #pragma once
 
 #include <cuda.h>
@@ -44,15 +44,91 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Waits for the phase with the given parity to complete; gives up after `limit` polls
-// (each try_wait itself suspends for a hardware-defined time), records `code` in *err and
-// returns false.
+// Waits for the phase with the given parity to complete.  Each poll may suspend the thread
+// for up to kSuspendNs; the wait gives up after about kWaitCycles SM clocks (about one second),
+// or as soon as *abort (when given) becomes non-zero, records `code` in *err and returns false.
+constexpr uint32_t kSuspendNs = 20000;
+constexpr long long kWaitCycles = 1LL << 31;
+
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, int code,
-                                          uint32_t limit = 1u << 20) {
-  for (uint32_t i = 0; i < limit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  if (err) atomicCAS(err, 0, code);
-  return false;
+                                          const int *abort = nullptr) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_try_wait_hint(bar, parity)) return true;
+    if ((abort && *(const volatile int *)abort) || clock64() - t0 > kWaitCycles) {
+      if (err) atomicCAS(err, 0, code);
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- clusters / distributed smem
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// All threads of every CTA of the cluster; release/acquire orders shared-memory accesses.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// Asynchronous stores into another CTA's shared memory; each signals its byte count on the
+// mbarrier `rbar` that lives in the destination CTA.
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, float a, float b, float c, float d, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   raddr),
+               "f"(a), "f"(b), "f"(c), "f"(d), "r"(rbar)
+               : "memory");
+}
+__device__ __forceinline__ void st_async_f32(uint32_t raddr, float a, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(raddr), "f"(a),
+               "r"(rbar)
+               : "memory");
+}
+// One arrival on an mbarrier of another CTA of the cluster (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t rbar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+// As mbar_wait, for phases completed by another CTA of the cluster (acquire at cluster scope).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, int *err, int code,
+                                                  const int *abort = nullptr) {
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((abort && *(const volatile int *)abort) || clock64() - t0 > kWaitCycles) {
+      if (err) atomicCAS(err, 0, code);
+      return false;
+    }
+  }
 }
 
 // ---------------------------------------------------------------- TMA
@@ -108,6 +184,16 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uin
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16; A is read from tensor memory (row m = lane m).
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // Signals `bar` (one arrival) when every tcgen05.mma issued so far by this thread is done.

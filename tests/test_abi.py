@@ -55,10 +55,15 @@ def test_status_strings(lib):
 def test_workspace_bytes(lib):
     ws = lib.mlstm_fwd_workspace_bytes
     assert ws(4, 4, 2048, 512, 512, 64, 1) > 0
-    # gate arrays (3 x P x S fp32) + chunk m + boundary states (P x (NC+1) x DV x DQK fp32)
     P, S, NC = 16, 2048, 32
-    need = 3 * P * S * 4 + P * (NC + 1) * 4 + P * (NC + 1) * 512 * 512 * 4 + P * (NC + 1) * 512 * 4
-    assert ws(4, 4, 2048, 512, 512, 64, 1) >= need
+    gates = 3 * P * S * 4 + P * (NC + 1) * 4
+    # CUDA-core path (fp32 inputs): gate arrays (3 x P x S fp32) + chunk m + boundary states
+    # (P x (NC+1) x DV x DQK fp32)
+    need = gates + P * (NC + 1) * 512 * 512 * 4 + P * (NC + 1) * 512 * 4
+    assert ws(4, 4, 2048, 512, 512, 64, 0) >= need
+    # tensor-core path (bf16, chunk 64): gate arrays, chunk m and a copy of n_init; no states
+    assert lib.mlstm_fwd_path(4, 4, 2048, 512, 512, 64, 1) == 2  # d_qk = 512: CTA pair
+    assert gates + P * 512 * 4 <= ws(4, 4, 2048, 512, 512, 64, 1) < need // 100
     assert ws(1, 1, 100, 64, 64, 64, 1) == 0      # S % chunk != 0
     assert ws(1, 1, 128, 48, 64, 64, 1) == 0      # DQK not a multiple of 32
     assert ws(1, 1, 128, 64, 1024, 64, 1) == 0    # DV above 512

@@ -374,6 +374,13 @@ TC_CASES = [
     (256, 384, 1, 2, 512, "stress", False),
     (128, 512, 2, 1, 320, "layer", True),
     (64, 256, 3, 1, 192, "stress", True),
+    # d_qk = 512: the state of a d_v tile is split over a CTA pair
+    (512, 128, 1, 1, 128, "layer", False),
+    (512, 256, 1, 2, 192, "stress", True),
+    (512, 512, 1, 1, 256, "layer", True),
+    # enough heads that one CTA per (head, d_v tile) fills the GPU: no pair
+    (128, 128, 2, 80, 64, "layer", True),
+    (256, 128, 1, 150, 128, "stress", False),
 ]
 
 
@@ -386,7 +393,8 @@ def test_tensor_core_path(B, dqk, dv, b, nh, s, gates, init):
     w = W.LAYER_350M.with_(B=b, NH=nh, S=s, DQK=dqk, DV=dv)
     if gates == "stress":
         w = w.with_(ig=("student_t", 4.0, 3.0), fg=("normal", 0.0, 2.0))
-    assert B.mlstm_fwd_path(b, nh, s, dqk, dv, 64) == 1
+    path = B.mlstm_fwd_path(b, nh, s, dqk, dv, 64)
+    assert path == (2 if dqk == 512 or (dqk >= 128 and b * nh * (dv // 128) < 148) else 1)
     inp = W.make_inputs(w)
     ora_kw, init_t = {}, None
     if init:
@@ -420,8 +428,27 @@ def test_tensor_core_path_matches_cuda_core_path(B):
     inputs holding the same bf16 values): outputs agree to the fp16-operand tolerance."""
     w = W.LAYER_350M.with_(B=1, NH=2, S=256, DQK=128, DV=256)
     inp = W.make_inputs(w)
-    assert B.mlstm_fwd_path(1, 2, 256, 128, 256, 64, torch.bfloat16) == 1
+    assert B.mlstm_fwd_path(1, 2, 256, 128, 256, 64, torch.bfloat16) >= 1
     assert B.mlstm_fwd_path(1, 2, 256, 128, 256, 64, torch.float32) == 0
     h16, C16, _, _ = run_fwd(B, w, inp)
     h32, C32, _, _ = run_fwd(B, w.with_(dtype="f32"), inp)
     assert rel_err(h16, h32) <= TOL_BF16 and rel_err(C16, C32) <= TOL_BF16
+
+
+@pytest.mark.parametrize("dqk", [256, 512])
+def test_tensor_core_in_place_state_update(B, dqk):
+    """Outputs may alias the initial state on the tensor-core path too (n_init is read by
+    every d_v tile while one of them writes n_last)."""
+    w = W.LAYER_350M.with_(B=1, NH=2, S=128, DQK=dqk, DV=256)
+    inp = W.make_inputs(w)
+    d = dev(inp, torch.bfloat16)
+    assert B.mlstm_fwd_path(1, 2, 128, dqk, 256, 64) >= 1
+    _, C, n, m = B.mlstm_fwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], 64, h_dtype=torch.float32)
+    C0, n0, m0 = C.clone(), n.clone(), m.clone()
+    h_ref, C_ref, n_ref, m_ref = B.mlstm_fwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], 64,
+                                                       h_dtype=torch.float32, C_init=C0, n_init=n0, m_init=m0)
+    h = torch.empty_like(h_ref)
+    B.mlstm_fwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], 64, h_dtype=torch.float32, C_init=C,
+                          n_init=n, m_init=m, out=(h, C, n, m))
+    torch.cuda.synchronize()
+    assert torch.equal(h, h_ref) and torch.equal(C, C_ref) and torch.equal(n, n_ref) and torch.equal(m, m_ref)
