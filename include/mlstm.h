@@ -151,6 +151,37 @@ mlstm_status mlstm_step(const void *q, const void *k, const void *v, const float
                         const float *fg, float *C, float *n, float *m, void *h, int B, int NH,
                         int DQK, int DV, mlstm_dtype dt, mlstm_dtype h_dt, void *stream);
 
+/* Forward without any device allocation (no counterpart on the source pages: an interface
+ * addition of this library).
+ *
+ * Some callers cannot allocate device memory for a workspace: a plugin running inside a host
+ * application that owns all device memory through its own pool (an extra cudaMalloc would
+ * fail or fragment it), or a latency-critical serving loop where cudaMalloc/cudaFree may
+ * synchronise the device.  This entry point takes the same arguments as mlstm_fwd_chunkwise
+ * minus the workspace, and computes exactly the same outputs; its scratch is a fixed array
+ * of MLSTM_NOALLOC_SCRATCH_BYTES bytes inside the library's device image, which every GPU
+ * that loads the library holds until the process exits.  Nothing is allocated by the call:
+ * no cudaMalloc, no cudaFree, no allocating library routine.
+ *   - Sizes whose mlstm_fwd_workspace_bytes(...) exceeds MLSTM_NOALLOC_SCRATCH_BYTES are
+ *     rejected with MLSTM_ERR_WORKSPACE before anything is launched (the 1.3B-style layer,
+ *     B=4 NH=4 S=2048 d=512 bf16 chunk 64, needs about 0.43 MB; sizes that take the CUDA-core
+ *     path and materialise boundary states fit only when small).
+ *   - The first call on a device resolves the array's device address on that device (with
+ *     it current, cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call in the process shares the one array: calls whose work may overlap on the
+ *     GPU (different streams, or different host threads, without ordering) race on it and
+ *     must be serialised by the caller.  Stale contents left by an earlier call are harmless:
+ *     the forward rewrites all it reads and clears what must start at zero.
+ * Other arguments, outputs and errors as for mlstm_fwd_chunkwise. */
+#define MLSTM_NOALLOC_SCRATCH_BYTES (8u << 20)
+mlstm_status mlstm_fwd_chunkwise_noalloc(const void *q, const void *k, const void *v,
+                                         const float *igate_pre, const float *fgate_pre, int B,
+                                         int NH, int S, int DQK, int DV, int chunk,
+                                         mlstm_dtype dt, const float *C_init,
+                                         const float *n_init, const float *m_init, void *h,
+                                         mlstm_dtype h_dt, float *C_last, float *n_last,
+                                         float *m_last, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

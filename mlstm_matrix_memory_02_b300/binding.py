@@ -54,10 +54,17 @@ _lib.mlstm_step.restype = _i
 _lib.mlstm_step.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _vp, _i, _i, _i, _i,
                             _i, _i, _vp]
 
+_lib.mlstm_fwd_chunkwise_noalloc.restype = _i
+_lib.mlstm_fwd_chunkwise_noalloc.argtypes = [_vp, _vp, _vp, _fp, _fp, _i, _i, _i, _i, _i, _i, _i,
+                                             _fp, _fp, _fp, _vp, _i, _fp, _fp, _fp, _vp]
+
 EXPORTED = ["mlstm_status_str", "mlstm_last_cuda_error", "mlstm_kernel_launches",
             "mlstm_fwd_workspace_bytes", "mlstm_fwd_chunkwise", "mlstm_fwd_from_gates",
             "mlstm_fwd_chunk_states", "mlstm_fwd_gates", "mlstm_fwd_check", "mlstm_fwd_path",
-            "mlstm_step"]
+            "mlstm_step", "mlstm_fwd_chunkwise_noalloc"]
+
+# Bytes of the fixed scratch array behind mlstm_fwd_chunkwise_noalloc (include/mlstm.h).
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class MlstmError(RuntimeError):
@@ -155,6 +162,42 @@ def mlstm_fwd_chunkwise(q, k, v, igate_pre, fgate_pre, chunk, h_dtype=None, C_in
         _DT[dt], _ptr(C_init), _ptr(n_init), _ptr(m_init), _ptr(h), _DT[h_dtype], _ptr(C_last),
         _ptr(n_last), _ptr(m_last), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(code, "mlstm_fwd_chunkwise")
+    return h, C_last, n_last, m_last
+
+
+def mlstm_fwd_chunkwise_noalloc(q, k, v, igate_pre, fgate_pre, chunk, out, C_init=None, n_init=None,
+                                m_init=None, stream=None):
+    """The chunkwise forward without any device allocation, for callers that cannot allocate
+    (a host application that owns all device memory, a serving loop where cudaMalloc could
+    synchronise the device): the library uses its own fixed scratch array.  The four outputs
+    (h, C_last, n_last, m_last) must be supplied in ``out`` -- this wrapper allocates nothing
+    either; h's dtype is taken from ``out``."""
+    B, NH, S, DQK = q.shape
+    DV = v.shape[-1]
+    dt = q.dtype
+    if dt not in _DT:
+        raise TypeError("q, k, v must be float32 or bfloat16")
+    _dev(q, "q", dt)
+    _dev(k, "k", dt, (B, NH, S, DQK))
+    _dev(v, "v", dt, (B, NH, S, DV))
+    _dev(igate_pre, "igate_pre", torch.float32, (B, NH, S))
+    _dev(fgate_pre, "fgate_pre", torch.float32, (B, NH, S))
+    if any(x is not None for x in (C_init, n_init, m_init)):
+        _dev(C_init, "C_init", torch.float32, (B, NH, DV, DQK))
+        _dev(n_init, "n_init", torch.float32, (B, NH, DQK))
+        _dev(m_init, "m_init", torch.float32, (B, NH))
+    h, C_last, n_last, m_last = out
+    if h.dtype not in _DT:
+        raise TypeError("h must be float32 or bfloat16")
+    _dev(h, "h", h.dtype, (B, NH, S, DV))
+    _dev(C_last, "C_last", torch.float32, (B, NH, DV, DQK))
+    _dev(n_last, "n_last", torch.float32, (B, NH, DQK))
+    _dev(m_last, "m_last", torch.float32, (B, NH))
+    code = _lib.mlstm_fwd_chunkwise_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(igate_pre), _ptr(fgate_pre), B, NH, S, DQK, DV, chunk,
+        _DT[dt], _ptr(C_init), _ptr(n_init), _ptr(m_init), _ptr(h), _DT[h.dtype], _ptr(C_last),
+        _ptr(n_last), _ptr(m_last), _stream(stream))
+    _check(code, "mlstm_fwd_chunkwise_noalloc")
     return h, C_last, n_last, m_last
 
 

@@ -328,4 +328,52 @@ mlstm_status mlstm_step(const void *q, const void *k, const void *v, const float
                                    B * NH, DQK, DV, (cudaStream_t)stream));
 }
 
+// ---------------------------------------------------------------- forward without allocation
+// The scratch of mlstm_fwd_chunkwise_noalloc: a fixed array in device memory, part of the
+// library's image, so that every GPU that loads the library holds it until the process exits.
+// Host code only ever sees a host-side stand-in for its name; the device address is resolved
+// per device with cudaGetSymbolAddress and passed to the kernels as an ordinary workspace.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MLSTM_NOALLOC_SCRATCH_BYTES];
+
+static void *g_noalloc_ptr[64];  // device address of g_noalloc_scratch, per device ordinal
+
+mlstm_status mlstm_fwd_chunkwise_noalloc(const void *q, const void *k, const void *v,
+                                         const float *igate_pre, const float *fgate_pre, int B,
+                                         int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt,
+                                         const float *C_init, const float *n_init,
+                                         const float *m_init, void *h, mlstm_dtype h_dt,
+                                         float *C_last, float *n_last, float *m_last,
+                                         void *stream) {
+  if (dt != MLSTM_F32 && dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
+  if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return MLSTM_ERR_SHAPE;
+  // sizes whose scratch would not fit in the fixed array are refused before anything runs
+  if (layout(B, NH, S, DQK, DV, chunk, dt).total > (size_t)MLSTM_NOALLOC_SCRATCH_BYTES)
+    return MLSTM_ERR_WORKSPACE;
+  if (mlstm_status st = check_device()) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    g_last_cuda_error = (int)cudaGetLastError();
+    return MLSTM_ERR_DEVICE;
+  }
+  if (dev < 0 || dev >= 64) return MLSTM_ERR_DEVICE;
+  // set-up, once per device, with that device current: the array's device address
+  void *scratch = __atomic_load_n(&g_noalloc_ptr[dev], __ATOMIC_ACQUIRE);
+  if (scratch == nullptr) {
+    const cudaError_t e = cudaGetSymbolAddress(&scratch, g_noalloc_scratch);
+    if (e != cudaSuccess || scratch == nullptr) {
+      g_last_cuda_error = (int)e;
+      cudaGetLastError();
+      return MLSTM_ERR_LAUNCH;
+    }
+    __atomic_store_n(&g_noalloc_ptr[dev], scratch, __ATOMIC_RELEASE);
+  }
+  // Everything the forward reads from its workspace is written by the same call first (the
+  // gate arrays, the chunk stabiliser, the copy of n_init) and the one word that must start
+  // at zero (the kernels' wait-error word) is cleared by the forward itself, so the stale
+  // contents of an earlier call never matter.
+  return mlstm_fwd_chunkwise(q, k, v, igate_pre, fgate_pre, B, NH, S, DQK, DV, chunk, dt, C_init,
+                             n_init, m_init, h, h_dt, C_last, n_last, m_last, scratch,
+                             (size_t)MLSTM_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 }  // extern "C"
