@@ -1,10 +1,12 @@
 """Benchmark of the mLSTM cell forward on one B300 (or N, one process per GPU).
 
 A step is one chunkwise forward of the 1.3B-style layer (B=4, NH=4, S=2048, d=512, chunk 64,
-bf16 q/k/v, fp32 gates, fp32 h) through the library: gate preprocessing, then the state
-passing and output stage.  The decode step (B=256, NH=8, d=256, fp32 state) is timed in its
-own loop and reported under "decode".  Inputs are synthetic (seeded) and resident in HBM;
-L2 is flushed between timed iterations (a 256 MiB write) outside the timed events.
+bf16 q/k/v, fp32 gates, fp32 h) through the library's mlstm_fwd_chunkwise: on the tensor-core
+path that is a single fused kernel (gate preprocessing, state passing and output).  The decode
+step (B=256, NH=8, d=256, fp32 state) is timed in its own loop and reported under "decode".
+Inputs are synthetic (seeded) and resident in HBM; L2 is flushed between timed iterations (a
+256 MiB write) outside the timed events.  SM clocks and throttle reasons are sampled during the
+timed region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -86,57 +88,102 @@ def load_peaks():
             "source": "fallback"}
 
 
+_NVML_LOOP = r"""
+import sys, time
+import pynvml as nvml
+nvml.nvmlInit()
+h = nvml.nvmlDeviceGetHandleByIndex(int(sys.argv[1]))
+period = float(sys.argv[2])
+get_reasons = getattr(nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+    nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+print("ready", flush=True)
+while True:
+    sm = nvml.nvmlDeviceGetClockInfo(h, nvml.NVML_CLOCK_SM)
+    mx = nvml.nvmlDeviceGetMaxClockInfo(h, nvml.NVML_CLOCK_SM)
+    print(time.time(), sm, mx, get_reasons(h), flush=True)
+    time.sleep(period)
+"""
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """SM clocks and throttle reasons sampled about every millisecond while the timed region
+    runs, by a separate process (NVML; nvidia-smi at 200 ms if NVML is unavailable); only the
+    samples taken inside the timed region are summarised."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+               "sw_power_cap": 0x4}
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_s: float = 0.001):
         self.gpu = gpu_index
+        self.period = period_s
+        self.samples = []  # (sm_mhz, max_mhz, reasons bitmask, wall time)
+        self.window = None
         self.proc = None
+        self.kind = None
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+            self.proc = subprocess.Popen([sys.executable, "-c", _NVML_LOOP, str(self.gpu), str(self.period)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            first = self.proc.stdout.readline()
+            if first.strip() != "ready":
+                raise RuntimeError("nvml sampler did not start")
+            self.kind = "nvml"
+        except Exception:  # noqa: BLE001
+            if self.proc is not None:
+                self.proc.kill()
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--id={self.gpu}",
+                     "--query-gpu=timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                     "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                     "clocks_event_reasons.sw_power_cap", "--format=csv,noheader,nounits", "-lms", "200"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.kind = "nvidia-smi"
+            except OSError:
+                self.proc = None
         return self
 
+    def mark(self, t0, t1):
+        self.window = (t0, t1)  # wall-clock time.time() bounds of the timed region
+
     def __exit__(self, *exc):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for ln in out.splitlines():
             try:
-                out, _ = self.proc.communicate(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+                if self.kind == "nvml":
+                    t, sm, mx, rs = ln.split()
+                    self.samples.append((float(sm), float(mx), int(rs), float(t)))
+                else:
+                    parts = [x.strip() for x in ln.split(",")]
+                    bits = [0x8, 0x40, 0x20, 0x4]
+                    mask = sum(b for b, v in zip(bits, parts[3:7]) if v.lower() == "active")
+                    self.samples.append((float(parts[1]), float(parts[2]), mask, None))
+            except (ValueError, IndexError):
+                continue
 
     def summary(self):
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in getattr(self, "lines", []):
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
+        sel, where = self.samples, "timed region"
+        if self.window is not None and self.kind == "nvml":
+            inside = [x for x in self.samples if self.window[0] <= x[3] <= self.window[1]]
+            if inside:
+                sel = inside
+            else:
+                where = "around the timed region (none fell inside it)"
+        elif self.kind != "nvml":
+            where = "while the timed region ran (nvidia-smi, 200 ms)"
+        if not sel:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        reasons = sorted(name for name, bit in self.REASONS.items() if any(x[2] & bit for x in sel))
+        return {"sm_mhz": statistics.median(x[0] for x in sel), "sm_max_mhz": max(x[1] for x in sel),
+                "reasons": reasons, "samples": len(sel), "sampled": where}
 
 
 def dist_setup():
@@ -177,11 +224,13 @@ def oracle_sample(w, heads: int):
     return inp
 
 
-def time_oracle(w, heads: int, reps: int = 1):
-    """Wall time of the oracle over `heads` head-sequences of workload w; tokens/s of the full
-    layer (each layer token needs NH head-tokens)."""
+def time_oracle(w, heads: int, reps: int = 1, s_len: int = None):
+    """Wall time of the oracle over `heads` head-sequences of workload w (the first s_len tokens
+    of each, default all); tokens/s of the full layer (each layer token needs NH head-tokens)."""
     import oracle
+    s_len = s_len or w.S
     inp = oracle_sample(w, heads)
+    inp = {key: val[:, :, :s_len] for key, val in inp.items()}
     oracle.load()
     times = []
     for _ in range(reps):
@@ -189,7 +238,7 @@ def time_oracle(w, heads: int, reps: int = 1):
         oracle.recurrent(**inp)
         times.append(time.perf_counter() - t0)
     cores = min(os.cpu_count() or 1, heads)
-    tps = heads * w.S / w.NH / statistics.median(times)
+    tps = heads * s_len / w.NH / statistics.median(times)
     return tps, cores, times
 
 
@@ -197,12 +246,18 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     heads = max(1, min(os.cpu_count() or 1, FWD.B * FWD.NH))
+    # each step is a bounded sample: every thread gets one head, and the sequence prefix is sized
+    # so that warm-up plus timed steps stay within about two and a half minutes
+    budget = min(2.0, 150.0 / max(1, args.steps + args.warmup))
+    _, _, t_cal = time_oracle(FWD, heads, s_len=min(FWD.S, 4 * FWD.chunk))
+    per_token = t_cal[0] / min(FWD.S, 4 * FWD.chunk)
+    s_len = int(min(FWD.S, max(FWD.chunk, budget / max(per_token, 1e-9))) // FWD.chunk * FWD.chunk)
     for _ in range(args.warmup):
-        time_oracle(FWD, 1)
-    tps, cores, times = time_oracle(FWD, heads, reps=args.steps)
+        time_oracle(FWD, heads, s_len=s_len)
+    tps, cores, times = time_oracle(FWD, heads, reps=args.steps, s_len=s_len)
     value = tps
-    sample = (f"{heads} of {FWD.B * FWD.NH} (batch, head) sequences of the {FWD.name}, full "
-              f"S={FWD.S}, per step; tokens/s scaled to the whole layer (x 1/NH)")
+    sample = (f"{heads} of {FWD.B * FWD.NH} (batch, head) sequences of the {FWD.name}, first {s_len} of "
+              f"S={FWD.S} tokens each, per step; tokens/s scaled to the whole layer (x 1/NH)")
     line = {
         "metric": "mLSTM chunkwise forward tokens/s (1.3B-style layer)", "value": value,
         "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -244,48 +299,48 @@ def run_ours(args, rank, local, world):
     stream = torch.cuda.current_stream()
 
     def step():
-        B.mlstm_fwd_gates(ig, fg, w.chunk, workspace=ws, outputs=False)
-        ev_mid.record(stream)
-        B.mlstm_fwd_from_gates(q, k, v, w.chunk, ws, (h, C, n, m))
+        B.mlstm_fwd_chunkwise(q, k, v, ig, fg, w.chunk, h_dtype=torch.float32, out=(h, C, n, m), workspace=ws)
 
-    ev_mid = torch.cuda.Event(enable_timing=True)
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     launches0 = B.mlstm_kernel_launches()
     with ClockSampler(local) as clk:
+        t_start = time.time()
         for i in range(args.steps):
             flush.zero_()  # evict the inputs from L2 (outside the timed events)
             starts[i].record(stream)
-            B.mlstm_fwd_gates(ig, fg, w.chunk, workspace=ws, outputs=False)
-            mids[i].record(stream)
-            B.mlstm_fwd_from_gates(q, k, v, w.chunk, ws, (h, C, n, m))
+            step()
             ends[i].record(stream)
         torch.cuda.synchronize()
+        clk.mark(t_start, time.time())
     launches_fwd = B.mlstm_kernel_launches() - launches0
     barrier(world)
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    main_ms = [s.elapsed_time(e) for s, e in zip(mids, ends)]
+    step_ms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
     ms = statistics.mean(step_ms)
     ms_max = max_over_ranks(ms, world)
     tokens = w.B * w.S
     value = tokens * world / (ms_max * 1e-3)
 
     flops = fwd_flops(w)
-    main_mean = statistics.mean(main_ms)
-    achieved_tf = flops / (main_mean * 1e-3) / 1e12
+    path = B.mlstm_fwd_path(w.B, w.NH, w.S, w.DQK, w.DV, w.chunk)
+    achieved_tf = flops / (ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved_tf, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved_tf / peaks["bf16_tflops"], "traffic": None,
-                "kernel": "state passing + output stage (mlstm_fwd_from_gates)",
-                "algorithmic_flops_per_launch": flops, "ms_per_launch": main_mean,
+                "unit": "TFLOP/s", "frac": achieved_tf / peaks["bf16_tflops"],
+                "traffic": captured_traffic("fwd_tc_kernel") if path >= 1 else None,
+                "kernel": ("fwd_tc_kernel (the whole forward: one launch)" if path >= 1
+                           else "gates + states + output kernels"),
+                "algorithmic_flops_per_launch": flops, "ms_per_launch": ms,
                 "peak_source": f"{peaks['source']} bf16 dense (burst); fp16 operands run at the same rate",
-                "hbm_gbs_of_algorithmic_bytes": fwd_bytes(w) / (main_mean * 1e-3) / 1e9}
+                "frac_of_sustained": achieved_tf / peaks["bf16_tflops_sustained"]
+                if peaks.get("bf16_tflops_sustained") else None,
+                "hbm_gbs_of_algorithmic_bytes": fwd_bytes(w) / (ms * 1e-3) / 1e9,
+                "hbm_frac_of_algorithmic_bytes": fwd_bytes(w) / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
 
     # ---- decode step: B=256, NH=8, d=256 state from a 512-token prefill through the library
     dw = DEC
@@ -417,7 +472,7 @@ def run_profile(kind: str):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -159,11 +159,15 @@ static mlstm_status check_fwd_args(const void *q, const void *k, const void *v, 
   return MLSTM_OK;
 }
 
-// Everything after kernel (a), on a workspace that kernel (a) has filled for these sizes.
+// Everything after kernel (a), on a workspace that kernel (a) has filled for these sizes -- or,
+// on the tensor-core path when ig is given, from the raw gate pre-activations (ig, fg, m_init),
+// whose preprocessing the fused kernel then does itself.
 static mlstm_status run_from_gates(const void *q, const void *k, const void *v, int B, int NH, int S,
                                    int DQK, int DV, int chunk, mlstm_dtype dt, const float *C_init,
                                    const float *n_init, void *h, mlstm_dtype h_dt, float *C_last,
-                                   float *n_last, float *m_last, void *workspace, cudaStream_t s) {
+                                   float *n_last, float *m_last, void *workspace, cudaStream_t s,
+                                   const float *ig = nullptr, const float *fg = nullptr,
+                                   const float *m_init = nullptr) {
   const Layout Lw = layout(B, NH, S, DQK, DV, chunk, dt);
   char *ws = (char *)workspace;
   float *gb = (float *)(ws + Lw.gb), *gx = (float *)(ws + Lw.gx), *gu = (float *)(ws + Lw.gu);
@@ -172,15 +176,14 @@ static mlstm_status run_from_gates(const void *q, const void *k, const void *v, 
   const int P = B * NH, NC = S / chunk;
   const bool bf16 = dt == MLSTM_BF16;
   if (Lw.tc) {
-    if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return launch_status(cudaGetLastError());
     if (n_init) {
       float *ncopy = (float *)(ws + Lw.ncopy);
       if (cudaMemcpyAsync(ncopy, n_init, sizeof(float) * (size_t)P * DQK, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
         return launch_status(cudaGetLastError());
       n_init = ncopy;
     }
-    return launch_status(launch_fwd_tc(q, k, v, h_dt == MLSTM_BF16, gb, gx, gu, cm, P, S, DQK, DV, C_init,
-                                         n_init, h, C_last, n_last, m_last, err, s));
+    return launch_status(launch_fwd_tc(q, k, v, h_dt == MLSTM_BF16, gb, gx, gu, cm, ig, fg, m_init, P, S, DQK,
+                                       DV, C_init, n_init, h, C_last, n_last, m_last, err, s));
   }
   if (mlstm_status st = launch_status(launch_states_simt(k, v, bf16, gb, gx, cm, P, S, chunk, DQK, DV, C_init,
                                                          n_init, Cs, ns, C_last, n_last, s)))
@@ -224,6 +227,9 @@ mlstm_status mlstm_fwd_chunkwise(const void *q, const void *k, const void *v, co
   const Layout Lw = layout(B, NH, S, DQK, DV, chunk, dt);
   char *ws = (char *)workspace;
   const int P = B * NH;
+  if (Lw.tc)  // the fused kernel preprocesses the gates itself
+    return run_from_gates(q, k, v, B, NH, S, DQK, DV, chunk, dt, C_init, n_init, h, h_dt, C_last, n_last,
+                          m_last, workspace, s, igate_pre, fgate_pre, m_init);
   if (mlstm_status st = launch_status(launch_gates(igate_pre, fgate_pre, P, S, chunk, m_init, (float *)(ws + Lw.gb),
                                                    (float *)(ws + Lw.gx), (float *)(ws + Lw.gu),
                                                    (float *)(ws + Lw.cm), nullptr, s)))

@@ -45,10 +45,10 @@
 // Optional timeline trace for performance analysis (build with -DMLSTM_TRACE): the SM clock at
 // fixed points of every role of CTA (0, 0), per chunk; read back with mlstm_trace_read.
 #ifdef MLSTM_TRACE
-__device__ long long g_trace[8][512][8];
-#define TRACE(role, k, ev)                                                              \
-  do {                                                                                  \
-    if (blockIdx.x == 0 && blockIdx.y == 0 && (k) < 512) g_trace[role][k][ev] = clock64(); \
+__device__ long long g_trace[2][8][512][8];
+#define TRACE(role, k, ev)                                                                            \
+  do {                                                                                                \
+    if (blockIdx.x < 2 && blockIdx.y == 0 && (k) < 512) g_trace[blockIdx.x][role][k][ev] = clock64(); \
   } while (0)
 extern "C" int mlstm_trace_read(long long *dst, size_t bytes) {
   return (int)cudaMemcpyFromSymbol(dst, g_trace, bytes < sizeof(g_trace) ? bytes : sizeof(g_trace));
@@ -87,18 +87,19 @@ struct Gate {
 };
 
 struct Smem {
-  uint64_t full[2], empty[2], bar_S[2], bar_nq[2];
-  uint64_t sfree, bar_U, bar_H, hfree, cready, opready, pready, fin;
-  uint64_t sx_full[2], sx_free[2], hx_full, hx_free;
+  uint64_t qk_full, qk_empty, v_full[2], v_empty[2], g_full[2], bar_nq[2];
+  uint64_t bar_S, sfree, bar_U, bar_H, hfree, cready, opready, pready, fin, n_ready;
+  uint64_t sx_full[2], sx_free[2], hx_full, hx_free, nqx_full[2], nqx_free[2];
   uint64_t grp[3];  // bounded group barriers of warpgroups 1, 2 and 3
   uint32_t tmem_base;
   int abort_flag;
-  Gate g[2];
-  float n[256];          // normaliser, this CTA's d_qk columns
-  float npart[1024];     // n-update partial sums of warpgroup 3
+  alignas(16) Gate g[2];
+  alignas(16) float n[256];       // normaliser, this CTA's d_qk columns (read as float4)
+  alignas(16) float npart[1024];  // n-update partial sums of warpgroup 3
   float nq[2][kL];       // n . q_r over this CTA's columns
   float nqx[2][32];      // partner's n . q_r for the rows finalised here (written remotely)
   float inv[2][kL];      // 1 / max(|den_r|, exp(-m_r))
+  float m_fin;           // stabiliser after the last chunk
 };
 
 __device__ __forceinline__ bool aborted(const Smem &sm) { return *(volatile const int *)&sm.abort_flag != 0; }
@@ -120,52 +121,101 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// Packed pairs of fp32 (Blackwell f32x2 arithmetic: one instruction for two lanes of data).
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// bf16 pair -> fp32 pair
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) { return f2pack(bf16_lo(w), bf16_hi(w)); }
+// fp32 pair -> fp16 pair (round to nearest)
+__device__ __forceinline__ uint32_t f2_to_h2(uint64_t x) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+  return pack_half2(lo, hi);
+}
+__device__ __forceinline__ float f2sum(uint64_t x) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+  return lo + hi;
+}
+
 template <int DH, bool PAIR, typename TO>
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
     const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
-    const __grid_constant__ CUtensorMap mapV, const float *__restrict__ gb, const float *__restrict__ gx,
-    const float *__restrict__ gu, const float *__restrict__ cm, int S, int DV, float scale,
-    const float *__restrict__ C_init, const float *__restrict__ n_init, TO *__restrict__ h,
-    float *__restrict__ C_last, float *__restrict__ n_last, float *__restrict__ m_last, int *__restrict__ err) {
+    const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapC,
+    const float *__restrict__ gb, const float *__restrict__ gx, const float *__restrict__ gu,
+    const float *__restrict__ cm, const float *__restrict__ igp, const float *__restrict__ fgp,
+    const float *__restrict__ m_init, int S, int DV, float scale, const float *__restrict__ C_init,
+    const float *__restrict__ n_init, TO *__restrict__ h, float *__restrict__ n_last, float *__restrict__ m_last,
+    int *__restrict__ err) {
   constexpr int D = PAIR ? 2 * DH : DH;  // d_qk
   constexpr int QB = DH * 128;           // bytes of a [64 x DH] 2-byte tile (DH / 64 swizzled blocks)
-  constexpr int STAGE = 2 * QB + 16384;  // q, k, v tiles of one chunk
   constexpr uint32_t kColC16 = DH;
   constexpr int NR = PAIR ? 32 : 64;     // output rows finalised per CTA
   static_assert(DH == 64 || DH == 128 || DH == 256, "DH");
+  // dynamic shared memory map (every region 1024-byte aligned)
+  constexpr int OFF_RQ = 0, OFF_RK = QB, OFF_BQ = 2 * QB, OFF_WK = 3 * QB, OFF_V = 4 * QB;
+  constexpr int OFF_P = OFF_V + 2 * 16384, OFF_SO = OFF_P + 8192, OFF_SX = OFF_SO + NR * 256;
+  constexpr int OFF_HX = OFF_SX + 16384;
 
   extern __shared__ uint8_t smem_dyn[];
   __shared__ Smem sm;
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-  uint8_t *const sP = base + 2 * STAGE;                                // fp16 P [64 x 64], K-major
-  float *const SX = reinterpret_cast<float *>(sP + 8192);              // [2][32][64] partner's S rows
-  float *const HX = reinterpret_cast<float *>(sP + 8192 + 16384);      // [128][32] partner's H^T cols
-#define STQ(s_) (base + (s_) * STAGE)
-#define STK(s_) (base + (s_) * STAGE + QB)
-#define STV(s_) (base + (s_) * STAGE + 2 * QB)
+  uint8_t *const sRQ = base + OFF_RQ;  // raw q of the chunk (bf16, TMA, 128-byte swizzle)
+  uint8_t *const sRK = base + OFF_RK;  // raw k
+  uint8_t *const sBQ = base + OFF_BQ;  // beta_r q_r, fp16 (B operand of the C q product)
+  uint8_t *const sWK = base + OFF_WK;  // w_j k_j, fp16 (B operand of the state update)
+  uint8_t *const sP = base + OFF_P;    // P, fp16 [64 x 64], K-major
+  float *const SO = reinterpret_cast<float *>(base + OFF_SO);  // this CTA's partial S rows [NR][64]
+  float *const SX = reinterpret_cast<float *>(base + OFF_SX);  // [2][32][64] partner's partial S rows
+  float *const HX = reinterpret_cast<float *>(base + OFF_HX);  // [128][32] partner's H^T columns
+#define STV(s_) (base + OFF_V + (s_) * 16384)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = PAIR ? (int)cluster_ctarank() : 0;
   const int atile = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int a0 = atile * kTile, c0 = rank * DH, p = blockIdx.y;
   const int NC = S / kL;
+  const int r_lo = PAIR ? 32 * rank : 0;  // first output row finalised here
+  const int prt = 1 - rank;
   const int *abort_ptr = &sm.abort_flag;
 
+  // The wait-error word starts at zero for this launch (a wait only gives up after about a
+  // second, long after the first CTA has started).
+  if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) *(volatile int *)err = 0;
   if (threadIdx.x == 0) {
+    mbar_init(&sm.qk_full, 1);
+    mbar_init(&sm.qk_empty, 1 + 256);  // the S MMA (commit) and the reads of warpgroups 2 and 3
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&sm.full[i], 2);
-      mbar_init(&sm.empty[i], 1);
-      mbar_init(&sm.bar_S[i], 1);
+      mbar_init(&sm.v_full[i], 1);
+      mbar_init(&sm.v_empty[i], 1);
+      mbar_init(&sm.g_full[i], 1);
       mbar_init(&sm.bar_nq[i], 128);
       mbar_init(&sm.sx_full[i], 1);
-      mbar_init(&sm.sx_free[i], 2);
+      mbar_init(&sm.sx_free[i], 4);
+      mbar_init(&sm.nqx_full[i], 1);
+      mbar_init(&sm.nqx_free[i], 4);
     }
+    mbar_init(&sm.bar_S, 1);
     mbar_init(&sm.sfree, 128);
     mbar_init(&sm.bar_U, 1);
     mbar_init(&sm.bar_H, 1);
     mbar_init(&sm.hfree, 128);
     mbar_init(&sm.cready, 128);
-    mbar_init(&sm.opready, 128);
+    mbar_init(&sm.opready, 256);  // warpgroup 3 (beta q, v) and warpgroup 2 (w k)
+    mbar_init(&sm.n_ready, 128);
     mbar_init(&sm.pready, 128);
     mbar_init(&sm.fin, 1);
     mbar_init(&sm.hx_full, 1);
@@ -183,32 +233,62 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
   tc_fence_after();
   if (PAIR) cluster_sync();  // the partner's barriers are initialised before any remote access
   const uint32_t tm = sm.tmem_base;
+  if (threadIdx.x == 0) TRACE(0, 511, 0);
 
   if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------------ TMA: q and k (one stage)
     if (lane == 0) {
       prefetch_tensormap(&mapQ);
       prefetch_tensormap(&mapK);
+      for (int k = 0; k < 2 && k < NC; ++k)
+#pragma unroll
+        for (int kb = 0; kb < DH / 64; ++kb) {
+          tma_prefetch_2d(&mapQ, c0 + kb * 64, p * S + k * kL);
+          tma_prefetch_2d(&mapK, c0 + kb * 64, p * S + k * kL);
+        }
+      int issued = 0;
+      for (int k = 0; k < NC; ++k) {
+        if (k >= 1 && !mbar_wait(&sm.qk_empty, (k - 1) & 1, err, 11, abort_ptr)) { set_abort(sm); break; }
+        if (aborted(sm)) break;
+        TRACE(0, k, 0);
+        mbar_arrive_expect_tx(&sm.qk_full, (uint32_t)(2 * QB));
+        const int row = p * S + k * kL;
+#pragma unroll
+        for (int kb = 0; kb < DH / 64; ++kb) {
+          tma_load_2d(sRQ + kb * 8192, &mapQ, c0 + kb * 64, row, &sm.qk_full);
+          tma_load_2d(sRK + kb * 8192, &mapK, c0 + kb * 64, row, &sm.qk_full);
+        }
+        if (k + 2 < NC)
+#pragma unroll
+          for (int kb = 0; kb < DH / 64; ++kb) {
+            tma_prefetch_2d(&mapQ, c0 + kb * 64, row + 2 * kL);
+            tma_prefetch_2d(&mapK, c0 + kb * 64, row + 2 * kL);
+          }
+        issued = k + 1;
+      }
+      if (issued > 0) mbar_wait(&sm.qk_full, (issued - 1) & 1, err, 19);  // the last copies land
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------------ TMA: v (two stages)
+    if (lane == 0) {
       prefetch_tensormap(&mapV);
       int issued = 0;
       for (int k = 0; k < NC; ++k) {
         const int s = k & 1;
-        if (k >= 2 && !mbar_wait(&sm.empty[s], ((k >> 1) - 1) & 1, err, 11, abort_ptr)) { set_abort(sm); break; }
+        if (k >= 2 && !mbar_wait(&sm.v_empty[s], ((k >> 1) - 1) & 1, err, 61, abort_ptr)) { set_abort(sm); break; }
         if (aborted(sm)) break;
-        TRACE(0, k, 0);
-        mbar_arrive_expect_tx(&sm.full[s], (uint32_t)STAGE);
+        mbar_arrive_expect_tx(&sm.v_full[s], 16384u);
         const int row = p * S + k * kL;
-#pragma unroll
-        for (int kb = 0; kb < DH / 64; ++kb) {
-          tma_load_2d(STQ(s) + kb * 8192, &mapQ, c0 + kb * 64, row, &sm.full[s]);
-          tma_load_2d(STK(s) + kb * 8192, &mapK, c0 + kb * 64, row, &sm.full[s]);
+        tma_load_2d(STV(s), &mapV, a0, row, &sm.v_full[s]);
+        tma_load_2d(STV(s) + 8192, &mapV, a0 + 64, row, &sm.v_full[s]);
+        if (k + 2 < NC) {
+          tma_prefetch_2d(&mapV, a0, row + 2 * kL);
+          tma_prefetch_2d(&mapV, a0 + 64, row + 2 * kL);
         }
-        tma_load_2d(STV(s), &mapV, a0, row, &sm.full[s]);
-        tma_load_2d(STV(s) + 8192, &mapV, a0 + 64, row, &sm.full[s]);
         issued = k + 1;
       }
-      // the copies of the last stages land before the CTA may leave
-      for (int k = issued >= 2 ? issued - 2 : 0; k < issued; ++k) mbar_wait(&sm.full[k & 1], (k >> 1) & 1, err, 19);
+      for (int k = issued >= 2 ? issued - 2 : 0; k < issued; ++k)
+        mbar_wait(&sm.v_full[k & 1], (k >> 1) & 1, err, 69);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -217,24 +297,26 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       const uint32_t id_X = idesc_f16(kTile, kL, 0, 0, 0);
       const uint32_t id_U = idesc_f16(kTile, DH, 0, /*a MN-major*/ 1, /*b MN-major*/ 1);
       const uint32_t id_P = idesc_f16(kTile, NR, 0, 1, 0);
-      const uint32_t sP_own = smem_u32(sP) + (PAIR ? rank * 32 * 128 : 0);
+      const uint32_t q_raw = smem_u32(sRQ), k_raw = smem_u32(sRK), q_b = smem_u32(sBQ), k_w = smem_u32(sWK);
+      const uint32_t p_own = smem_u32(sP) + r_lo * 128;
       int k = 0;
       for (; k < NC; ++k) {
         const int s = k & 1;
-        // S_k = Q K^T over this CTA's d_qk columns
-        if (!mbar_wait(&sm.full[s], (k >> 1) & 1, err, 12, abort_ptr)) break;
+        const uint32_t v_s = smem_u32(STV(s));
+        // S_k = Q K^T over this CTA's d_qk columns (raw bf16 inputs)
+        if (!mbar_wait(&sm.qk_full, k & 1, err, 12, abort_ptr)) break;
         if (k >= 1 && !mbar_wait(&sm.sfree, (k - 1) & 1, err, 13, abort_ptr)) break;
         tc_fence_after();
         TRACE(1, k, 0);
-        const uint32_t q_s = smem_u32(STQ(s)), k_s = smem_u32(STK(s)), v_s = smem_u32(STV(s));
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-          mma_f16_ss(tm + kColS, smem_desc(q_s + off, 16, 1024, kSwizzle128B),
-                     smem_desc(k_s + off, 16, 1024, kSwizzle128B), id_S, kk > 0);
+          mma_f16_ss(tm + kColS, smem_desc(q_raw + off, 16, 1024, kSwizzle128B),
+                     smem_desc(k_raw + off, 16, 1024, kSwizzle128B), id_S, kk > 0);
         }
-        mma_commit(&sm.bar_S[s]);
-        // H^T = C16 (beta q)^T and T += V^T (w k): need the state copy, the scaled operands and a free H
+        mma_commit(&sm.bar_S);
+        mma_commit(&sm.qk_empty);
+        // H^T = C16 (beta q)^T and T += V^T (w k): the state copy, the operands and a free H
         if (!mbar_wait(&sm.cready, k & 1, err, 14, abort_ptr)) break;
         TRACE(1, k, 1);
         if (!mbar_wait(&sm.opready, k & 1, err, 15, abort_ptr)) break;
@@ -245,13 +327,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-          mma_f16_ts(tm + kColH, tm + kColC16 + kk * 8, smem_desc(q_s + off, 16, 1024, kSwizzle128B), id_X,
-                     kk > 0);
+          mma_f16_ts(tm + kColH, tm + kColC16 + kk * 8, smem_desc(q_b + off, 16, 1024, kSwizzle128B), id_X, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < kL / 16; ++kk)
           mma_f16_ss(tm, smem_desc(v_s + kk * 2048, 8192, 1024, kSwizzle128B),
-                     smem_desc(k_s + kk * 2048, 8192, 1024, kSwizzle128B), id_U, 1);
+                     smem_desc(k_w + kk * 2048, 8192, 1024, kSwizzle128B), id_U, 1);
         mma_commit(&sm.bar_U);
         // H^T[:, own rows] += V^T P^T
         if (!mbar_wait(&sm.pready, k & 1, err, 17, abort_ptr)) break;
@@ -259,10 +340,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kL / 16; ++kk)
-          mma_f16_ss(tm + kColH + (PAIR ? rank * 32 : 0), smem_desc(v_s + kk * 2048, 8192, 1024, kSwizzle128B),
-                     smem_desc(sP_own + kk * 32, 16, 1024, kSwizzle128B), id_P, 1);
+          mma_f16_ss(tm + kColH + r_lo, smem_desc(v_s + kk * 2048, 8192, 1024, kSwizzle128B),
+                     smem_desc(p_own + kk * 32, 16, 1024, kSwizzle128B), id_P, 1);
         mma_commit(&sm.bar_H);
-        mma_commit(&sm.empty[s]);
+        mma_commit(&sm.v_empty[s]);
       }
       if (k < NC) set_abort(sm);
       mma_commit(&sm.fin);  // completes once every MMA issued above has finished
@@ -271,18 +352,59 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
   } else if (warp == 2) {
     // ------------------------------------------------------------------ gate factors
     float sigma = 0.f;  // frame of T entering the chunk: C = exp(sigma) T
+    float m_chain = m_init ? m_init[p] : 0.f;  // stabiliser entering the chunk (raw-gate mode)
     for (int k = 0; k < NC; ++k) {
       const int s = k & 1;
-      if (k >= 2 && !mbar_wait(&sm.empty[s], ((k >> 1) - 1) & 1, err, 41, abort_ptr)) { set_abort(sm); break; }
+      // the factors of chunk k share the lifetime of v stage s (free once PV of chunk k-2 is done)
+      if (k >= 2 && !mbar_wait(&sm.v_empty[s], ((k >> 1) - 1) & 1, err, 41, abort_ptr)) { set_abort(sm); break; }
       if (aborted(sm)) break;
       const size_t tok0 = (size_t)p * S + (size_t)k * kL;
-      const float m_in = cm[(size_t)p * (NC + 1) + k], m_out = cm[(size_t)p * (NC + 1) + k + 1];
-      float bb[2], xx[2], uu[2];
+      // b, x = i~ - b and the running max u for rows 2 lane and 2 lane + 1, and the chunk's
+      // stabiliser chain m_out = b_L + max(m_in, u_L)
+      float bb[2], xx[2], uu[2], m_in, m_out;
+      if (igp != nullptr) {
+        // from the raw pre-activations (the same operations, in the same order, as the gate kernel)
+        const float2 f2 = *reinterpret_cast<const float2 *>(fgp + tok0 + 2 * lane);
+        const float2 i2 = *reinterpret_cast<const float2 *>(igp + tok0 + 2 * lane);
+        float lf0 = log_sigmoid(f2.x), lf1 = log_sigmoid(f2.y);
+        float bsum = lf0;
+        bsum += lf1;
+        lf1 = bsum;
+        float incl = bsum;
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        bb[i] = gb[tok0 + 32 * i + lane];
-        xx[i] = gx[tok0 + 32 * i + lane];
-        uu[i] = gu[tok0 + 32 * i + lane];
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const float excl = incl - bsum;
+        bb[0] = lf0 + excl;
+        bb[1] = lf1 + excl;
+        xx[0] = i2.x - bb[0];
+        xx[1] = i2.y - bb[1];
+        float imax = fmaxf(fmaxf(-INFINITY, xx[0]), xx[1]);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, imax, o);
+          if (lane >= o) imax = fmaxf(imax, y);
+        }
+        float run = __shfl_up_sync(0xffffffffu, imax, 1);
+        if (lane == 0) run = -INFINITY;
+        run = fmaxf(run, xx[0]);
+        uu[0] = run;
+        run = fmaxf(run, xx[1]);
+        uu[1] = run;
+        m_in = m_chain;
+        m_out = __shfl_sync(0xffffffffu, bb[1], 31) + fmaxf(m_in, __shfl_sync(0xffffffffu, uu[1], 31));
+        m_chain = m_out;
+      } else {
+        m_in = cm[(size_t)p * (NC + 1) + k];
+        m_out = cm[(size_t)p * (NC + 1) + k + 1];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          bb[i] = gb[tok0 + 2 * lane + i];
+          xx[i] = gx[tok0 + 2 * lane + i];
+          uu[i] = gu[tok0 + 2 * lane + i];
+        }
       }
       const float bl = __shfl_sync(0xffffffffu, bb[1], 31);
       const float log_alpha = bl + m_in - m_out;  // <= 0
@@ -291,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       Gate &g = sm.g[s];
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
-        const int r = 32 * i + lane;
+        const int r = 2 * lane + i;
         const float mr = fmaxf(m_in, uu[i]);
         g.mr[r] = mr;
         g.floor_[r] = __expf(-(bb[i] + mr));
@@ -301,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
         g.wt[r] = __expf(bl + xx[i] - m_out) * scale;
       }
       if (lane == 0) {
+        if (k == NC - 1) sm.m_fin = m_out;
         g.alpha = __expf(log_alpha);
         g.fr_c = __expf(sigma);
         g.fr_w = __expf(sigma + log_alpha);
@@ -311,167 +434,237 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       __syncwarp();
       if (lane == 0) {
         TRACE(2, k, 0);
-        mbar_arrive(&sm.full[s]);
+        mbar_arrive(&sm.g_full[s]);
       }
     }
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------------ warpgroup 1: P and h
+    // Software-pipelined over chunks: the H columns of chunk k and the S rows of chunk k+1 are
+    // read and sent to the partner before the partner's halves of either are waited for.
     const int t = threadIdx.x - 128;  // tensor-memory lane = d_v row within the tile
     const int q4 = warp & 3;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const int r_s = 16 * q4 + (lane & 15);  // S row held by this lane (M = 64 layout, lanes < 16)
     const bool own_rows = !PAIR || ((q4 >> 1) == rank);
-    const int r_lo = PAIR ? 32 * rank : 0;
-    const int prt = 1 - rank;
+    constexpr int TPR = 128 / NR;  // P formation: threads per row (4 with a pair, 2 without)
+    constexpr int SEG = kL / TPR;  // columns per thread (16 or 32)
+    const int pi = t / TPR, pseg = t % TPR;
+    const int pr = r_lo + pi;  // the row this thread forms
     uint32_t gph = 0;
-    for (int k = 0; k < NC; ++k) {
-      const int s = k & 1, par = k & 1;
-      const size_t tok0 = (size_t)p * S + (size_t)k * kL;
-      if (!mbar_wait(&sm.full[s], (k >> 1) & 1, err, 21, abort_ptr)) { set_abort(sm); break; }
-      if (!mbar_wait(&sm.bar_S[s], (k >> 1) & 1, err, 22, abort_ptr)) { set_abort(sm); break; }
-      if (t == 0) TRACE(3, k, 0);
+
+    // S rows of chunk kk: own rows -> SO, the partner's rows -> partner's SX
+    auto s_read = [&](int kk) -> bool {
+      const int s = kk & 1, par = kk & 1;
+      if (!mbar_wait(&sm.g_full[s], (kk >> 1) & 1, err, 21, abort_ptr)) return false;
+      if (!mbar_wait(&sm.bar_S, kk & 1, err, 22, abort_ptr)) return false;
+      if (t == 0) TRACE(3, kk, 0);
       tc_fence_after();
-      float srow[kL];
-      {
-        uint32_t u[4][16];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld16(tm + lane_base + kColS + 16 * c, u[c]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 16; ++i) srow[16 * c + i] = __uint_as_float(u[c][i]);
-      }
+      uint32_t u[2][32];
+      tmem_ld32(tm + lane_base + kColS, u[0]);
+      tmem_ld32(tm + lane_base + kColS + 32, u[1]);
+      tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&sm.sfree);
-      if (!mbar_wait(&sm.bar_nq[s], (k >> 1) & 1, err, 23, abort_ptr)) { set_abort(sm); break; }
-      if (t == 0) TRACE(3, k, 1);
-      if (PAIR && !own_rows) {
-        // partial S rows and n.q of the partner's rows -> partner
-        if (k >= 2 && !mbar_wait_cluster(&sm.sx_free[par], ((k >> 1) - 1) & 1, err, 24, abort_ptr)) {
-          set_abort(sm);
-          break;
+      if (own_rows) {
+        if (lane < 16) {
+          const int i = r_s - r_lo;
+          float *dst = SO + i * 64;
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            *reinterpret_cast<float4 *>(dst + 4 * (c ^ (i & 7))) =
+                make_float4(__uint_as_float(u[c >> 3][(4 * c) & 31]), __uint_as_float(u[c >> 3][(4 * c + 1) & 31]),
+                            __uint_as_float(u[c >> 3][(4 * c + 2) & 31]), __uint_as_float(u[c >> 3][(4 * c + 3) & 31]));
         }
+      } else if (PAIR) {
+        if (kk >= 2 && !mbar_wait_cluster(&sm.sx_free[par], ((kk >> 1) - 1) & 1, err, 24, abort_ptr)) return false;
         if (lane < 16) {
           const int rr = r_s - 32 * prt;
           const uint32_t rbar = mapa_shared(smem_u32(&sm.sx_full[par]), prt);
           const uint32_t dst = mapa_shared(smem_u32(SX + (par * 32 + rr) * 64), prt);
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            st_async_v4(dst + ((i ^ (rr & 7)) << 4), srow[4 * i], srow[4 * i + 1], srow[4 * i + 2], srow[4 * i + 3],
-                        rbar);
-          st_async_f32(mapa_shared(smem_u32(&sm.nqx[par][rr]), prt), sm.nq[s][r_s], rbar);
+          for (int c = 0; c < 16; ++c)
+            st_async_v4(dst + ((c ^ (rr & 7)) << 4), __uint_as_float(u[c >> 3][(4 * c) & 31]),
+                        __uint_as_float(u[c >> 3][(4 * c + 1) & 31]), __uint_as_float(u[c >> 3][(4 * c + 2) & 31]),
+                        __uint_as_float(u[c >> 3][(4 * c + 3) & 31]), rbar);
         }
-      } else {
-        if (PAIR) {
-          if (lane == 0 && q4 == 2 * rank) mbar_arrive_expect_tx(&sm.sx_full[par], 32 * 64 * 4 + 32 * 4);
-          if (!mbar_wait_cluster(&sm.sx_full[par], (k >> 1) & 1, err, 25, abort_ptr)) { set_abort(sm); break; }
-          if (t == 0) TRACE(3, k, 2);
+      }
+      if (t == 0) TRACE(6, kk, 1);
+      return true;
+    };
+
+    // P rows of chunk kk (needs SO of every warp: call after a group barrier) and their 1/den
+    auto p_form = [&](int kk) -> bool {
+      const int s = kk & 1, par = kk & 1;
+      if (PAIR) {
+        if (t == 0) {
+          mbar_arrive_expect_tx(&sm.sx_full[par], 32 * 64 * 4);
+          mbar_arrive_expect_tx(&sm.nqx_full[par], 32 * 4);
         }
-        if (lane < 16) {
-          const Gate &g = sm.g[s];
-          float nqf = sm.nq[s][r_s];
+        if (!mbar_wait_cluster(&sm.sx_full[par], (kk >> 1) & 1, err, 25, abort_ptr)) return false;
+        if (!mbar_wait_cluster(&sm.nqx_full[par], (kk >> 1) & 1, err, 30, abort_ptr)) return false;
+        if (t == 0) TRACE(3, kk, 1);
+      }
+      if (!mbar_wait(&sm.bar_nq[par], (kk >> 1) & 1, err, 23, abort_ptr)) return false;
+      const Gate &g = sm.g[s];
+      const float mrr = g.mr[pr];
+      const float *so = SO + pi * 64;
+      const float *sx = SX + (par * 32 + pi) * 64;
+      float den = 0.f;
+#pragma unroll
+      for (int h16 = 0; h16 < SEG / 16; ++h16) {
+        const int j0 = SEG * pseg + 16 * h16;  // first column of this block
+        float sv[16], xv[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int c4 = j0 / 4 + q;
+          float4 a = *reinterpret_cast<const float4 *>(so + 4 * (c4 ^ (pi & 7)));
           if (PAIR) {
-            const int rr = r_s - 32 * rank;
-            const float *src = SX + (par * 32 + rr) * 64;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float4 v4 = *reinterpret_cast<const float4 *>(src + 4 * (i ^ (rr & 7)));
-              srow[4 * i] += v4.x;
-              srow[4 * i + 1] += v4.y;
-              srow[4 * i + 2] += v4.z;
-              srow[4 * i + 3] += v4.w;
-            }
-            nqf += sm.nqx[par][rr];
+            const float4 b = *reinterpret_cast<const float4 *>(sx + 4 * (c4 ^ (pi & 7)));
+            a.x += b.x;
+            a.y += b.y;
+            a.z += b.z;
+            a.w += b.w;
           }
-          const float mrr = g.mr[r_s];
-          float den = 0.f;
-          uint8_t *prow = sP + r_s * 128;
-#pragma unroll
-          for (int c8 = 0; c8 < kL / 8; ++c8) {
-            float pv[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int j = c8 * 8 + i;
-              pv[i] = (j <= r_s) ? srow[j] * scale * __expf(g.xg[j] - mrr) : 0.f;
-              den += pv[i];
-            }
-            uint4 w4;
-            w4.x = pack_half2(pv[0], pv[1]);
-            w4.y = pack_half2(pv[2], pv[3]);
-            w4.z = pack_half2(pv[4], pv[5]);
-            w4.w = pack_half2(pv[6], pv[7]);
-            *reinterpret_cast<uint4 *>(prow + ((c8 ^ (r_s & 7)) << 4)) = w4;
-          }
-          den += g.beta[r_s] * nqf;
-          sm.inv[par][r_s] = 1.f / fmaxf(fabsf(den), g.floor_[r_s]);
+          const float4 xq = *reinterpret_cast<const float4 *>(&g.xg[j0 + 4 * q]);
+          sv[4 * q] = a.x;
+          sv[4 * q + 1] = a.y;
+          sv[4 * q + 2] = a.z;
+          sv[4 * q + 3] = a.w;
+          xv[4 * q] = xq.x;
+          xv[4 * q + 1] = xq.y;
+          xv[4 * q + 2] = xq.z;
+          xv[4 * q + 3] = xq.w;
         }
-        if (PAIR) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&sm.sx_free[par]), prt));
+        float pv[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float pe = sv[e] * scale * __expf(xv[e] - mrr);
+          pv[e] = (j0 + e <= pr) ? pe : 0.f;
+        }
+        float d8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) d8[e] = pv[e] + pv[e + 8];
+        den += ((d8[0] + d8[4]) + (d8[1] + d8[5])) + ((d8[2] + d8[6]) + (d8[3] + d8[7]));
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int cb = j0 / 8 + hh;  // 16-byte chunk of the P row (8 fp16 columns)
+          uint4 w4;
+          w4.x = pack_half2(pv[8 * hh], pv[8 * hh + 1]);
+          w4.y = pack_half2(pv[8 * hh + 2], pv[8 * hh + 3]);
+          w4.z = pack_half2(pv[8 * hh + 4], pv[8 * hh + 5]);
+          w4.w = pack_half2(pv[8 * hh + 6], pv[8 * hh + 7]);
+          *reinterpret_cast<uint4 *>(sP + pr * 128 + ((cb ^ (pr & 7)) << 4)) = w4;
+        }
+      }
+#pragma unroll
+      for (int o = 1; o < TPR; o <<= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+      if (pseg == 0) {
+        // denominator of row pr: intra-chunk part + beta_r n.q_r (both halves of d_qk with a pair)
+        float nqf = sm.nq[par][pr];
+        if (PAIR) nqf += sm.nqx[par][pi];
+        const float dn = den + g.beta[pr] * nqf;
+        sm.inv[par][pr] = 1.f / fmaxf(fabsf(dn), g.floor_[pr]);
+      }
+      if (PAIR) {
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_remote(mapa_shared(smem_u32(&sm.sx_free[par]), prt));
+          mbar_arrive_remote(mapa_shared(smem_u32(&sm.nqx_free[par]), prt));
         }
       }
       fence_proxy_async_smem();
-      if (t == 0) TRACE(3, k, 3);
+      if (t == 0) TRACE(3, kk, 2);
       mbar_arrive(&sm.pready);
-      // inv[] of this chunk visible to the whole warpgroup
-      if (!group_sync(&sm.grp[0], gph, err, 29, abort_ptr)) { set_abort(sm); break; }
-      // -------------------------------- epilogue: h rows of this CTA
-      if (!mbar_wait(&sm.bar_H, k & 1, err, 26, abort_ptr)) { set_abort(sm); break; }
-      if (t == 0) TRACE(3, k, 4);
+      return true;
+    };
+
+    bool ok = NC == 0 || (s_read(0) && group_sync(&sm.grp[0], gph, err, 20, abort_ptr) && p_form(0));
+    for (int k = 0; ok && k < NC; ++k) {
+      const int par = k & 1;
+      const size_t tok0 = (size_t)p * S + (size_t)k * kL;
+      // H^T of chunk k: read, free the accumulator, send the partner's columns
+      if (!mbar_wait(&sm.bar_H, k & 1, err, 26, abort_ptr)) { ok = false; break; }
+      if (t == 0) TRACE(3, k, 3);
       tc_fence_after();
-      float hv[kL];
-      {
-        uint32_t u[4][16];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld16(tm + lane_base + kColH + 16 * c, u[c]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 16; ++i) hv[16 * c + i] = __uint_as_float(u[c][i]);
-      }
-      tc_fence_before();
-      mbar_arrive(&sm.hfree);
       float own[NR];
-      if (PAIR) {
-        if (k >= 1 && !mbar_wait_cluster(&sm.hx_free, (k - 1) & 1, err, 27, abort_ptr)) { set_abort(sm); break; }
-        const uint32_t rbar = mapa_shared(smem_u32(&sm.hx_full), prt);
-        const uint32_t dst = mapa_shared(smem_u32(HX + t * 32), prt);
+      {
+        uint32_t u[2][32];
+        tmem_ld32(tm + lane_base + kColH, u[0]);
+        tmem_ld32(tm + lane_base + kColH + 32, u[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&sm.hfree);
+        if (PAIR) {
+          if (k >= 1 && !mbar_wait_cluster(&sm.hx_free, (k - 1) & 1, err, 27, abort_ptr)) { ok = false; break; }
+          const uint32_t rbar = mapa_shared(smem_u32(&sm.hx_full), prt);
+          const uint32_t dst = mapa_shared(smem_u32(HX + t * 32), prt);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float e[4];
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t *src = rank ? u[0] : u[1];  // the partner's 32 rows
+            st_async_v4(dst + ((i ^ (t & 7)) << 4), __uint_as_float(src[4 * i]), __uint_as_float(src[4 * i + 1]),
+                        __uint_as_float(src[4 * i + 2]), __uint_as_float(src[4 * i + 3]), rbar);
+          }
 #pragma unroll
-          for (int j = 0; j < 4; ++j) e[j] = rank ? hv[4 * i + j] : hv[32 + 4 * i + j];
-          st_async_v4(dst + ((i ^ (t & 7)) << 4), e[0], e[1], e[2], e[3], rbar);
+          for (int i = 0; i < 32; ++i) own[i] = __uint_as_float(rank ? u[1][i] : u[0][i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            own[i] = __uint_as_float(u[0][i]);
+            own[32 + i] = __uint_as_float(u[1][i]);
+          }
         }
+      }
+      if (t == 0) TRACE(6, k, 6);
+      // With a pair, P of the next chunk is formed now (its S rows read and exchanged), so that
+      // the exchange of the H columns overlaps it and PV of the next chunk can start earlier.
+      if (PAIR && k + 1 < NC) {
+        if (!s_read(k + 1) || !group_sync(&sm.grp[0], gph, err, 20, abort_ptr) || !p_form(k + 1)) {
+          ok = false;
+          break;
+        }
+      }
+      if (PAIR) {
         if (t == 0) mbar_arrive_expect_tx(&sm.hx_full, 128 * 32 * 4);
-        if (!mbar_wait_cluster(&sm.hx_full, k & 1, err, 28, abort_ptr)) { set_abort(sm); break; }
-        if (t == 0) TRACE(3, k, 5);
+        if (!mbar_wait_cluster(&sm.hx_full, k & 1, err, 28, abort_ptr)) { ok = false; break; }
+        if (t == 0) TRACE(3, k, 4);
         const float *src = HX + t * 32;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float4 v4 = *reinterpret_cast<const float4 *>(src + 4 * (i ^ (t & 7)));
-          own[4 * i] = (rank ? hv[32 + 4 * i] : hv[4 * i]) + v4.x;
-          own[4 * i + 1] = (rank ? hv[32 + 4 * i + 1] : hv[4 * i + 1]) + v4.y;
-          own[4 * i + 2] = (rank ? hv[32 + 4 * i + 2] : hv[4 * i + 2]) + v4.z;
-          own[4 * i + 3] = (rank ? hv[32 + 4 * i + 3] : hv[4 * i + 3]) + v4.w;
+          own[4 * i] += v4.x;
+          own[4 * i + 1] += v4.y;
+          own[4 * i + 2] += v4.z;
+          own[4 * i + 3] += v4.w;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&sm.hx_free), prt));
-      } else {
-#pragma unroll
-        for (int i = 0; i < NR; ++i) own[i] = hv[i];
       }
+      // inv[] of chunk k was formed by every warp before the last group barrier, except for the
+      // last chunk of a pair and every chunk without one
+      if ((!PAIR || k + 1 == NC) && !group_sync(&sm.grp[0], gph, err, 29, abort_ptr)) { ok = false; break; }
+      if (t == 0) TRACE(6, k, 7);
       TO *hp = h + (tok0 + r_lo) * DV + a0 + t;
 #pragma unroll
       for (int i = 0; i < NR; ++i) hp[(size_t)i * DV] = from_f32<TO>(own[i] * sm.inv[par][r_lo + i]);
-      if (t == 0) TRACE(3, k, 6);
+      if (t == 0) TRACE(3, k, 5);
+      if (!PAIR && k + 1 < NC) {
+        // no partner: the next S rows and P after the stores (keeps the 64 output rows out of registers)
+        if (!s_read(k + 1) || !group_sync(&sm.grp[0], gph, err, 20, abort_ptr) || !p_form(k + 1)) {
+          ok = false;
+          break;
+        }
+      }
     }
+    if (!ok) set_abort(sm);
   } else if (warp >= 8 && warp < 12) {
     // ------------------------------------------------------------------ warpgroup 2: state copy
     const int t = threadIdx.x - 256;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    constexpr int KCPR = DH / 8;     // 16-byte chunks per row of k
+    constexpr int KRG = 128 / KCPR;  // rows handled at once (column layout)
+    const int kcc = t % KCPR, krg = t / KCPR;
+    const int kcolb = (kcc >> 3) * 8192, kc8 = kcc & 7;
+    uint32_t gph2 = 0;
     for (int c = 0; c < DH; c += 16) {
       uint32_t r[16];
 #pragma unroll
@@ -480,11 +673,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       tmem_st16(tm + lane_base + c, r);
     }
     tmem_wait_st();
+    if (t == 0) TRACE(4, 511, 0);
     float sig_last = 0.f;
     bool ok = true;
     for (int k = 0; k < NC; ++k) {
       const int s = k & 1;
-      if (!mbar_wait(&sm.full[s], (k >> 1) & 1, err, 31, abort_ptr)) { ok = false; break; }
+      if (!mbar_wait(&sm.g_full[s], (k >> 1) & 1, err, 31, abort_ptr)) { ok = false; break; }
       if (k >= 1 && !mbar_wait(&sm.bar_U, (k - 1) & 1, err, 32, abort_ptr)) { ok = false; break; }
       if (t == 0) TRACE(4, k, 0);
       tc_fence_after();
@@ -492,201 +686,249 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       const float fr_c = g.fr_c, fr_w = g.fr_w;
       const bool lazy = g.lazy != 0;
       sig_last = g.sig_next;
-#pragma unroll 1
-      for (int c = 0; c < DH; c += 32) {
-        uint32_t u0[16], u1[16];
-        tmem_ld16(tm + lane_base + c, u0);
-        tmem_ld16(tm + lane_base + c + 16, u1);
+      if (lazy) {
+        // C16 = fp16(exp(sigma) T): the next 32 columns load while the current ones convert
+        uint32_t ua[32], ub[32];
+        tmem_ld32(tm + lane_base, ua);
         tmem_wait_ld();
-        uint32_t hv[16];
+#pragma unroll 1
+        for (int c = 0; c < DH; c += 64) {
+          tmem_ld32(tm + lane_base + c + 32, ub);
+          {
+            uint32_t hv[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          hv[i] = pack_half2(__uint_as_float(u0[2 * i]) * fr_c, __uint_as_float(u0[2 * i + 1]) * fr_c);
-          hv[8 + i] = pack_half2(__uint_as_float(u1[2 * i]) * fr_c, __uint_as_float(u1[2 * i + 1]) * fr_c);
+            for (int i = 0; i < 16; ++i)
+              hv[i] = pack_half2(__uint_as_float(ua[2 * i]) * fr_c, __uint_as_float(ua[2 * i + 1]) * fr_c);
+            tmem_st16(tm + lane_base + kColC16 + c / 2, hv);
+          }
+          tmem_wait_ld();
+          if (c + 64 < DH) tmem_ld32(tm + lane_base + c + 64, ua);
+          {
+            uint32_t hv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              hv[i] = pack_half2(__uint_as_float(ub[2 * i]) * fr_c, __uint_as_float(ub[2 * i + 1]) * fr_c);
+            tmem_st16(tm + lane_base + kColC16 + c / 2 + 16, hv);
+          }
+          tmem_wait_ld();
         }
-        if (!lazy) {
+      } else {
+        // eager: also write the decayed state back to frame 0
+#pragma unroll 1
+        for (int c = 0; c < DH; c += 32) {
+          uint32_t u[32];
+          tmem_ld32(tm + lane_base + c, u);
+          tmem_wait_ld();
+          uint32_t hv[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            hv[i] = pack_half2(__uint_as_float(u[2 * i]) * fr_c, __uint_as_float(u[2 * i + 1]) * fr_c);
+          tmem_st16(tm + lane_base + kColC16 + c / 2, hv);
+          uint32_t w0[16], w1[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            u0[i] = __float_as_uint(__uint_as_float(u0[i]) * fr_w);
-            u1[i] = __float_as_uint(__uint_as_float(u1[i]) * fr_w);
+            w0[i] = __float_as_uint(__uint_as_float(u[i]) * fr_w);
+            w1[i] = __float_as_uint(__uint_as_float(u[16 + i]) * fr_w);
           }
-          tmem_st16(tm + lane_base + c, u0);
-          tmem_st16(tm + lane_base + c + 16, u1);
+          tmem_st16(tm + lane_base + c, w0);
+          tmem_st16(tm + lane_base + c + 16, w1);
         }
-        tmem_st16(tm + lane_base + kColC16 + c / 2, hv);
       }
       tmem_wait_st();
       tc_fence_before();
       if (t == 0) TRACE(4, k, 1);
       mbar_arrive(&sm.cready);
+      // ---- k: n-update partial sums and w_j k_j (frame of T) in fp16 (column layout)
+      if (!mbar_wait(&sm.qk_full, k & 1, err, 36, abort_ptr)) { ok = false; break; }
+      const float alpha = g.alpha;
+      {
+        uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll 4
+        for (int i = 0; i < 64 / KRG; ++i) {
+          const int j = krg + KRG * i;
+          const int off = kcolb + j * 128 + ((kc8 ^ (j & 7)) << 4);
+          const uint4 raw = *reinterpret_cast<const uint4 *>(sRK + off);
+          const uint64_t wt2 = f2pack(g.wt[j], g.wt[j]), wk2 = f2pack(g.wk[j], g.wk[j]);
+          const uint64_t x0 = bf2_to_f2(raw.x), x1 = bf2_to_f2(raw.y), x2 = bf2_to_f2(raw.z), x3 = bf2_to_f2(raw.w);
+          acc[0] = f2fma(wt2, x0, acc[0]);
+          acc[1] = f2fma(wt2, x1, acc[1]);
+          acc[2] = f2fma(wt2, x2, acc[2]);
+          acc[3] = f2fma(wt2, x3, acc[3]);
+          uint4 o4;
+          o4.x = f2_to_h2(f2mul(x0, wk2));
+          o4.y = f2_to_h2(f2mul(x1, wk2));
+          o4.z = f2_to_h2(f2mul(x2, wk2));
+          o4.w = f2_to_h2(f2mul(x3, wk2));
+          *reinterpret_cast<uint4 *>(sWK + off) = o4;
+        }
+        mbar_arrive(&sm.qk_empty);  // raw k is no longer read here
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          *reinterpret_cast<uint64_t *>(&sm.npart[krg * DH + kcc * 8 + 2 * e]) = acc[e];
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&sm.opready);
+      // ---- n after chunk k: once warpgroup 3 has used n before it (n . q) and every partial is in
+      if (!mbar_wait(&sm.bar_nq[k & 1], (k >> 1) & 1, err, 37, abort_ptr)) { ok = false; break; }
+      if (!group_sync(&sm.grp[1], gph2, err, 38, abort_ptr)) { ok = false; break; }
+      for (int c = t; c < DH; c += 128) {
+        float a = 0.f;
+#pragma unroll
+        for (int gi = 0; gi < KRG; ++gi) a += sm.npart[gi * DH + c];
+        sm.n[c] = alpha * sm.n[c] + a;
+      }
+      if (!group_sync(&sm.grp[1], gph2, err, 39, abort_ptr)) { ok = false; break; }  // partials read
+      mbar_arrive(&sm.n_ready);
+    }
+    if (ok && atile == 0) {
+      for (int c = t; c < DH; c += 128) n_last[(size_t)p * D + c0 + c] = sm.n[c];
+      if (rank == 0 && t == 0) m_last[p] = sm.m_fin;
     }
     if (!ok) set_abort(sm);
     // final state C_last = exp(sigma) T, transposed through shared memory for coalesced stores
     if (ok && !mbar_wait(&sm.bar_U, (NC - 1) & 1, err, 33, abort_ptr)) ok = false;
+    if (t == 0) TRACE(4, 511, 1);
     if (ok) {
+      // C_last = exp(sigma) T, 32 columns at a time through two swizzled staging tiles
+      // [128 rows x 128 bytes] in the (now unused) raw q/k buffers, stored by TMA
       tc_fence_after();
       const float fr = __expf(sig_last);
-      float *buf = reinterpret_cast<float *>(base + (((NC - 1) & 1) ^ 1) * STAGE);  // stage unused by chunk NC-1
-      const int wq = warp & 3;
-      uint32_t gph = 0;
 #pragma unroll 1
-      for (int c = 0; c < DH; c += 32) {
-        uint32_t u0[16], u1[16];
-        tmem_ld16(tm + lane_base + c, u0);
-        tmem_ld16(tm + lane_base + c + 16, u1);
+      for (int c = 0, slab = 0; c < DH; c += 32, ++slab) {
+        uint8_t *tile = sRQ + (slab & 1) * 16384;
+        if (slab >= 2) {
+          if (t == 0) bulk_wait_read<1>();  // the store that used this tile has read it
+          if (!group_sync(&sm.grp[1], gph2, err, 34, abort_ptr)) break;
+        }
+        uint32_t u[32];
+        tmem_ld32(tm + lane_base + c, u);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          buf[t * 33 + i] = __uint_as_float(u0[i]) * fr;
-          buf[t * 33 + 16 + i] = __uint_as_float(u1[i]) * fr;
+        for (int i = 0; i < 8; ++i)
+          *reinterpret_cast<float4 *>(tile + t * 128 + ((i ^ (t & 7)) << 4)) =
+              make_float4(__uint_as_float(u[4 * i]) * fr, __uint_as_float(u[4 * i + 1]) * fr,
+                          __uint_as_float(u[4 * i + 2]) * fr, __uint_as_float(u[4 * i + 3]) * fr);
+        fence_proxy_async_smem();
+        if (!group_sync(&sm.grp[1], gph2, err, 35, abort_ptr)) break;
+        if (t == 0) {
+          tma_store_2d(&mapC, c0 + c, p * DV + a0, tile);
+          bulk_commit();
         }
-        if (!group_sync(&sm.grp[1], gph, err, 34, abort_ptr)) break;
-#pragma unroll 4
-        for (int rr = 0; rr < 32; ++rr) {
-          const int row = wq * 32 + rr;
-          C_last[((size_t)p * DV + a0 + row) * D + c0 + c + lane] = buf[row * 33 + lane];
-        }
-        if (!group_sync(&sm.grp[1], gph, err, 35, abort_ptr)) break;
       }
+      if (t == 0) bulk_wait_all();
+      if (t == 0) TRACE(4, 511, 2);
     } else {
       set_abort(sm);
     }
   } else if (warp >= 12) {
-    // ------------------------------------------------------------------ warpgroup 3: operands and n
+    // ------------------------------------------------------------------ warpgroup 3: v and q operands
     const int t = threadIdx.x - 384;
-    constexpr int CPR = DH / 8;    // 16-byte chunks per row
-    constexpr int RG = 128 / CPR;  // rows handled at once
-    const int cc = t % CPR, rg = t / CPR;
-    const int colb = (cc >> 3) * 8192, c8 = cc & 7;
+    constexpr int CPR = DH / 8;  // 16-byte chunks per row
+    // row layout for q: two threads per row, each half of the row's chunks
+    const int qr = t >> 1, qh = t & 1;
     for (int c = t; c < DH; c += 128) sm.n[c] = n_init ? n_init[(size_t)p * D + c0 + c] : 0.f;
     uint32_t gph = 0;
     bool ok = group_sync(&sm.grp[2], gph, err, 50, abort_ptr);
     for (int k = 0; ok && k < NC; ++k) {
-      const int s = k & 1;
-      if (!mbar_wait(&sm.full[s], (k >> 1) & 1, err, 51, abort_ptr)) { ok = false; break; }
-      if (!mbar_wait(&sm.bar_S[s], (k >> 1) & 1, err, 52, abort_ptr)) { ok = false; break; }
+      const int s = k & 1, par = k & 1;
+      if (!mbar_wait(&sm.g_full[s], (k >> 1) & 1, err, 51, abort_ptr)) { ok = false; break; }
+      if (!mbar_wait(&sm.v_full[s], (k >> 1) & 1, err, 55, abort_ptr)) { ok = false; break; }
+      // v: bf16 -> fp16 (exact), in place
+      {
+        uint4 *vp = reinterpret_cast<uint4 *>(STV(s));
+#pragma unroll 4
+        for (int i = t; i < 1024; i += 128) {
+          const uint4 raw = vp[i];
+          uint4 o4;
+          o4.x = pack_half2(bf16_lo(raw.x), bf16_hi(raw.x));
+          o4.y = pack_half2(bf16_lo(raw.y), bf16_hi(raw.y));
+          o4.z = pack_half2(bf16_lo(raw.z), bf16_hi(raw.z));
+          o4.w = pack_half2(bf16_lo(raw.w), bf16_hi(raw.w));
+          vp[i] = o4;
+        }
+      }
+      if (!mbar_wait(&sm.qk_full, k & 1, err, 52, abort_ptr)) { ok = false; break; }
+      // beta q is free once the previous chunk's products are done; n after the previous chunk
+      if (k >= 1 && !mbar_wait(&sm.bar_U, (k - 1) & 1, err, 56, abort_ptr)) { ok = false; break; }
+      if (k >= 1 && !mbar_wait(&sm.n_ready, (k - 1) & 1, err, 58, abort_ptr)) { ok = false; break; }
       if (t == 0) TRACE(5, k, 0);
       const Gate &g = sm.g[s];
-      const float alpha = g.alpha;
-      float nreg[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) nreg[e] = sm.n[cc * 8 + e];
-      // q: n . q_r over this CTA's columns, and beta_r q_r in fp16 (in place)
-#pragma unroll 2
-      for (int i = 0; i < 64 / RG; ++i) {
-        const int r = rg + RG * i;
-        uint4 *ptr = reinterpret_cast<uint4 *>(STQ(s) + colb + r * 128 + ((c8 ^ (r & 7)) << 4));
-        const uint4 raw = *ptr;
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-        float f[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          f[2 * e] = bf16_lo(w[e]);
-          f[2 * e + 1] = bf16_hi(w[e]);
+      // q: n . q_r over this CTA's columns and beta_r q_r in fp16 (row layout)
+      {
+        const float bq = g.beta[qr];
+        const uint64_t bq2 = f2pack(bq, bq);
+        uint64_t part2 = 0;
+#pragma unroll 4
+        for (int i = 0; i < CPR / 2; ++i) {
+          const int ch = qh * (CPR / 2) + i;  // chunk of the row
+          const int off = (ch >> 3) * 8192 + qr * 128 + (((ch & 7) ^ (qr & 7)) << 4);
+          const uint4 raw = *reinterpret_cast<const uint4 *>(sRQ + off);
+          const uint4 na = *reinterpret_cast<const uint4 *>(&sm.n[ch * 8]);
+          const uint4 nb = *reinterpret_cast<const uint4 *>(&sm.n[ch * 8 + 4]);
+          const uint64_t x0 = bf2_to_f2(raw.x), x1 = bf2_to_f2(raw.y), x2 = bf2_to_f2(raw.z), x3 = bf2_to_f2(raw.w);
+          part2 = f2fma(x0, (uint64_t)na.x | ((uint64_t)na.y << 32), part2);
+          part2 = f2fma(x1, (uint64_t)na.z | ((uint64_t)na.w << 32), part2);
+          part2 = f2fma(x2, (uint64_t)nb.x | ((uint64_t)nb.y << 32), part2);
+          part2 = f2fma(x3, (uint64_t)nb.z | ((uint64_t)nb.w << 32), part2);
+          uint4 o4;
+          o4.x = f2_to_h2(f2mul(x0, bq2));
+          o4.y = f2_to_h2(f2mul(x1, bq2));
+          o4.z = f2_to_h2(f2mul(x2, bq2));
+          o4.w = f2_to_h2(f2mul(x3, bq2));
+          *reinterpret_cast<uint4 *>(sBQ + off) = o4;
         }
-        float part = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) part = fmaf(f[e], nreg[e], part);
-#pragma unroll
-        for (int o = CPR / 2; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-        if (cc == 0) sm.nq[s][r] = part;
-        const float bq = g.beta[r];
-        uint4 o4;
-        o4.x = pack_half2(f[0] * bq, f[1] * bq);
-        o4.y = pack_half2(f[2] * bq, f[3] * bq);
-        o4.z = pack_half2(f[4] * bq, f[5] * bq);
-        o4.w = pack_half2(f[6] * bq, f[7] * bq);
-        *ptr = o4;
+        float part = f2sum(part2);
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        if (PAIR && (qr >> 5) == prt) {
+          // n . q of the partner's rows -> partner (after it has used the previous one in this slot)
+          if (k >= 2 && !mbar_wait_cluster(&sm.nqx_free[par], ((k >> 1) - 1) & 1, err, 57, abort_ptr)) {
+            ok = false;
+            break;
+          }
+          if (qh == 0)
+            st_async_f32(mapa_shared(smem_u32(&sm.nqx[par][qr & 31]), prt), part,
+                         mapa_shared(smem_u32(&sm.nqx_full[par]), prt));
+        } else if (qh == 0) {
+          sm.nq[par][qr] = part;
+        }
       }
       if (t == 0) TRACE(5, k, 1);
-      mbar_arrive(&sm.bar_nq[s]);
-      // k: n-update partial sums, and w_j k_j (frame of T) in fp16 (in place)
-      float acc[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-#pragma unroll 2
-      for (int i = 0; i < 64 / RG; ++i) {
-        const int j = rg + RG * i;
-        uint4 *ptr = reinterpret_cast<uint4 *>(STK(s) + colb + j * 128 + ((c8 ^ (j & 7)) << 4));
-        const uint4 raw = *ptr;
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-        float f[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          f[2 * e] = bf16_lo(w[e]);
-          f[2 * e + 1] = bf16_hi(w[e]);
-        }
-        const float wt = g.wt[j], wkj = g.wk[j];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = fmaf(wt, f[e], acc[e]);
-        uint4 o4;
-        o4.x = pack_half2(f[0] * wkj, f[1] * wkj);
-        o4.y = pack_half2(f[2] * wkj, f[3] * wkj);
-        o4.z = pack_half2(f[4] * wkj, f[5] * wkj);
-        o4.w = pack_half2(f[6] * wkj, f[7] * wkj);
-        *ptr = o4;
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sm.npart[rg * DH + cc * 8 + e] = acc[e];
-      // v: bf16 -> fp16 (exact), in place
-      uint4 *vp = reinterpret_cast<uint4 *>(STV(s));
-#pragma unroll 2
-      for (int i = t; i < 1024; i += 128) {
-        const uint4 raw = vp[i];
-        uint4 o4;
-        o4.x = pack_half2(bf16_lo(raw.x), bf16_hi(raw.x));
-        o4.y = pack_half2(bf16_lo(raw.y), bf16_hi(raw.y));
-        o4.z = pack_half2(bf16_lo(raw.z), bf16_hi(raw.z));
-        o4.w = pack_half2(bf16_lo(raw.w), bf16_hi(raw.w));
-        vp[i] = o4;
-      }
+      mbar_arrive(&sm.bar_nq[par]);
+      mbar_arrive(&sm.qk_empty);  // raw q is no longer read here
       fence_proxy_async_smem();
       if (t == 0) TRACE(5, k, 2);
       mbar_arrive(&sm.opready);
-      // every partial of this chunk written
-      if (!group_sync(&sm.grp[2], gph, err, 53, abort_ptr)) { ok = false; break; }
-      for (int c = t; c < DH; c += 128) {
-        float a = 0.f;
-#pragma unroll
-        for (int gi = 0; gi < RG; ++gi) a += sm.npart[gi * DH + c];
-        sm.n[c] = alpha * sm.n[c] + a;
-      }
-      // n after chunk k visible before the next n . q
-      if (!group_sync(&sm.grp[2], gph, err, 54, abort_ptr)) { ok = false; break; }
-      if (t == 0) TRACE(5, k, 3);
     }
     if (!ok) set_abort(sm);
-    if (ok && atile == 0) {
-      for (int c = t; c < DH; c += 128) n_last[(size_t)p * D + c0 + c] = sm.n[c];
-      if (rank == 0 && t == 0) m_last[p] = cm[(size_t)p * (NC + 1) + NC];
-    }
   }
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) TRACE(0, 511, 1);
   if (PAIR) cluster_sync();  // no CTA leaves while its partner may still access its shared memory
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tm, 512);
   }
-#undef STQ
-#undef STK
 #undef STV
 }
 
-// Dynamic shared memory: two stages, P, the pair exchange buffers and alignment slack; never
-// less than 120 KB, so that one CTA (which allocates all 512 tensor-memory columns) runs per SM.
+// Dynamic shared memory: raw and converted q/k tiles, two v stages, P, this CTA's partial S rows,
+// the pair exchange buffers and alignment slack; never less than 120 KB, so that one CTA (which
+// allocates all 512 tensor-memory columns) runs per SM.
 template <int DH, bool PAIR>
 size_t smem_bytes() {
-  const size_t need = (size_t)2 * (2 * DH * 128 + 16384) + 8192 + (PAIR ? 32768 : 0) + 1024;
+  const size_t NR = PAIR ? 32 : 64;
+  const size_t need = (size_t)4 * DH * 128 + 2 * 16384 + 8192 + NR * 256 + (PAIR ? 32768 : 0) + 1024;
   return need > 120 * 1024 ? need : 120 * 1024;
 }
 
 template <int DH, bool PAIR, typename TO>
-cudaError_t launch_one(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const float *gb,
-                       const float *gx, const float *gu, const float *cm, int P, int S, int DV, float scale,
-                       const float *C_init, const float *n_init, void *h, float *C_last, float *n_last,
-                       float *m_last, int *err, cudaStream_t stream) {
+cudaError_t launch_one(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mc,
+                       const float *gb, const float *gx, const float *gu, const float *cm, const float *ig,
+                       const float *fg, const float *m_init, int P, int S, int DV, float scale,
+                       const float *C_init, const float *n_init, void *h, float *n_last, float *m_last, int *err,
+                       cudaStream_t stream) {
   auto kern = fwd_tc_kernel<DH, PAIR, TO>;
   const size_t smem = smem_bytes<DH, PAIR>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -703,19 +945,20 @@ cudaError_t launch_one(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, gb, gx, gu, cm, S, DV, scale, C_init, n_init,
-                            static_cast<TO *>(h), C_last, n_last, m_last, err);
+  return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mc, gb, gx, gu, cm, ig, fg, m_init, S, DV, scale, C_init, n_init,
+                            static_cast<TO *>(h), n_last, m_last, err);
 }
 
 template <typename TO>
 cudaError_t launch_dispatch(int DH, bool pair, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                            const float *gb, const float *gx, const float *gu, const float *cm, int P, int S,
-                            int DV, float scale, const float *C_init, const float *n_init, void *h, float *C_last,
-                            float *n_last, float *m_last, int *err, cudaStream_t stream) {
+                            const CUtensorMap &mc, const float *gb, const float *gx, const float *gu,
+                            const float *cm, const float *ig, const float *fg, const float *m_init, int P, int S,
+                            int DV, float scale, const float *C_init, const float *n_init, void *h, float *n_last,
+                            float *m_last, int *err, cudaStream_t stream) {
 #define MLSTM_TC_CASE(dh_, pr_)                                                                                  \
   if (DH == dh_ && pair == pr_)                                                                                  \
-    return launch_one<dh_, pr_, TO>(mq, mk, mv, gb, gx, gu, cm, P, S, DV, scale, C_init, n_init, h, C_last,     \
-                                    n_last, m_last, err, stream);
+    return launch_one<dh_, pr_, TO>(mq, mk, mv, mc, gb, gx, gu, cm, ig, fg, m_init, P, S, DV, scale, C_init,    \
+                                    n_init, h, n_last, m_last, err, stream);
   MLSTM_TC_CASE(64, false)
   MLSTM_TC_CASE(128, false)
   MLSTM_TC_CASE(256, false)
@@ -739,21 +982,23 @@ bool fwd_tc_pair(int P, int D, int DV) {
 }
 
 cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, bool out_bf16, const float *gb,
-                          const float *gx, const float *gu, const float *cm, int P, int S, int D, int DV,
-                          const float *C_init, const float *n_init, void *h, float *C_last, float *n_last,
-                          float *m_last, int *err, cudaStream_t stream) {
+                          const float *gx, const float *gu, const float *cm, const float *ig, const float *fg,
+                          const float *m_init, int P, int S, int D, int DV, const float *C_init,
+                          const float *n_init, void *h, float *C_last, float *n_last, float *m_last, int *err,
+                          cudaStream_t stream) {
   const bool pair = fwd_tc_pair(P, D, DV);
   const int DH = pair ? D / 2 : D;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mc;
   if (!make_tmap_2d_b16(&mq, q, true, (uint64_t)P * S, D, D, 64, kL)) return cudaErrorInvalidValue;
   if (!make_tmap_2d_b16(&mk, k, true, (uint64_t)P * S, D, D, 64, kL)) return cudaErrorInvalidValue;
   if (!make_tmap_2d_b16(&mv, v, true, (uint64_t)P * S, DV, DV, 64, kL)) return cudaErrorInvalidValue;
+  if (!make_tmap_2d_f32(&mc, C_last, (uint64_t)P * DV, D, kTile)) return cudaErrorInvalidValue;
   const float scale = (float)(1.0 / __builtin_sqrt((double)D));
   if (out_bf16)
-    return launch_dispatch<__nv_bfloat16>(DH, pair, mq, mk, mv, gb, gx, gu, cm, P, S, DV, scale, C_init, n_init, h,
-                                          C_last, n_last, m_last, err, stream);
-  return launch_dispatch<float>(DH, pair, mq, mk, mv, gb, gx, gu, cm, P, S, DV, scale, C_init, n_init, h, C_last,
-                                n_last, m_last, err, stream);
+    return launch_dispatch<__nv_bfloat16>(DH, pair, mq, mk, mv, mc, gb, gx, gu, cm, ig, fg, m_init, P, S, DV, scale,
+                                          C_init, n_init, h, n_last, m_last, err, stream);
+  return launch_dispatch<float>(DH, pair, mq, mk, mv, mc, gb, gx, gu, cm, ig, fg, m_init, P, S, DV, scale, C_init,
+                                n_init, h, n_last, m_last, err, stream);
 }
 
 }  // namespace mlstm

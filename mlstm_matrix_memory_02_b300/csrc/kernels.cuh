@@ -31,10 +31,13 @@ cudaError_t launch_step(const void *q, const void *k, const void *v, bool bf16, 
 // d_v a multiple of 128.  fwd_tc_pair says whether a head's d_qk is split over a CTA pair.
 bool fwd_tc_supported(int S, int L, int D, int DV, bool bf16);
 bool fwd_tc_pair(int P, int D, int DV);
+// The gate factors come from the raw pre-activations ig, fg (and m_init) when ig is not NULL,
+// otherwise from the gate kernel's b, x, u and chunk stabiliser in the workspace.
 cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, bool out_bf16, const float *gb,
-                          const float *gx, const float *gu, const float *cm, int P, int S, int D, int DV,
-                          const float *C_init, const float *n_init, void *h, float *C_last, float *n_last,
-                          float *m_last, int *err, cudaStream_t stream);
+                          const float *gx, const float *gu, const float *cm, const float *ig, const float *fg,
+                          const float *m_init, int P, int S, int D, int DV, const float *C_init,
+                          const float *n_init, void *h, float *C_last, float *n_last, float *m_last, int *err,
+                          cudaStream_t stream);
 
 // small helpers
 cudaError_t launch_copy_chunk_m(const float *cm, int P, int NC, float *m_last, cudaStream_t stream);

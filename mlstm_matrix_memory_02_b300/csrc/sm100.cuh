@@ -44,14 +44,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Waits for the phase with the given parity to complete.  Each poll may suspend the thread
-// for up to kSuspendNs; the wait gives up after about kWaitCycles SM clocks (about one second),
-// or as soon as *abort (when given) becomes non-zero, records `code` in *err and returns false.
+// Waits for the phase with the given parity to complete.  The wait polls with try_wait (which
+// may suspend the thread for a short, hardware-chosen time); it gives up after about
+// kWaitCycles SM clocks (about one second), or as soon as *abort (when given) becomes non-zero,
+// records `code` in *err and returns false.
+#ifndef MLSTM_WAIT_MODE
+#define MLSTM_WAIT_MODE 1  // 0: try_wait with a suspend-time hint, 1: try_wait, 2: test_wait spin
+#endif
 constexpr uint32_t kSuspendNs = 20000;
 constexpr long long kWaitCycles = 1LL << 31;
 
-__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_poll(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
+#if MLSTM_WAIT_MODE == 0
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
@@ -59,14 +64,31 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parit
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
       : "memory");
+#elif MLSTM_WAIT_MODE == 1
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+#else
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+#endif
   return ok != 0;
 }
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, int code,
                                           const int *abort = nullptr) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_poll(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
-    if (mbar_try_wait_hint(bar, parity)) return true;
+    if (mbar_poll(bar, parity)) return true;
     if ((abort && *(const volatile int *)abort) || clock64() - t0 > kWaitCycles) {
       if (err) atomicCAS(err, 0, code);
       return false;
@@ -103,12 +125,16 @@ __device__ __forceinline__ void st_async_f32(uint32_t raddr, float a, uint32_t r
                "r"(rbar)
                : "memory");
 }
-// One arrival on an mbarrier of another CTA of the cluster (release at cluster scope).
+// One arrival on an mbarrier of another CTA of the cluster, relaxed: it orders nothing, so it is
+// only used to say "the buffer you write into is free again" after every value read from that
+// buffer has been consumed (a release at cluster scope would also wait for this thread's
+// outstanding global stores, which costs about a microsecond).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t rbar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_poll_cluster(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
+#if MLSTM_WAIT_MODE == 0
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
@@ -116,14 +142,32 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t pa
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
       : "memory");
+#elif MLSTM_WAIT_MODE == 1
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+#else
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+#endif
   return ok != 0;
 }
 // As mbar_wait, for phases completed by another CTA of the cluster (acquire at cluster scope).
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, int *err, int code,
                                                   const int *abort = nullptr) {
+  if (mbar_poll_cluster(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (mbar_poll_cluster(bar, parity)) return true;
     if ((abort && *(const volatile int *)abort) || clock64() - t0 > kWaitCycles) {
       if (err) atomicCAS(err, 0, code);
       return false;
@@ -146,6 +190,28 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *m
           smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
+}
+// Stores a tile from shared memory through a tensor map (bulk async group of this thread).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int y, const void *smem_src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(smem_u32(smem_src))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's bulk groups are still reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Waits until every bulk group of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Prefetches a tile of a tensor map into L2 (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -217,6 +283,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
+}
+// 32 lanes x 32 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
