@@ -25,12 +25,14 @@
 // rescaled frame C = exp(sigma) T: the chunk decay is folded into sigma and into the scale of the
 // update's k operand, and T is multiplied back only when exp(-sigma) would exceed 2^8.
 //
-// Warp roles (512 threads): warp 0 issues TMA loads of the q, k, v tiles (two stages); warp 1
-// allocates tensor memory and issues every MMA; warp 2 computes the per-chunk gate factors;
-// warpgroup 1 (warps 4-7) forms P and writes h; warpgroup 2 (warps 8-11) copies the state to
-// fp16 (the serial chain of the recurrence); warpgroup 3 (warps 12-15) converts q, k, v in place
-// to the scaled fp16 operands and keeps n.  Hand-offs use mbarriers; every wait is bounded in
-// time and reports through an error word.
+// Warp roles (640 threads): warp 0 issues TMA loads of q and k (one stage, L2 prefetch two
+// chunks ahead), warp 3 those of v (two stages); warp 1 allocates tensor memory and issues every
+// MMA; warp 2 preprocesses the gates and computes the per-chunk factors; warpgroup 1 (warps 4-7)
+// forms P and the denominators; warpgroup 2 (warps 8-11) copies the state to fp16 (the serial
+// chain of the recurrence), forms w k and keeps n; warpgroup 3 (warps 12-15) forms v and beta q
+// in fp16 and n.q; warpgroup 4 (warps 16-19) reads H, completes it with the partner's columns
+// and writes h.  Hand-offs use mbarriers; every wait is bounded in time and reports through an
+// error word.
 //
 // Operand precision: q, k, v arrive as bf16 and convert to fp16 exactly; the computed operands
 // (P, beta q, w k and the state copy) are rounded to fp16 (11 significant bits); sums are fp32.
@@ -66,7 +68,7 @@ using namespace sm100;
 
 constexpr int kL = 64;        // chunk length
 constexpr int kTile = 128;    // d_v rows per CTA (MMA M)
-constexpr int kThreads = 512;
+constexpr int kThreads = 640;
 constexpr float kRescaleLog = 5.545177444479562f;  // ln(2^8): largest lazy frame factor
 constexpr uint32_t kColS = 384, kColH = 448;
 
@@ -90,6 +92,7 @@ struct Smem {
   uint64_t qk_full, qk_empty, v_full[2], v_empty[2], g_full[2], bar_nq[2];
   uint64_t bar_S, sfree, bar_U, bar_H, hfree, cready, opready, pready, fin, n_ready;
   uint64_t sx_full[2], sx_free[2], hx_full, hx_free, nqx_full[2], nqx_free[2];
+  uint64_t inv_ready[2], inv_free[2];  // 1/den of a chunk: written by warpgroup 1, read by warpgroup 4
   uint64_t grp[3];  // bounded group barriers of warpgroups 1, 2 and 3
   uint32_t tmem_base;
   int abort_flag;
@@ -221,6 +224,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
     mbar_init(&sm.hx_full, 1);
     mbar_init(&sm.hx_free, 4);
     for (int i = 0; i < 3; ++i) mbar_init(&sm.grp[i], 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.inv_ready[i], 128);
+      mbar_init(&sm.inv_free[i], 128);
+    }
     sm.abort_flag = 0;
     fence_barrier_init();
   }
@@ -299,23 +306,32 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       const uint32_t id_P = idesc_f16(kTile, NR, 0, 1, 0);
       const uint32_t q_raw = smem_u32(sRQ), k_raw = smem_u32(sRK), q_b = smem_u32(sBQ), k_w = smem_u32(sWK);
       const uint32_t p_own = smem_u32(sP) + r_lo * 128;
-      int k = 0;
-      for (; k < NC; ++k) {
-        const int s = k & 1;
-        const uint32_t v_s = smem_u32(STV(s));
-        // S_k = Q K^T over this CTA's d_qk columns (raw bf16 inputs)
-        if (!mbar_wait(&sm.qk_full, k & 1, err, 12, abort_ptr)) break;
-        if (k >= 1 && !mbar_wait(&sm.sfree, (k - 1) & 1, err, 13, abort_ptr)) break;
+      // S_k = Q K^T over this CTA's d_qk columns (raw bf16 inputs)
+      auto issue_S_now = [&](int kk) {
         tc_fence_after();
-        TRACE(1, k, 0);
+        TRACE(1, kk, 0);
 #pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
+        for (int c = 0; c < DH / 16; ++c) {
+          const uint32_t off = (c >> 2) * 8192 + (c & 3) * 32;
           mma_f16_ss(tm + kColS, smem_desc(q_raw + off, 16, 1024, kSwizzle128B),
-                     smem_desc(k_raw + off, 16, 1024, kSwizzle128B), id_S, kk > 0);
+                     smem_desc(k_raw + off, 16, 1024, kSwizzle128B), id_S, c > 0);
         }
         mma_commit(&sm.bar_S);
         mma_commit(&sm.qk_empty);
+      };
+      auto issue_S = [&](int kk) -> bool {
+        if (!mbar_wait(&sm.qk_full, kk & 1, err, 12, abort_ptr)) return false;
+        if (kk >= 1 && !mbar_wait(&sm.sfree, (kk - 1) & 1, err, 13, abort_ptr)) return false;
+        issue_S_now(kk);
+        return true;
+      };
+      // Tensor-pipe order per chunk k: X_k, U_k, S_{k+1}, PV_k.  S of the next chunk goes ahead of
+      // P V so that the next P is formed while this chunk finishes.
+      int k = 0;
+      bool ok = NC == 0 || issue_S(0);
+      for (; ok && k < NC; ++k) {
+        const int s = k & 1;
+        const uint32_t v_s = smem_u32(STV(s));
         // H^T = C16 (beta q)^T and T += V^T (w k): the state copy, the operands and a free H
         if (!mbar_wait(&sm.cready, k & 1, err, 14, abort_ptr)) break;
         TRACE(1, k, 1);
@@ -334,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
           mma_f16_ss(tm, smem_desc(v_s + kk * 2048, 8192, 1024, kSwizzle128B),
                      smem_desc(k_w + kk * 2048, 8192, 1024, kSwizzle128B), id_U, 1);
         mma_commit(&sm.bar_U);
-        // H^T[:, own rows] += V^T P^T
+        const bool s_next = k + 1 >= NC;
         if (!mbar_wait(&sm.pready, k & 1, err, 17, abort_ptr)) break;
         TRACE(1, k, 4);
         tc_fence_after();
@@ -344,7 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
                      smem_desc(p_own + kk * 32, 16, 1024, kSwizzle128B), id_P, 1);
         mma_commit(&sm.bar_H);
         mma_commit(&sm.v_empty[s]);
+        if (!s_next && !issue_S(k + 1)) break;
       }
+      if (!ok) k = -1;
       if (k < NC) set_abort(sm);
       mma_commit(&sm.fin);  // completes once every MMA issued above has finished
       mbar_wait(&sm.fin, 0, err, 18);
@@ -558,6 +576,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       }
 #pragma unroll
       for (int o = 1; o < TPR; o <<= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+      // warpgroup 4 has read this slot's 1/den for chunk kk-2
+      if (kk >= 2 && !mbar_wait(&sm.inv_free[par], ((kk >> 1) - 1) & 1, err, 31, abort_ptr)) return false;
       if (pseg == 0) {
         // denominator of row pr: intra-chunk part + beta_r n.q_r (both halves of d_qk with a pair)
         float nqf = sm.nq[par][pr];
@@ -575,54 +595,62 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       fence_proxy_async_smem();
       if (t == 0) TRACE(3, kk, 2);
       mbar_arrive(&sm.pready);
+      mbar_arrive(&sm.inv_ready[par]);
       return true;
     };
 
-    bool ok = NC == 0 || (s_read(0) && group_sync(&sm.grp[0], gph, err, 20, abort_ptr) && p_form(0));
+    bool ok = true;
     for (int k = 0; ok && k < NC; ++k) {
+      if (!s_read(k) || !group_sync(&sm.grp[0], gph, err, 20, abort_ptr) || !p_form(k)) ok = false;
+    }
+    if (!ok) set_abort(sm);
+  } else if (warp >= 16) {
+    // ------------------------------------------------------------------ warpgroup 4: h
+    const int t = threadIdx.x - 512;  // tensor-memory lane = d_v row within the tile
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    bool ok = true;
+    for (int k = 0; k < NC; ++k) {
       const int par = k & 1;
       const size_t tok0 = (size_t)p * S + (size_t)k * kL;
-      // H^T of chunk k: read, free the accumulator, send the partner's columns
+      // H^T of chunk k: send the partner's columns, keep this CTA's rows, free the accumulator
       if (!mbar_wait(&sm.bar_H, k & 1, err, 26, abort_ptr)) { ok = false; break; }
       if (t == 0) TRACE(3, k, 3);
       tc_fence_after();
       float own[NR];
-      {
-        uint32_t u[2][32];
-        tmem_ld32(tm + lane_base + kColH, u[0]);
-        tmem_ld32(tm + lane_base + kColH + 32, u[1]);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&sm.hfree);
-        if (PAIR) {
-          if (k >= 1 && !mbar_wait_cluster(&sm.hx_free, (k - 1) & 1, err, 27, abort_ptr)) { ok = false; break; }
+      if (PAIR) {
+        if (k >= 1 && !mbar_wait_cluster(&sm.hx_free, (k - 1) & 1, err, 27, abort_ptr)) { ok = false; break; }
+        {
+          uint32_t u[32];
+          tmem_ld32(tm + lane_base + kColH + 32 * prt, u);  // the partner's 32 rows
+          tmem_wait_ld();
           const uint32_t rbar = mapa_shared(smem_u32(&sm.hx_full), prt);
           const uint32_t dst = mapa_shared(smem_u32(HX + t * 32), prt);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t *src = rank ? u[0] : u[1];  // the partner's 32 rows
-            st_async_v4(dst + ((i ^ (t & 7)) << 4), __uint_as_float(src[4 * i]), __uint_as_float(src[4 * i + 1]),
-                        __uint_as_float(src[4 * i + 2]), __uint_as_float(src[4 * i + 3]), rbar);
-          }
-#pragma unroll
-          for (int i = 0; i < 32; ++i) own[i] = __uint_as_float(rank ? u[1][i] : u[0][i]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            own[i] = __uint_as_float(u[0][i]);
-            own[32 + i] = __uint_as_float(u[1][i]);
-          }
+          for (int i = 0; i < 8; ++i)
+            st_async_v4(dst + ((i ^ (t & 7)) << 4), __uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
+                        __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3]), rbar);
         }
+        {
+          uint32_t u[32];
+          tmem_ld32(tm + lane_base + kColH + 32 * rank, u);  // this CTA's rows
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) own[i] = __uint_as_float(u[i]);
+        }
+      } else {
+        uint32_t u[32];
+        tmem_ld32(tm + lane_base + kColH, u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) own[i] = __uint_as_float(u[i]);
+        tmem_ld32(tm + lane_base + kColH + 32, u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) own[32 + i] = __uint_as_float(u[i]);
       }
+      tc_fence_before();
+      mbar_arrive(&sm.hfree);
       if (t == 0) TRACE(6, k, 6);
-      // With a pair, P of the next chunk is formed now (its S rows read and exchanged), so that
-      // the exchange of the H columns overlaps it and PV of the next chunk can start earlier.
-      if (PAIR && k + 1 < NC) {
-        if (!s_read(k + 1) || !group_sync(&sm.grp[0], gph, err, 20, abort_ptr) || !p_form(k + 1)) {
-          ok = false;
-          break;
-        }
-      }
       if (PAIR) {
         if (t == 0) mbar_arrive_expect_tx(&sm.hx_full, 128 * 32 * 4);
         if (!mbar_wait_cluster(&sm.hx_full, k & 1, err, 28, abort_ptr)) { ok = false; break; }
@@ -639,21 +667,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&sm.hx_free), prt));
       }
-      // inv[] of chunk k was formed by every warp before the last group barrier, except for the
-      // last chunk of a pair and every chunk without one
-      if ((!PAIR || k + 1 == NC) && !group_sync(&sm.grp[0], gph, err, 29, abort_ptr)) { ok = false; break; }
+      // 1/den of every row of chunk k (warpgroup 1)
+      if (!mbar_wait(&sm.inv_ready[par], (k >> 1) & 1, err, 29, abort_ptr)) { ok = false; break; }
       if (t == 0) TRACE(6, k, 7);
       TO *hp = h + (tok0 + r_lo) * DV + a0 + t;
 #pragma unroll
       for (int i = 0; i < NR; ++i) hp[(size_t)i * DV] = from_f32<TO>(own[i] * sm.inv[par][r_lo + i]);
+      mbar_arrive(&sm.inv_free[par]);
       if (t == 0) TRACE(3, k, 5);
-      if (!PAIR && k + 1 < NC) {
-        // no partner: the next S rows and P after the stores (keeps the 64 output rows out of registers)
-        if (!s_read(k + 1) || !group_sync(&sm.grp[0], gph, err, 20, abort_ptr) || !p_form(k + 1)) {
-          ok = false;
-          break;
-        }
-      }
     }
     if (!ok) set_abort(sm);
   } else if (warp >= 8 && warp < 12) {
@@ -742,24 +763,38 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       if (!mbar_wait(&sm.qk_full, k & 1, err, 36, abort_ptr)) { ok = false; break; }
       const float alpha = g.alpha;
       {
+        // rows in batches of four: every load of a batch is issued before its stores
         uint64_t acc[4] = {0, 0, 0, 0};
-#pragma unroll 4
-        for (int i = 0; i < 64 / KRG; ++i) {
-          const int j = krg + KRG * i;
-          const int off = kcolb + j * 128 + ((kc8 ^ (j & 7)) << 4);
-          const uint4 raw = *reinterpret_cast<const uint4 *>(sRK + off);
-          const uint64_t wt2 = f2pack(g.wt[j], g.wt[j]), wk2 = f2pack(g.wk[j], g.wk[j]);
-          const uint64_t x0 = bf2_to_f2(raw.x), x1 = bf2_to_f2(raw.y), x2 = bf2_to_f2(raw.z), x3 = bf2_to_f2(raw.w);
-          acc[0] = f2fma(wt2, x0, acc[0]);
-          acc[1] = f2fma(wt2, x1, acc[1]);
-          acc[2] = f2fma(wt2, x2, acc[2]);
-          acc[3] = f2fma(wt2, x3, acc[3]);
-          uint4 o4;
-          o4.x = f2_to_h2(f2mul(x0, wk2));
-          o4.y = f2_to_h2(f2mul(x1, wk2));
-          o4.z = f2_to_h2(f2mul(x2, wk2));
-          o4.w = f2_to_h2(f2mul(x3, wk2));
-          *reinterpret_cast<uint4 *>(sWK + off) = o4;
+#pragma unroll 1
+        for (int i0 = 0; i0 < 64 / KRG; i0 += 4) {
+          uint4 raw[4];
+          int off[4];
+          float wt[4], wk[4];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const int j = krg + KRG * (i0 + b);
+            off[b] = kcolb + j * 128 + ((kc8 ^ (j & 7)) << 4);
+            raw[b] = *reinterpret_cast<const uint4 *>(sRK + off[b]);
+            wt[b] = g.wt[j];
+            wk[b] = g.wk[j];
+          }
+          uint4 o4[4];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const uint64_t wt2 = f2pack(wt[b], wt[b]), wk2 = f2pack(wk[b], wk[b]);
+            const uint64_t x0 = bf2_to_f2(raw[b].x), x1 = bf2_to_f2(raw[b].y), x2 = bf2_to_f2(raw[b].z),
+                           x3 = bf2_to_f2(raw[b].w);
+            acc[0] = f2fma(wt2, x0, acc[0]);
+            acc[1] = f2fma(wt2, x1, acc[1]);
+            acc[2] = f2fma(wt2, x2, acc[2]);
+            acc[3] = f2fma(wt2, x3, acc[3]);
+            o4[b].x = f2_to_h2(f2mul(x0, wk2));
+            o4[b].y = f2_to_h2(f2mul(x1, wk2));
+            o4[b].z = f2_to_h2(f2mul(x2, wk2));
+            o4[b].w = f2_to_h2(f2mul(x3, wk2));
+          }
+#pragma unroll
+          for (int b = 0; b < 4; ++b) *reinterpret_cast<uint4 *>(sWK + off[b]) = o4[b];
         }
         mbar_arrive(&sm.qk_empty);  // raw k is no longer read here
 #pragma unroll
@@ -836,15 +871,20 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       // v: bf16 -> fp16 (exact), in place
       {
         uint4 *vp = reinterpret_cast<uint4 *>(STV(s));
-#pragma unroll 4
-        for (int i = t; i < 1024; i += 128) {
-          const uint4 raw = vp[i];
-          uint4 o4;
-          o4.x = pack_half2(bf16_lo(raw.x), bf16_hi(raw.x));
-          o4.y = pack_half2(bf16_lo(raw.y), bf16_hi(raw.y));
-          o4.z = pack_half2(bf16_lo(raw.z), bf16_hi(raw.z));
-          o4.w = pack_half2(bf16_lo(raw.w), bf16_hi(raw.w));
-          vp[i] = o4;
+#pragma unroll 1
+        for (int i0 = t; i0 < 1024; i0 += 4 * 128) {
+          uint4 raw[4];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) raw[b] = vp[i0 + 128 * b];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            uint4 o4;
+            o4.x = pack_half2(bf16_lo(raw[b].x), bf16_hi(raw[b].x));
+            o4.y = pack_half2(bf16_lo(raw[b].y), bf16_hi(raw[b].y));
+            o4.z = pack_half2(bf16_lo(raw[b].z), bf16_hi(raw[b].z));
+            o4.w = pack_half2(bf16_lo(raw[b].w), bf16_hi(raw[b].w));
+            vp[i0 + 128 * b] = o4;
+          }
         }
       }
       if (!mbar_wait(&sm.qk_full, k & 1, err, 52, abort_ptr)) { ok = false; break; }
@@ -858,24 +898,35 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
         const float bq = g.beta[qr];
         const uint64_t bq2 = f2pack(bq, bq);
         uint64_t part2 = 0;
-#pragma unroll 4
-        for (int i = 0; i < CPR / 2; ++i) {
-          const int ch = qh * (CPR / 2) + i;  // chunk of the row
-          const int off = (ch >> 3) * 8192 + qr * 128 + (((ch & 7) ^ (qr & 7)) << 4);
-          const uint4 raw = *reinterpret_cast<const uint4 *>(sRQ + off);
-          const uint4 na = *reinterpret_cast<const uint4 *>(&sm.n[ch * 8]);
-          const uint4 nb = *reinterpret_cast<const uint4 *>(&sm.n[ch * 8 + 4]);
-          const uint64_t x0 = bf2_to_f2(raw.x), x1 = bf2_to_f2(raw.y), x2 = bf2_to_f2(raw.z), x3 = bf2_to_f2(raw.w);
-          part2 = f2fma(x0, (uint64_t)na.x | ((uint64_t)na.y << 32), part2);
-          part2 = f2fma(x1, (uint64_t)na.z | ((uint64_t)na.w << 32), part2);
-          part2 = f2fma(x2, (uint64_t)nb.x | ((uint64_t)nb.y << 32), part2);
-          part2 = f2fma(x3, (uint64_t)nb.z | ((uint64_t)nb.w << 32), part2);
-          uint4 o4;
-          o4.x = f2_to_h2(f2mul(x0, bq2));
-          o4.y = f2_to_h2(f2mul(x1, bq2));
-          o4.z = f2_to_h2(f2mul(x2, bq2));
-          o4.w = f2_to_h2(f2mul(x3, bq2));
-          *reinterpret_cast<uint4 *>(sBQ + off) = o4;
+#pragma unroll 1
+        for (int i0 = 0; i0 < CPR / 2; i0 += 4) {
+          // chunks in batches of four: every load of a batch is issued before its stores
+          uint4 raw[4], na[4], nb[4];
+          int off[4];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const int ch = qh * (CPR / 2) + i0 + b;  // chunk of the row
+            off[b] = (ch >> 3) * 8192 + qr * 128 + (((ch & 7) ^ (qr & 7)) << 4);
+            raw[b] = *reinterpret_cast<const uint4 *>(sRQ + off[b]);
+            na[b] = *reinterpret_cast<const uint4 *>(&sm.n[ch * 8]);
+            nb[b] = *reinterpret_cast<const uint4 *>(&sm.n[ch * 8 + 4]);
+          }
+          uint4 o4[4];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const uint64_t x0 = bf2_to_f2(raw[b].x), x1 = bf2_to_f2(raw[b].y), x2 = bf2_to_f2(raw[b].z),
+                           x3 = bf2_to_f2(raw[b].w);
+            part2 = f2fma(x0, (uint64_t)na[b].x | ((uint64_t)na[b].y << 32), part2);
+            part2 = f2fma(x1, (uint64_t)na[b].z | ((uint64_t)na[b].w << 32), part2);
+            part2 = f2fma(x2, (uint64_t)nb[b].x | ((uint64_t)nb[b].y << 32), part2);
+            part2 = f2fma(x3, (uint64_t)nb[b].z | ((uint64_t)nb[b].w << 32), part2);
+            o4[b].x = f2_to_h2(f2mul(x0, bq2));
+            o4[b].y = f2_to_h2(f2mul(x1, bq2));
+            o4[b].z = f2_to_h2(f2mul(x2, bq2));
+            o4[b].w = f2_to_h2(f2mul(x3, bq2));
+          }
+#pragma unroll
+          for (int b = 0; b < 4; ++b) *reinterpret_cast<uint4 *>(sBQ + off[b]) = o4[b];
         }
         float part = f2sum(part2);
         part += __shfl_xor_sync(0xffffffffu, part, 1);

@@ -132,36 +132,13 @@ __device__ __forceinline__ void st_async_f32(uint32_t raddr, float a, uint32_t r
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t rbar) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
 }
-__device__ __forceinline__ bool mbar_poll_cluster(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-#if MLSTM_WAIT_MODE == 0
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
-      : "memory");
-#elif MLSTM_WAIT_MODE == 1
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-#else
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-#endif
-  return ok != 0;
-}
-// As mbar_wait, for phases completed by another CTA of the cluster (acquire at cluster scope).
+// Phases completed by another CTA of the cluster come in two kinds here: the byte count of
+// st.async / bulk copies into this CTA's shared memory (complete-tx on a local mbarrier, which
+// makes the data visible to the threads that observe the phase, as for TMA loads), and relaxed
+// "buffer free" arrivals that carry no data.  Neither needs an acquire at cluster scope, so the
+// poll is the plain CTA-scope one.
+__device__ __forceinline__ bool mbar_poll_cluster(uint64_t *bar, uint32_t parity) { return mbar_poll(bar, parity); }
+// As mbar_wait, for phases completed by another CTA of the cluster.
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, int *err, int code,
                                                   const int *abort = nullptr) {
   if (mbar_poll_cluster(bar, parity)) return true;
