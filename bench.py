@@ -89,26 +89,31 @@ def load_peaks():
 
 
 _NVML_LOOP = r"""
-import sys, time
-import pynvml as nvml
-nvml.nvmlInit()
-h = nvml.nvmlDeviceGetHandleByIndex(int(sys.argv[1]))
+import ctypes, sys, time
+nvml = ctypes.CDLL("libnvidia-ml.so.1")
+assert nvml.nvmlInit_v2() == 0
+h = ctypes.c_void_p()
+assert nvml.nvmlDeviceGetHandleByIndex_v2(int(sys.argv[1]), ctypes.byref(h)) == 0
 period = float(sys.argv[2])
-get_reasons = getattr(nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-    nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+try:
+    reasons_fn = nvml.nvmlDeviceGetCurrentClocksEventReasons
+except AttributeError:
+    reasons_fn = nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+sm, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
 print("ready", flush=True)
 while True:
-    sm = nvml.nvmlDeviceGetClockInfo(h, nvml.NVML_CLOCK_SM)
-    mx = nvml.nvmlDeviceGetMaxClockInfo(h, nvml.NVML_CLOCK_SM)
-    print(time.time(), sm, mx, get_reasons(h), flush=True)
+    nvml.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm))      # NVML_CLOCK_SM
+    nvml.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+    reasons_fn(h, ctypes.byref(rs))
+    print(time.time(), sm.value, mx.value, rs.value, flush=True)
     time.sleep(period)
 """
 
 
 class ClockSampler:
     """SM clocks and throttle reasons sampled about every millisecond while the timed region
-    runs, by a separate process (NVML; nvidia-smi at 200 ms if NVML is unavailable); only the
-    samples taken inside the timed region are summarised."""
+    runs, by a separate process calling the NVML library directly (nvidia-smi at 200 ms if that
+    fails); only the samples taken inside the timed region are summarised."""
 
     REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
                "sw_power_cap": 0x4}
