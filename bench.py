@@ -349,7 +349,7 @@ def run_ours(args, rank, local, world):
 
     # ---- decode step: B=256, NH=8, d=256 state from a 512-token prefill through the library
     dw = DEC
-    prior, steps = W.make_decode_inputs(dw.with_(S=max(args.steps, 1)))
+    prior, steps = W.make_decode_inputs(dw.with_(S=max(args.steps, 16)))
     dq = torch.from_numpy(prior["q"]).to(dev).to(torch.bfloat16)
     dk = torch.from_numpy(prior["k"]).to(dev).to(torch.bfloat16)
     dv = torch.from_numpy(prior["v"]).to(dev).to(torch.bfloat16)
@@ -376,8 +376,35 @@ def run_ours(args, rank, local, world):
     d1.record(stream)
     torch.cuda.synchronize()
     launches_dec = B.mlstm_kernel_launches() - launches1
+    P_dec = dw.B * dw.NH
     dec_ms = d0.elapsed_time(d1) / max(args.steps, 1)
     dec_gbs = dec_bytes(dw) / (dec_ms * 1e-3) / 1e9
+    # multi-token decode: T tokens per launch, the state crosses HBM once per launch
+    multi = {}
+    for T in (4, 16):
+        mq, mk, mv = (x[:, :, :T].contiguous() for x in (sq, sk, sv))
+        mig, mfg = sig[:, :, :T].contiguous(), sfg[:, :, :T].contiguous()
+        hm = torch.empty((dw.B, dw.NH, T, dw.DV), dtype=torch.float32, device=dev)
+        for _ in range(max(args.warmup, 3)):
+            B.mlstm_step_multi(mq, mk, mv, mig, mfg, Cd, nd, md, h=hm)
+        torch.cuda.synchronize()
+        reps = max(4, args.steps // T)
+        m0 = torch.cuda.Event(enable_timing=True)
+        m1 = torch.cuda.Event(enable_timing=True)
+        l0 = B.mlstm_kernel_launches()
+        m0.record(stream)
+        for _ in range(reps):
+            B.mlstm_step_multi(mq, mk, mv, mig, mfg, Cd, nd, md, h=hm)
+        m1.record(stream)
+        torch.cuda.synchronize()
+        launches_dec += B.mlstm_kernel_launches() - l0
+        us = m0.elapsed_time(m1) / reps * 1e3
+        state_bytes = float(P_dec * 2 * dw.DV * dw.DQK * 4)
+        tok_bytes = float(P_dec * T * ((2 * dw.DQK + dw.DV) * 2 + 2 * 4 + dw.DV * 4))
+        multi[f"T{T}"] = {"us_per_launch": us, "tokens_per_s": dw.B * T / (us * 1e-6),
+                          "speedup_vs_single_step": (dec_ms * 1e3 * T) / us,
+                          "effective_gbs": (state_bytes + tok_bytes) / (us * 1e-6) / 1e9,
+                          "frac_of_hbm": (state_bytes + tok_bytes) / (us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
     decode = {"metric": "mLSTM decode step GB/s (B=256, NH=8, d=256, fp32 state)",
               "value": dec_gbs, "unit": "GB/s", "us_per_step": dec_ms * 1e3,
               "tokens_per_s": dw.B / (dec_ms * 1e-3),
@@ -386,7 +413,8 @@ def run_ours(args, rank, local, world):
                            "traffic": captured_traffic("step_kernel"),
                            "kernel": "mlstm_step", "algorithmic_bytes_per_launch": dec_bytes(dw),
                            "peak_source": peaks["source"] + " HBM copy"},
-              "frac_of_nominal_8tbs": dec_gbs / 8000.0}
+              "frac_of_nominal_8tbs": dec_gbs / 8000.0,
+              "multi_token": multi}
     del Cd, nd, md
 
     # ---- end to end through the public API: pinned host inputs in, h back to the host

@@ -151,6 +151,19 @@ mlstm_status mlstm_step(const void *q, const void *k, const void *v, const float
                         const float *fg, float *C, float *n, float *m, void *h, int B, int NH,
                         int DQK, int DV, mlstm_dtype dt, mlstm_dtype h_dt, void *stream);
 
+/* T consecutive decode steps in one launch, in place (section 5 "Inference Memory and Throughput
+ * Trade-Offs"; section 2 stabiliser; section 3 updates): exactly the results of T calls to
+ * mlstm_step on tokens t = 0..T-1 in order, but the state C is read and written once for the T
+ * tokens instead of T times (for speculative decoding or short prompt extensions).
+ *   q, k [B, NH, T, DQK] (dt), v [B, NH, T, DV] (dt), ig, fg [B, NH, T] float32
+ *   C [B, NH, DV, DQK], n [B, NH, DQK], m [B, NH] float32: read, then overwritten with the
+ *       state after the T-th token
+ *   h [B, NH, T, DV] (h_dt) output: h for every token.
+ * 1 <= T <= 16; other sizes as for mlstm_step. */
+mlstm_status mlstm_step_multi(const void *q, const void *k, const void *v, const float *ig,
+                              const float *fg, float *C, float *n, float *m, void *h, int B, int NH,
+                              int T, int DQK, int DV, mlstm_dtype dt, mlstm_dtype h_dt, void *stream);
+
 /* Forward without any device allocation (no counterpart on the source pages: an interface
  * addition of this library).
  *

@@ -54,6 +54,9 @@ _lib.mlstm_step.restype = _i
 _lib.mlstm_step.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _vp, _i, _i, _i, _i,
                             _i, _i, _vp]
 
+_lib.mlstm_step_multi.restype = _i
+_lib.mlstm_step_multi.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _vp, _i, _i, _i, _i, _i,
+                                  _i, _i, _vp]
 _lib.mlstm_fwd_chunkwise_noalloc.restype = _i
 _lib.mlstm_fwd_chunkwise_noalloc.argtypes = [_vp, _vp, _vp, _fp, _fp, _i, _i, _i, _i, _i, _i, _i,
                                              _fp, _fp, _fp, _vp, _i, _fp, _fp, _fp, _vp]
@@ -61,7 +64,7 @@ _lib.mlstm_fwd_chunkwise_noalloc.argtypes = [_vp, _vp, _vp, _fp, _fp, _i, _i, _i
 EXPORTED = ["mlstm_status_str", "mlstm_last_cuda_error", "mlstm_kernel_launches",
             "mlstm_fwd_workspace_bytes", "mlstm_fwd_chunkwise", "mlstm_fwd_from_gates",
             "mlstm_fwd_chunk_states", "mlstm_fwd_gates", "mlstm_fwd_check", "mlstm_fwd_path",
-            "mlstm_step", "mlstm_fwd_chunkwise_noalloc"]
+            "mlstm_step", "mlstm_step_multi", "mlstm_fwd_chunkwise_noalloc"]
 
 # Bytes of the fixed scratch array behind mlstm_fwd_chunkwise_noalloc (include/mlstm.h).
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -163,6 +166,31 @@ def mlstm_fwd_chunkwise(q, k, v, igate_pre, fgate_pre, chunk, h_dtype=None, C_in
         _ptr(n_last), _ptr(m_last), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(code, "mlstm_fwd_chunkwise")
     return h, C_last, n_last, m_last
+
+
+def mlstm_step_multi(q, k, v, ig, fg, C, n, m, h=None, h_dtype=None, stream=None):
+    """T consecutive decode steps in one launch, in place on (C, n, m).  q, k [B,NH,T,DQK],
+    v [B,NH,T,DV], ig, fg [B,NH,T]; returns h [B,NH,T,DV]."""
+    B, NH, T, DQK = q.shape
+    DV = v.shape[-1]
+    dt = q.dtype
+    _dev(q, "q", dt)
+    _dev(k, "k", dt, (B, NH, T, DQK))
+    _dev(v, "v", dt, (B, NH, T, DV))
+    _dev(ig, "ig", torch.float32, (B, NH, T))
+    _dev(fg, "fg", torch.float32, (B, NH, T))
+    _dev(C, "C", torch.float32, (B, NH, DV, DQK))
+    _dev(n, "n", torch.float32, (B, NH, DQK))
+    _dev(m, "m", torch.float32, (B, NH))
+    h_dtype = h_dtype or (h.dtype if h is not None else dt)
+    if h is None:
+        h = torch.empty((B, NH, T, DV), dtype=h_dtype, device=q.device)
+    _dev(h, "h", h_dtype, (B, NH, T, DV))
+    code = _lib.mlstm_step_multi(_ptr(q), _ptr(k), _ptr(v), _ptr(ig), _ptr(fg), _ptr(C), _ptr(n),
+                                 _ptr(m), _ptr(h), B, NH, T, DQK, DV, _DT[dt], _DT[h_dtype],
+                                 _stream(stream))
+    _check(code, "mlstm_step_multi")
+    return h
 
 
 def mlstm_fwd_chunkwise_noalloc(q, k, v, igate_pre, fgate_pre, chunk, out, C_init=None, n_init=None,

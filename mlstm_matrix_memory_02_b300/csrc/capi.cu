@@ -334,6 +334,21 @@ mlstm_status mlstm_step(const void *q, const void *k, const void *v, const float
                                    B * NH, DQK, DV, (cudaStream_t)stream));
 }
 
+mlstm_status mlstm_step_multi(const void *q, const void *k, const void *v, const float *ig, const float *fg,
+                              float *C, float *n, float *m, void *h, int B, int NH, int T, int DQK, int DV,
+                              mlstm_dtype dt, mlstm_dtype h_dt, void *stream) {
+  if (dt != MLSTM_F32 && dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
+  if (h_dt != MLSTM_F32 && h_dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
+  if (!sizes_ok(B, NH, 0, DQK, DV, 16) || T < 1 || T > step_multi_max_tokens()) return MLSTM_ERR_SHAPE;
+  if (!q || !k || !v || !ig || !fg || !C || !n || !m || !h) return MLSTM_ERR_NULL;
+  for (const void *ptr : {(const void *)q, (const void *)k, (const void *)v, (const void *)ig, (const void *)fg,
+                          (const void *)C, (const void *)n, (const void *)m, (const void *)h})
+    if (!aligned16(ptr)) return MLSTM_ERR_ALIGN;
+  if (mlstm_status st = check_device()) return st;
+  return launch_status(launch_step_multi(q, k, v, dt == MLSTM_BF16, h_dt == MLSTM_BF16, ig, fg, C, n, m, h,
+                                         B * NH, T, DQK, DV, (cudaStream_t)stream));
+}
+
 // ---------------------------------------------------------------- forward without allocation
 // The scratch of mlstm_fwd_chunkwise_noalloc: a fixed array in device memory, part of the
 // library's image, so that every GPU that loads the library holds it until the process exits.

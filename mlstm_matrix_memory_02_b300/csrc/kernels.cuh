@@ -39,6 +39,12 @@ cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, bool out_
                           const float *n_init, void *h, float *C_last, float *n_last, float *m_last, int *err,
                           cudaStream_t stream);
 
+// (d') T consecutive decode steps in one launch, in place (T <= step_multi_max_tokens()).
+int step_multi_max_tokens();
+cudaError_t launch_step_multi(const void *q, const void *k, const void *v, bool bf16, bool out_bf16,
+                              const float *ig, const float *fg, float *C, float *n, float *m, void *h, int P,
+                              int NT, int DQK, int DV, cudaStream_t stream);
+
 // small helpers
 cudaError_t launch_copy_chunk_m(const float *cm, int P, int NC, float *m_last, cudaStream_t stream);
 

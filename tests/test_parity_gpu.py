@@ -197,6 +197,93 @@ def test_decode_step_fp32_matches_oracle(B):
     assert eC <= TOL_F32 and en <= TOL_F32 and em <= 1e-5
 
 
+@pytest.mark.parametrize("T,dtype,dqk,dv", [(1, "f32", 64, 96), (3, "f32", 96, 64), (16, "f32", 64, 64),
+                                            (5, "bf16", 256, 256), (16, "bf16", 512, 128)])
+def test_step_multi_matches_oracle(B, T, dtype, dqk, dv):
+    """T decode steps in one launch from a prior state: h of every token and the final state."""
+    w = W.DECODE.with_(B=3, NH=2, S=T, prior=40, DQK=dqk, DV=dv, dtype=dtype)
+    prior, steps = W.make_decode_inputs(w)
+    o_prior = oracle.recurrent(**prior, want_h=False)
+    o = oracle.recurrent(**steps, C0=o_prior["C"], n0=o_prior["n"], m0=o_prior["m"])
+    C = torch.from_numpy(o_prior["C"].astype(np.float32)).cuda()
+    n = torch.from_numpy(o_prior["n"].astype(np.float32)).cuda()
+    m = torch.from_numpy(o_prior["m"].astype(np.float32)).cuda()
+    s = dev(steps, tdt(w))
+    h = B.mlstm_step_multi(s["q"], s["k"], s["v"], s["ig"], s["fg"], C, n, m, h_dtype=torch.float32)
+    torch.cuda.synchronize()
+    tol = tol_for(w)
+    assert rel_err(npy(h), o["h"]) <= tol
+    eC, en, em = state_errs(npy(C), npy(n), npy(m), o["C"], o["n"], o["m"])
+    assert eC <= tol and en <= tol and em <= 1e-5
+
+
+def test_step_multi_equals_single_steps(B):
+    """One launch for T tokens gives what T single-step launches give (same arithmetic)."""
+    w = W.DECODE.with_(B=4, NH=2, S=7, prior=16, DQK=128, DV=192, dtype="bf16")
+    prior, steps = W.make_decode_inputs(w)
+    d = dev(prior, torch.bfloat16)
+    _, C, n, m = B.mlstm_fwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], 16, h_dtype=torch.float32)
+    C2, n2, m2 = C.clone(), n.clone(), m.clone()
+    s = dev(steps, torch.bfloat16)
+    hs = [B.mlstm_step(*(s[k_][:, :, t].contiguous() for k_ in ("q", "k", "v", "ig", "fg")), C, n, m,
+                       h_dtype=torch.float32) for t in range(w.S)]
+    hm = B.mlstm_step_multi(s["q"], s["k"], s["v"], s["ig"], s["fg"], C2, n2, m2, h_dtype=torch.float32)
+    torch.cuda.synchronize()
+    hs = torch.stack(hs, 2)
+    assert torch.allclose(hm, hs, rtol=1e-5, atol=1e-6)
+    assert torch.allclose(C2, C, rtol=1e-5, atol=1e-6) and torch.allclose(n2, n, rtol=1e-5, atol=1e-6)
+    assert torch.equal(m2, m)
+
+
+def test_step_multi_full_size_sampled_heads(B):
+    """B=256, NH=8, d=256: 4 tokens per launch, twice, on the full batch; 12 sampled heads
+    against the oracle from the oracle's own 512-token prior state."""
+    w = W.DECODE.with_(S=8)
+    prior, steps = W.make_decode_inputs(w)
+    P = w.B * w.NH
+    rng = np.random.default_rng(321)
+    sample = np.sort(rng.choice(P, 12, replace=False))
+    bi, hi = sample // w.NH, sample % w.NH
+
+    def pick(x):
+        return x[bi, hi][:, None]
+
+    o_prior = oracle.recurrent(**{k_: pick(v_) for k_, v_ in prior.items()}, want_h=False)
+    o_steps = oracle.recurrent(**{k_: pick(v_) for k_, v_ in steps.items()},
+                               C0=o_prior["C"], n0=o_prior["n"], m0=o_prior["m"])
+    d = dev(prior, torch.bfloat16)
+    _, C, n, m = B.mlstm_fwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], 64)
+    bt, ht = torch.from_numpy(bi).cuda(), torch.from_numpy(hi).cuda()
+    C[bt, ht] = torch.from_numpy(o_prior["C"][:, 0].astype(np.float32)).cuda()
+    n[bt, ht] = torch.from_numpy(o_prior["n"][:, 0].astype(np.float32)).cuda()
+    m[bt, ht] = torch.from_numpy(o_prior["m"][:, 0].astype(np.float32)).cuda()
+    s = dev(steps, torch.bfloat16)
+    hs = []
+    for t0 in (0, 4):
+        part = [s[k_][:, :, t0:t0 + 4].contiguous() for k_ in ("q", "k", "v", "ig", "fg")]
+        hs.append(B.mlstm_step_multi(*part, C, n, m, h_dtype=torch.float32)[bt, ht])
+    torch.cuda.synchronize()
+    h_gpu = npy(torch.cat(hs, dim=1))  # [12, 8, DV]
+    assert rel_err(h_gpu, o_steps["h"][:, 0]) <= TOL_BF16
+    eC, en, em = state_errs(npy(C[bt, ht]), npy(n[bt, ht]), npy(m[bt, ht]), o_steps["C"][:, 0],
+                            o_steps["n"][:, 0], o_steps["m"][:, 0])
+    assert eC <= TOL_BF16 and en <= TOL_BF16 and em <= 1e-4
+
+
+def test_step_multi_argument_errors(B):
+    q = torch.zeros(1, 1, 17, 64, device="cuda")
+    v = torch.zeros(1, 1, 17, 64, device="cuda")
+    g = torch.zeros(1, 1, 17, device="cuda")
+    C = torch.full((1, 1, 64, 64), 3.0, device="cuda")
+    n = torch.full((1, 1, 64), 3.0, device="cuda")
+    m = torch.full((1, 1), 3.0, device="cuda")
+    with pytest.raises(B.MlstmError) as e:
+        B.mlstm_step_multi(q, q, v, g, g, C, n, m)  # T = 17 > 16
+    assert e.value.code == 3
+    torch.cuda.synchronize()
+    assert bool((C == 3).all() and (n == 3).all() and (m == 3).all())
+
+
 def test_prefill_then_decode_handoff(B):
     """Chunkwise prefill over S1 tokens, then single steps, equals the oracle over S1+S2."""
     w = W.LAYER_350M.with_(B=2, NH=2, S=192, DQK=128, DV=128)
