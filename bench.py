@@ -381,7 +381,7 @@ def run_ours(args, rank, local, world):
     dec_gbs = dec_bytes(dw) / (dec_ms * 1e-3) / 1e9
     # multi-token decode: T tokens per launch, the state crosses HBM once per launch
     multi = {}
-    for T in (4, 16):
+    for T in (4, 8, 16):
         mq, mk, mv = (x[:, :, :T].contiguous() for x in (sq, sk, sv))
         mig, mfg = sig[:, :, :T].contiguous(), sfg[:, :, :T].contiguous()
         hm = torch.empty((dw.B, dw.NH, T, dw.DV), dtype=torch.float32, device=dev)

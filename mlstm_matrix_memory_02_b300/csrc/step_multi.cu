@@ -22,7 +22,44 @@ constexpr int kThreads = 256;
 constexpr int kMaxT = 16;
 }  // namespace
 
-template <typename T, typename TO>
+// Reduces 32 per-lane partial sums at once: afterwards lane l holds slot l summed over the
+// warp (five butterfly stages, 31 shuffles, instead of 5 shuffles per slot).
+__device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const bool up = lane & 16;
+    const float send = up ? v[i] : v[i + 16], keep = up ? v[i + 16] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool up = lane & 8;
+    const float send = up ? v[i] : v[i + 8], keep = up ? v[i + 8] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const bool up = lane & 4;
+    const float send = up ? v[i] : v[i + 4], keep = up ? v[i + 4] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const bool up = lane & 2;
+    const float send = up ? v[i] : v[i + 2], keep = up ? v[i + 2] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+  }
+  {
+    const bool up = lane & 1;
+    const float send = up ? v[0] : v[1], keep = up ? v[1] : v[0];
+    v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+  }
+  return v[0];
+}
+
+// BUTTERFLY: reduce the 2 T dot products of a row pair together (worth it from T = 8 on; below
+// that the per-dot warp sums are cheaper and the kernel needs half the registers).
+template <typename T, typename TO, bool BUTTERFLY>
 __global__ void __launch_bounds__(kThreads) step_multi_kernel(
     const T *__restrict__ qin, const T *__restrict__ kin, const T *__restrict__ vin, const float *__restrict__ ig,
     const float *__restrict__ fg, float *__restrict__ C, float *__restrict__ n, float *__restrict__ m,
@@ -111,33 +148,73 @@ __global__ void __launch_bounds__(kThreads) step_multi_kernel(
         else x[i][j] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-    for (int t = 0; t < NT; ++t) {
-      const float al = s_alpha[t], inv = s_inv[t];
+    if (BUTTERFLY) {
+      // the 2 NT dot products of this row pair (slot i NT + t) are reduced together at the end
+      float dots[32];
 #pragma unroll
-      for (int i = 0; i < kRowsInFlight; ++i) {
-        const int a = a0 + i;
-        if (a >= DV) break;
-        const float va = sv[t * DV + a];
-        float dot = 0.f;
+      for (int sl = 0; sl < 32; ++sl) dots[sl] = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int c4 = lane + 32 * j;
-          if (j < per_lane && c4 < nv4) {
-            const float4 kv = sk4[t * nv4 + c4], qv = sq4[t * nv4 + c4];
-            float4 y = x[i][j];
-            y.x = fmaf(al, y.x, va * kv.x);
-            y.y = fmaf(al, y.y, va * kv.y);
-            y.z = fmaf(al, y.z, va * kv.z);
-            y.w = fmaf(al, y.w, va * kv.w);
-            x[i][j] = y;
-            dot = fmaf(y.x, qv.x, dot);
-            dot = fmaf(y.y, qv.y, dot);
-            dot = fmaf(y.z, qv.z, dot);
-            dot = fmaf(y.w, qv.w, dot);
+      for (int t = 0; t < kMaxT; ++t) {
+        if (t < NT) {
+          const float al = s_alpha[t];
+#pragma unroll
+          for (int i = 0; i < kRowsInFlight; ++i) {
+            const int a = a0 + i;
+            const float va = a < DV ? sv[t * DV + a] : 0.f;
+            float dot = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int c4 = lane + 32 * j;
+              if (j < per_lane && c4 < nv4) {
+                const float4 kv = sk4[t * nv4 + c4], qv = sq4[t * nv4 + c4];
+                float4 y = x[i][j];
+                y.x = fmaf(al, y.x, va * kv.x);
+                y.y = fmaf(al, y.y, va * kv.y);
+                y.z = fmaf(al, y.z, va * kv.z);
+                y.w = fmaf(al, y.w, va * kv.w);
+                x[i][j] = y;
+                dot = fmaf(y.x, qv.x, dot);
+                dot = fmaf(y.y, qv.y, dot);
+                dot = fmaf(y.z, qv.z, dot);
+                dot = fmaf(y.w, qv.w, dot);
+              }
+            }
+            dots[i * kMaxT + t] = dot;
           }
         }
-        dot = warp_sum(dot);
-        if (lane == 0) h[((size_t)p * NT + t) * DV + a] = from_f32<TO>(dot * inv);
+      }
+      const float tot = transpose_reduce32(dots, lane);
+      const int i = lane / kMaxT, t = lane % kMaxT, a = a0 + i;
+      if (t < NT && a < DV) h[((size_t)p * NT + t) * DV + a] = from_f32<TO>(tot * s_inv[t]);
+    } else {
+      for (int t = 0; t < NT; ++t) {
+        const float al = s_alpha[t], inv = s_inv[t];
+#pragma unroll
+        for (int i = 0; i < kRowsInFlight; ++i) {
+          const int a = a0 + i;
+          if (a >= DV) break;
+          const float va = sv[t * DV + a];
+          float dot = 0.f;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c4 = lane + 32 * j;
+            if (j < per_lane && c4 < nv4) {
+              const float4 kv = sk4[t * nv4 + c4], qv = sq4[t * nv4 + c4];
+              float4 y = x[i][j];
+              y.x = fmaf(al, y.x, va * kv.x);
+              y.y = fmaf(al, y.y, va * kv.y);
+              y.z = fmaf(al, y.z, va * kv.z);
+              y.w = fmaf(al, y.w, va * kv.w);
+              x[i][j] = y;
+              dot = fmaf(y.x, qv.x, dot);
+              dot = fmaf(y.y, qv.y, dot);
+              dot = fmaf(y.z, qv.z, dot);
+              dot = fmaf(y.w, qv.w, dot);
+            }
+          }
+          dot = warp_sum(dot);
+          if (lane == 0) h[((size_t)p * NT + t) * DV + a] = from_f32<TO>(dot * inv);
+        }
       }
     }
 #pragma unroll
@@ -156,7 +233,7 @@ template <typename T, typename TO>
 cudaError_t launch_step_multi_t(const void *q, const void *k, const void *v, const float *ig, const float *fg,
                                 float *C, float *n, float *m, void *h, int P, int NT, int DQK, int DV,
                                 cudaStream_t stream) {
-  auto kern = step_multi_kernel<T, TO>;
+  auto kern = NT >= 8 ? step_multi_kernel<T, TO, true> : step_multi_kernel<T, TO, false>;
   const size_t smem = (size_t)NT * (2 * DQK + DV) * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
