@@ -473,8 +473,9 @@ def run_ours(args, rank, local, world):
 def run_profile(kind: str):
     """Small, self-contained launches for ncu captures: one warm-up and one timed-shape call.
 
-    fwd:    the --workload forward (gates, then the state passing and output stage)
-    decode: one decode step of the B=256, NH=8, d=256 state (state initialised randomly)"""
+    fwd:          the --workload forward (one fused launch on the tensor-core path)
+    decode:       one decode step of the B=256, NH=8, d=256 state (state initialised randomly)
+    decode_multi: 16 decode steps in one launch on the same state"""
     import torch
     from mlstm_matrix_memory_02_b300 import binding as B
     dev = torch.device("cuda", 0)
@@ -485,6 +486,18 @@ def run_profile(kind: str):
         ig, fg = (torch.from_numpy(inp[x]).to(dev) for x in ("ig", "fg"))
         for _ in range(2):
             B.mlstm_fwd_chunkwise(q, k, v, ig, fg, w.chunk, h_dtype=torch.float32)
+    elif kind == "decode_multi":
+        w = DEC
+        T = 16
+        g = torch.Generator(device=dev).manual_seed(0)
+        C = torch.randn((w.B, w.NH, w.DV, w.DQK), device=dev, generator=g)
+        n = torch.randn((w.B, w.NH, w.DQK), device=dev, generator=g)
+        m = torch.zeros((w.B, w.NH), device=dev)
+        q, k = (torch.randn((w.B, w.NH, T, w.DQK), device=dev, generator=g).to(torch.bfloat16) for _ in range(2))
+        v = torch.randn((w.B, w.NH, T, w.DV), device=dev, generator=g).to(torch.bfloat16)
+        ig, fg = (torch.randn((w.B, w.NH, T), device=dev, generator=g) for _ in range(2))
+        for _ in range(2):
+            B.mlstm_step_multi(q, k, v, ig, fg, C, n, m, h_dtype=torch.float32)
     else:
         w = DEC
         P = w.B * w.NH
@@ -511,7 +524,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["1p3b", "350m", "stress"], default="1p3b",
                     help="forward workload (default: the 1.3B-style layer)")
-    ap.add_argument("--profile", choices=["fwd", "decode"], default=None,
+    ap.add_argument("--profile", choices=["fwd", "decode", "decode_multi"], default=None,
                     help="run one small forward or decode step for ncu captures and exit")
     args = ap.parse_args()
     global FWD
