@@ -25,20 +25,35 @@
 // rescaled frame C = exp(sigma) T: the chunk decay is folded into sigma and into the scale of the
 // update's k operand, and T is multiplied back only when exp(-sigma) would exceed 2^8.
 //
-// Warp roles (640 threads): warp 0 issues TMA loads of q and k (one stage, L2 prefetch two
-// chunks ahead), warp 3 those of v (two stages); warp 1 allocates tensor memory and issues every
-// MMA; warp 2 preprocesses the gates and computes the per-chunk factors; warpgroup 1 (warps 4-7)
-// forms P and the denominators; warpgroup 2 (warps 8-11) copies the state to fp16 (the serial
-// chain of the recurrence), forms w k and keeps n; warpgroup 3 (warps 12-15) forms v and beta q
-// in fp16 and n.q; warpgroup 4 (warps 16-19) reads H, completes it with the partner's columns
-// and writes h.  Hand-offs use mbarriers; every wait is bounded in time and reports through an
-// error word.
+// q and k pass through two shared-memory stages.  A stage is read raw by the S product and then
+// converted in place: q to beta q (B operand of the C q product), k to w k (B operand of the
+// state update).  With two stages the operands of chunk k+1 are formed while chunk k's products
+// run, so the serial chain of the recurrence is only: state copy to fp16, C q, state update.
+//
+// Warp roles (640 threads): warp 1 allocates tensor memory, issues the state chain's MMAs (C q,
+// the update) and the TMA loads of q and k into the stage each update frees; warp 0 issues the S
+// and P V products; warp 3 issues the TMA loads of v (two stages, L2 prefetch two chunks ahead
+// for q, k and v); warp 2
+// preprocesses the gates and computes the per-chunk factors; warpgroup 1 (warps 4-7) reads S,
+// forms w k and the n-update partial sums, then P and the denominators; warpgroup 2 (warps 8-11)
+// copies the state to fp16 (the serial chain) and stores the final state; warpgroup 3 (warps
+// 12-15) keeps n and forms v and beta q in fp16 and n.q; warpgroup 4 (warps 16-19) reads H,
+// completes it with the partner's columns and writes h.  Hand-offs use mbarriers; every wait is
+// bounded in time and reports through an error word.
 //
 // Operand precision: q, k, v arrive as bf16 and convert to fp16 exactly; the computed operands
 // (P, beta q, w k and the state copy) are rounded to fp16 (11 significant bits); sums are fp32.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#ifdef MLSTM_TRACE
+// poll iterations of the bounded waits, per warp of CTA (0, 0)
+__device__ unsigned long long g_polls[32];
+#define MLSTM_POLL_HOOK()                                                                               \
+  do {                                                                                                  \
+    if (blockIdx.x == 0 && blockIdx.y == 0 && (threadIdx.x & 31) == 0) atomicAdd(&g_polls[threadIdx.x >> 5], 1ull); \
+  } while (0)
+#endif
 #include "common.cuh"
 #include "kernels.cuh"
 #include "sm100.cuh"
@@ -52,12 +67,41 @@ __device__ long long g_trace[2][8][512][8];
   do {                                                                                                \
     if (blockIdx.x < 2 && blockIdx.y == 0 && (k) < 512) g_trace[blockIdx.x][role][k][ev] = clock64(); \
   } while (0)
+// per CTA: global timer at entry and exit, SM id
+__device__ unsigned long long g_span[2048][3];
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ unsigned smid() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
+#define SPAN(ev)                                                          \
+  do {                                                                    \
+    const unsigned b_ = blockIdx.y * gridDim.x + blockIdx.x;              \
+    if (b_ < 2048) {                                                      \
+      g_span[b_][ev] = global_ns();                                       \
+      if ((ev) == 0) g_span[b_][2] = smid();                              \
+    }                                                                     \
+  } while (0)
 extern "C" int mlstm_trace_read(long long *dst, size_t bytes) {
   return (int)cudaMemcpyFromSymbol(dst, g_trace, bytes < sizeof(g_trace) ? bytes : sizeof(g_trace));
+}
+extern "C" int mlstm_polls_read(unsigned long long *dst) {
+  return (int)cudaMemcpyFromSymbol(dst, g_polls, sizeof(g_polls));
+}
+extern "C" int mlstm_span_read(unsigned long long *dst, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(dst, g_span, bytes < sizeof(g_span) ? bytes : sizeof(g_span));
 }
 #else
 #define TRACE(role, k, ev) \
   do {                     \
+  } while (0)
+#define SPAN(ev) \
+  do {           \
   } while (0)
 #endif
 
@@ -89,16 +133,17 @@ struct Gate {
 };
 
 struct Smem {
-  uint64_t qk_full, qk_empty, v_full[2], v_empty[2], g_full[2], bar_nq[2];
-  uint64_t bar_S, sfree, bar_U, bar_H, hfree, cready, opready, pready, fin, n_ready;
+  uint64_t qk_full[2], qk_empty[2], v_full[2], v_empty[2], g_full[2], bar_nq[2];
+  uint64_t bar_S[2], xready[2], kready[2];  // by chunk parity: the producers may run a chunk ahead
+  uint64_t sfree, bar_X, bar_U, bar_H, hfree, cready, npart_free, pready, fin;
   uint64_t sx_full[2], sx_free[2], hx_full, hx_free, nqx_full[2], nqx_free[2];
   uint64_t inv_ready[2], inv_free[2];  // 1/den of a chunk: written by warpgroup 1, read by warpgroup 4
   uint64_t grp[3];  // bounded group barriers of warpgroups 1, 2 and 3
   uint32_t tmem_base;
   int abort_flag;
   alignas(16) Gate g[2];
-  alignas(16) float n[256];       // normaliser, this CTA's d_qk columns (read as float4)
-  alignas(16) float npart[1024];  // n-update partial sums of warpgroup 3
+  alignas(16) float n[2][256];    // normaliser entering chunk k in n[k & 1], this CTA's d_qk columns
+  alignas(16) float npart[1024];  // n-update partial sums of a chunk (warpgroup 1 -> warpgroup 3)
   float nq[2][kL];       // n . q_r over this CTA's columns
   float nqx[2][32];      // partner's n . q_r for the rows finalised here (written remotely)
   float inv[2][kL];      // 1 / max(|den_r|, exp(-m_r))
@@ -169,21 +214,21 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
   constexpr int NR = PAIR ? 32 : 64;     // output rows finalised per CTA
   static_assert(DH == 64 || DH == 128 || DH == 256, "DH");
   // dynamic shared memory map (every region 1024-byte aligned)
-  constexpr int OFF_RQ = 0, OFF_RK = QB, OFF_BQ = 2 * QB, OFF_WK = 3 * QB, OFF_V = 4 * QB;
+  constexpr int OFF_V = 4 * QB;  // [0, 4 QB): two stages of (q, k)
   constexpr int OFF_P = OFF_V + 2 * 16384, OFF_SO = OFF_P + 8192, OFF_SX = OFF_SO + NR * 256;
   constexpr int OFF_HX = OFF_SX + 16384;
 
   extern __shared__ uint8_t smem_dyn[];
   __shared__ Smem sm;
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-  uint8_t *const sRQ = base + OFF_RQ;  // raw q of the chunk (bf16, TMA, 128-byte swizzle)
-  uint8_t *const sRK = base + OFF_RK;  // raw k
-  uint8_t *const sBQ = base + OFF_BQ;  // beta_r q_r, fp16 (B operand of the C q product)
-  uint8_t *const sWK = base + OFF_WK;  // w_j k_j, fp16 (B operand of the state update)
   uint8_t *const sP = base + OFF_P;    // P, fp16 [64 x 64], K-major
   float *const SO = reinterpret_cast<float *>(base + OFF_SO);  // this CTA's partial S rows [NR][64]
   float *const SX = reinterpret_cast<float *>(base + OFF_SX);  // [2][32][64] partner's partial S rows
   float *const HX = reinterpret_cast<float *>(base + OFF_HX);  // [128][32] partner's H^T columns
+// stage s of q (raw bf16 from TMA with 128-byte swizzle, then beta q in fp16) and of k (raw,
+// then w k in fp16); v stage s (bf16, then fp16)
+#define STQ(s_) (base + (2 * (s_)) * QB)
+#define STK(s_) (base + (2 * (s_) + 1) * QB)
 #define STV(s_) (base + OFF_V + (s_) * 16384)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -199,11 +244,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
   // second, long after the first CTA has started).
   if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) *(volatile int *)err = 0;
   if (threadIdx.x == 0) {
-    mbar_init(&sm.qk_full, 1);
-    mbar_init(&sm.qk_empty, 1 + 256);  // the S MMA (commit) and the reads of warpgroups 2 and 3
+    SPAN(0);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.qk_full[i], 1);
+      mbar_init(&sm.qk_empty[i], 1);  // committed after the state update that last reads the stage
       mbar_init(&sm.v_full[i], 1);
-      mbar_init(&sm.v_empty[i], 1);
+      mbar_init(&sm.v_empty[i], 2);  // the state update (warp 1) and P V (warp 0) of the chunk
       mbar_init(&sm.g_full[i], 1);
       mbar_init(&sm.bar_nq[i], 128);
       mbar_init(&sm.sx_full[i], 1);
@@ -211,16 +257,20 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       mbar_init(&sm.nqx_full[i], 1);
       mbar_init(&sm.nqx_free[i], 4);
     }
-    mbar_init(&sm.bar_S, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.bar_S[i], 1);
+      mbar_init(&sm.xready[i], 128);  // warpgroup 3: beta q and v in fp16
+      mbar_init(&sm.kready[i], 128);  // warpgroup 1: w k in fp16 and the n-update partial sums
+    }
     mbar_init(&sm.sfree, 128);
+    mbar_init(&sm.bar_X, 1);
     mbar_init(&sm.bar_U, 1);
     mbar_init(&sm.bar_H, 1);
     mbar_init(&sm.hfree, 128);
     mbar_init(&sm.cready, 128);
-    mbar_init(&sm.opready, 256);  // warpgroup 3 (beta q, v) and warpgroup 2 (w k)
-    mbar_init(&sm.n_ready, 128);
+    mbar_init(&sm.npart_free, 128);  // warpgroup 3 has read the partial sums
     mbar_init(&sm.pready, 128);
-    mbar_init(&sm.fin, 1);
+    mbar_init(&sm.fin, 2);  // both MMA issuers
     mbar_init(&sm.hx_full, 1);
     mbar_init(&sm.hx_free, 4);
     for (int i = 0; i < 3; ++i) mbar_init(&sm.grp[i], 128);
@@ -243,37 +293,47 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
   if (threadIdx.x == 0) TRACE(0, 511, 0);
 
   if (warp == 0) {
-    // ------------------------------------------------------------------ TMA: q and k (one stage)
+    // ------------------------------------------------------------------ MMA issuer: S and P V
     if (lane == 0) {
-      prefetch_tensormap(&mapQ);
-      prefetch_tensormap(&mapK);
-      for (int k = 0; k < 2 && k < NC; ++k)
-#pragma unroll
-        for (int kb = 0; kb < DH / 64; ++kb) {
-          tma_prefetch_2d(&mapQ, c0 + kb * 64, p * S + k * kL);
-          tma_prefetch_2d(&mapK, c0 + kb * 64, p * S + k * kL);
-        }
-      int issued = 0;
-      for (int k = 0; k < NC; ++k) {
-        if (k >= 1 && !mbar_wait(&sm.qk_empty, (k - 1) & 1, err, 11, abort_ptr)) { set_abort(sm); break; }
-        if (aborted(sm)) break;
-        TRACE(0, k, 0);
-        mbar_arrive_expect_tx(&sm.qk_full, (uint32_t)(2 * QB));
-        const int row = p * S + k * kL;
-#pragma unroll
-        for (int kb = 0; kb < DH / 64; ++kb) {
-          tma_load_2d(sRQ + kb * 8192, &mapQ, c0 + kb * 64, row, &sm.qk_full);
-          tma_load_2d(sRK + kb * 8192, &mapK, c0 + kb * 64, row, &sm.qk_full);
-        }
-        if (k + 2 < NC)
-#pragma unroll
-          for (int kb = 0; kb < DH / 64; ++kb) {
-            tma_prefetch_2d(&mapQ, c0 + kb * 64, row + 2 * kL);
-            tma_prefetch_2d(&mapK, c0 + kb * 64, row + 2 * kL);
+      const uint32_t id_S = idesc_f16(64, kL, /*bf16*/ 1, 0, 0);
+      const uint32_t id_P = idesc_f16(kTile, NR, 0, 1, 0);
+      const uint64_t dp_own = smem_desc(smem_u32(sP) + r_lo * 128, 16, 1024, kSwizzle128B);
+      // per step k: S_k = Q K^T (raw bf16 inputs) once its stage has landed and the S columns are
+      // free, then H^T[own rows] += V^T P^T of chunk k-1 once P is formed and X_{k-1} is done
+      int k = 0;
+      for (; k <= NC; ++k) {
+        if (k < NC) {
+          const int s = k & 1;
+          if (!mbar_wait(&sm.qk_full[s], (k >> 1) & 1, err, 12, abort_ptr)) break;
+          if (k >= 1 && !mbar_wait(&sm.sfree, (k - 1) & 1, err, 13, abort_ptr)) break;
+          tc_fence_after();
+          TRACE(1, k, 0);
+          const uint64_t dq_raw = smem_desc(smem_u32(STQ(s)), 16, 1024, kSwizzle128B);
+          const uint64_t dk_raw = smem_desc(smem_u32(STK(s)), 16, 1024, kSwizzle128B);
+#pragma unroll 1
+          for (int c = 0; c < DH / 16; ++c) {
+            const uint64_t off = (uint64_t)(((c >> 2) * 8192 + (c & 3) * 32) >> 4);
+            mma_f16_ss(tm + kColS, dq_raw + off, dk_raw + off, id_S, c > 0);
           }
-        issued = k + 1;
+          mma_commit(&sm.bar_S[s]);
+        }
+        if (k >= 1) {
+          const int kp = k - 1;
+          if (!mbar_wait(&sm.pready, kp & 1, err, 17, abort_ptr)) break;
+          if (!mbar_wait(&sm.bar_X, kp & 1, err, 9, abort_ptr)) break;
+          tc_fence_after();
+          TRACE(1, kp, 4);
+          const uint64_t dv = smem_desc(smem_u32(STV(kp & 1)), 8192, 1024, kSwizzle128B);
+#pragma unroll 1
+          for (int kk = 0; kk < kL / 16; ++kk)
+            mma_f16_ss(tm + kColH + r_lo, dv + (uint64_t)(kk * 2048 >> 4), dp_own + (uint64_t)(kk * 32 >> 4), id_P, 1);
+          mma_commit(&sm.bar_H);
+          mma_commit(&sm.v_empty[kp & 1]);
+        }
       }
-      if (issued > 0) mbar_wait(&sm.qk_full, (issued - 1) & 1, err, 19);  // the last copies land
+      if (k <= NC) set_abort(sm);
+      mma_commit(&sm.fin);
+      mbar_wait(&sm.fin, 0, err, 8);
     }
   } else if (warp == 3) {
     // ------------------------------------------------------------------ TMA: v (two stages)
@@ -300,69 +360,60 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t id_S = idesc_f16(64, kL, /*bf16*/ 1, 0, 0);
       const uint32_t id_X = idesc_f16(kTile, kL, 0, 0, 0);
       const uint32_t id_U = idesc_f16(kTile, DH, 0, /*a MN-major*/ 1, /*b MN-major*/ 1);
-      const uint32_t id_P = idesc_f16(kTile, NR, 0, 1, 0);
-      const uint32_t q_raw = smem_u32(sRQ), k_raw = smem_u32(sRK), q_b = smem_u32(sBQ), k_w = smem_u32(sWK);
-      const uint32_t p_own = smem_u32(sP) + r_lo * 128;
-      // S_k = Q K^T over this CTA's d_qk columns (raw bf16 inputs)
-      auto issue_S_now = [&](int kk) {
-        tc_fence_after();
-        TRACE(1, kk, 0);
-#pragma unroll
-        for (int c = 0; c < DH / 16; ++c) {
-          const uint32_t off = (c >> 2) * 8192 + (c & 3) * 32;
-          mma_f16_ss(tm + kColS, smem_desc(q_raw + off, 16, 1024, kSwizzle128B),
-                     smem_desc(k_raw + off, 16, 1024, kSwizzle128B), id_S, c > 0);
+      // The state chain: X_k (H^T = C16 (beta q)^T) and U_k (T += V^T (w k)), and the q/k loads
+      // of chunk k+2 into the stage that U_k frees.  S and P V are issued by warp 0, so that
+      // neither chain waits behind the other.  Descriptors are advanced by adding (byte offset >> 4)
+      // to the start-address field; the loops stay rolled.
+      prefetch_tensormap(&mapQ);
+      prefetch_tensormap(&mapK);
+      auto load_qk = [&](int kk) {
+        const int s = kk & 1, row = p * S + kk * kL;
+        TRACE(0, kk, 0);
+        mbar_arrive_expect_tx(&sm.qk_full[s], (uint32_t)(2 * QB));
+#pragma unroll 1
+        for (int kb = 0; kb < DH / 64; ++kb) {
+          tma_load_2d(STQ(s) + kb * 8192, &mapQ, c0 + kb * 64, row, &sm.qk_full[s]);
+          tma_load_2d(STK(s) + kb * 8192, &mapK, c0 + kb * 64, row, &sm.qk_full[s]);
+          if (kk + 2 < NC) {
+            tma_prefetch_2d(&mapQ, c0 + kb * 64, row + 2 * kL);
+            tma_prefetch_2d(&mapK, c0 + kb * 64, row + 2 * kL);
+          }
         }
-        mma_commit(&sm.bar_S);
-        mma_commit(&sm.qk_empty);
       };
-      auto issue_S = [&](int kk) -> bool {
-        if (!mbar_wait(&sm.qk_full, kk & 1, err, 12, abort_ptr)) return false;
-        if (kk >= 1 && !mbar_wait(&sm.sfree, (kk - 1) & 1, err, 13, abort_ptr)) return false;
-        issue_S_now(kk);
-        return true;
-      };
-      // Tensor-pipe order per chunk k: X_k, U_k, S_{k+1}, PV_k.  S of the next chunk goes ahead of
-      // P V so that the next P is formed while this chunk finishes.
+      for (int kk = 0; kk < 2 && kk < NC; ++kk) load_qk(kk);
       int k = 0;
-      bool ok = NC == 0 || issue_S(0);
-      for (; ok && k < NC; ++k) {
+      for (; k < NC; ++k) {
         const int s = k & 1;
-        const uint32_t v_s = smem_u32(STV(s));
-        // H^T = C16 (beta q)^T and T += V^T (w k): the state copy, the operands and a free H
         if (!mbar_wait(&sm.cready, k & 1, err, 14, abort_ptr)) break;
-        TRACE(1, k, 1);
-        if (!mbar_wait(&sm.opready, k & 1, err, 15, abort_ptr)) break;
-        TRACE(1, k, 2);
+        if (!mbar_wait(&sm.xready[s], (k >> 1) & 1, err, 15, abort_ptr)) break;
         if (k >= 1 && !mbar_wait(&sm.hfree, (k - 1) & 1, err, 16, abort_ptr)) break;
-        TRACE(1, k, 3);
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-          mma_f16_ts(tm + kColH, tm + kColC16 + kk * 8, smem_desc(q_b + off, 16, 1024, kSwizzle128B), id_X, kk > 0);
-        }
-#pragma unroll
+        TRACE(1, k, 1);
+        const uint64_t dq_b = smem_desc(smem_u32(STQ(s)), 16, 1024, kSwizzle128B);
+#pragma unroll 1
+        for (int kk = 0; kk < DH / 16; ++kk)
+          mma_f16_ts(tm + kColH, tm + kColC16 + kk * 8, dq_b + (uint64_t)(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4),
+                     id_X, kk > 0);
+        mma_commit(&sm.bar_X);
+        if (!mbar_wait(&sm.kready[s], (k >> 1) & 1, err, 10, abort_ptr)) break;
+        tc_fence_after();
+        TRACE(1, k, 2);
+        const uint64_t dv = smem_desc(smem_u32(STV(s)), 8192, 1024, kSwizzle128B);
+        const uint64_t dk_w = smem_desc(smem_u32(STK(s)), 8192, 1024, kSwizzle128B);
+#pragma unroll 1
         for (int kk = 0; kk < kL / 16; ++kk)
-          mma_f16_ss(tm, smem_desc(v_s + kk * 2048, 8192, 1024, kSwizzle128B),
-                     smem_desc(k_w + kk * 2048, 8192, 1024, kSwizzle128B), id_U, 1);
+          mma_f16_ss(tm, dv + (uint64_t)(kk * 2048 >> 4), dk_w + (uint64_t)(kk * 2048 >> 4), id_U, 1);
         mma_commit(&sm.bar_U);
-        const bool s_next = k + 1 >= NC;
-        if (!mbar_wait(&sm.pready, k & 1, err, 17, abort_ptr)) break;
-        TRACE(1, k, 4);
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kL / 16; ++kk)
-          mma_f16_ss(tm + kColH + r_lo, smem_desc(v_s + kk * 2048, 8192, 1024, kSwizzle128B),
-                     smem_desc(p_own + kk * 32, 16, 1024, kSwizzle128B), id_P, 1);
-        mma_commit(&sm.bar_H);
-        mma_commit(&sm.v_empty[s]);
-        if (!s_next && !issue_S(k + 1)) break;
+        mma_commit(&sm.qk_empty[s]);
+        mma_commit(&sm.v_empty[s]);  // with warp 0's commit after P V
+        // stage s is free once X_k and U_k (the last readers of beta q and w k) are done
+        if (k + 2 < NC) {
+          if (!mbar_wait(&sm.qk_empty[s], (k >> 1) & 1, err, 11, abort_ptr)) break;
+          load_qk(k + 2);
+        }
       }
-      if (!ok) k = -1;
       if (k < NC) set_abort(sm);
       mma_commit(&sm.fin);  // completes once every MMA issued above has finished
       mbar_wait(&sm.fin, 0, err, 18);
@@ -371,6 +422,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
     // ------------------------------------------------------------------ gate factors
     float sigma = 0.f;  // frame of T entering the chunk: C = exp(sigma) T
     float m_chain = m_init ? m_init[p] : 0.f;  // stabiliser entering the chunk (raw-gate mode)
+    // raw pre-activations of the next chunk, loaded one chunk ahead
+    float2 f2n = make_float2(0.f, 0.f), i2n = f2n;
+    if (igp != nullptr && NC > 0) {
+      f2n = *reinterpret_cast<const float2 *>(fgp + (size_t)p * S + 2 * lane);
+      i2n = *reinterpret_cast<const float2 *>(igp + (size_t)p * S + 2 * lane);
+    }
     for (int k = 0; k < NC; ++k) {
       const int s = k & 1;
       // the factors of chunk k share the lifetime of v stage s (free once PV of chunk k-2 is done)
@@ -382,8 +439,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       float bb[2], xx[2], uu[2], m_in, m_out;
       if (igp != nullptr) {
         // from the raw pre-activations (the same operations, in the same order, as the gate kernel)
-        const float2 f2 = *reinterpret_cast<const float2 *>(fgp + tok0 + 2 * lane);
-        const float2 i2 = *reinterpret_cast<const float2 *>(igp + tok0 + 2 * lane);
+        const float2 f2 = f2n, i2 = i2n;
+        if (k + 1 < NC) {
+          f2n = *reinterpret_cast<const float2 *>(fgp + tok0 + kL + 2 * lane);
+          i2n = *reinterpret_cast<const float2 *>(igp + tok0 + kL + 2 * lane);
+        }
         float lf0 = log_sigmoid(f2.x), lf1 = log_sigmoid(f2.y);
         float bsum = lf0;
         bsum += lf1;
@@ -456,9 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       }
     }
   } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------------ warpgroup 1: P and h
-    // Software-pipelined over chunks: the H columns of chunk k and the S rows of chunk k+1 are
-    // read and sent to the partner before the partner's halves of either are waited for.
+    // ------------------------------------------------------------------ warpgroup 1: S, w k and P
+    // Per chunk: the S rows (own rows kept, the partner's sent), then w k and the n-update partial
+    // sums while the partner's S rows are in flight, then P and the denominators.
     const int t = threadIdx.x - 128;  // tensor-memory lane = d_v row within the tile
     const int q4 = warp & 3;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
@@ -468,13 +528,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
     constexpr int SEG = kL / TPR;  // columns per thread (16 or 32)
     const int pi = t / TPR, pseg = t % TPR;
     const int pr = r_lo + pi;  // the row this thread forms
+    constexpr int KCPR = DH / 8;     // w k pass: 16-byte chunks per row of k
+    constexpr int KRG = 128 / KCPR;  // rows handled at once (column layout)
+    const int kcc = t % KCPR, krg = t / KCPR;
+    const int kcolb = (kcc >> 3) * 8192, kc8 = kcc & 7;
     uint32_t gph = 0;
 
     // S rows of chunk kk: own rows -> SO, the partner's rows -> partner's SX
     auto s_read = [&](int kk) -> bool {
       const int s = kk & 1, par = kk & 1;
       if (!mbar_wait(&sm.g_full[s], (kk >> 1) & 1, err, 21, abort_ptr)) return false;
-      if (!mbar_wait(&sm.bar_S, kk & 1, err, 22, abort_ptr)) return false;
+      if (!mbar_wait(&sm.bar_S[kk & 1], (kk >> 1) & 1, err, 22, abort_ptr)) return false;
       if (t == 0) TRACE(3, kk, 0);
       tc_fence_after();
       uint32_t u[2][32];
@@ -483,6 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&sm.sfree);
+      // S of the next chunk can complete before every thread is done with the previous P rows:
+      // SO is rewritten only after the whole group has left the previous p_form
+      if (kk >= 1 && !group_sync(&sm.grp[0], gph, err, 38, abort_ptr)) return false;
       if (own_rows) {
         if (lane < 16) {
           const int i = r_s - r_lo;
@@ -510,6 +577,56 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       return true;
     };
 
+    // w_j k_j (frame of T) in fp16, in place over the raw k of the stage, and the n-update partial
+    // sums sum_j w_j k_j / sqrt(d) (column layout), once the S product of the chunk has read raw k
+    auto k_pass = [&](int kk) -> bool {
+      const int s = kk & 1;
+      if (!mbar_wait(&sm.qk_full[s], (kk >> 1) & 1, err, 36, abort_ptr)) return false;
+      if (kk >= 1 && !mbar_wait(&sm.npart_free, (kk - 1) & 1, err, 37, abort_ptr)) return false;
+      if (t == 0) TRACE(7, kk, 0);
+      const Gate &g = sm.g[s];
+      uint8_t *const kb = STK(s);
+      // rows in batches of four: every load of a batch is issued before its stores
+      uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll 1
+      for (int i0 = 0; i0 < 64 / KRG; i0 += 4) {
+        uint4 raw[4];
+        int off[4];
+        float wt[4], wk[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int j = krg + KRG * (i0 + b);
+          off[b] = kcolb + j * 128 + ((kc8 ^ (j & 7)) << 4);
+          raw[b] = *reinterpret_cast<const uint4 *>(kb + off[b]);
+          wt[b] = g.wt[j];
+          wk[b] = g.wk[j];
+        }
+        uint4 o4[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const uint64_t wt2 = f2pack(wt[b], wt[b]), wk2 = f2pack(wk[b], wk[b]);
+          const uint64_t x0 = bf2_to_f2(raw[b].x), x1 = bf2_to_f2(raw[b].y), x2 = bf2_to_f2(raw[b].z),
+                         x3 = bf2_to_f2(raw[b].w);
+          acc[0] = f2fma(wt2, x0, acc[0]);
+          acc[1] = f2fma(wt2, x1, acc[1]);
+          acc[2] = f2fma(wt2, x2, acc[2]);
+          acc[3] = f2fma(wt2, x3, acc[3]);
+          o4[b].x = f2_to_h2(f2mul(x0, wk2));
+          o4[b].y = f2_to_h2(f2mul(x1, wk2));
+          o4[b].z = f2_to_h2(f2mul(x2, wk2));
+          o4[b].w = f2_to_h2(f2mul(x3, wk2));
+        }
+#pragma unroll
+        for (int b = 0; b < 4; ++b) *reinterpret_cast<uint4 *>(kb + off[b]) = o4[b];
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) *reinterpret_cast<uint64_t *>(&sm.npart[krg * DH + kcc * 8 + 2 * e]) = acc[e];
+      fence_proxy_async_smem();
+      if (t == 0) TRACE(7, kk, 1);
+      mbar_arrive(&sm.kready[kk & 1]);
+      return true;
+    };
+
     // P rows of chunk kk (needs SO of every warp: call after a group barrier) and their 1/den
     auto p_form = [&](int kk) -> bool {
       const int s = kk & 1, par = kk & 1;
@@ -523,6 +640,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
         if (t == 0) TRACE(3, kk, 1);
       }
       if (!mbar_wait(&sm.bar_nq[par], (kk >> 1) & 1, err, 23, abort_ptr)) return false;
+      // P of the previous chunk has been read by its P V product (which may run after S of this chunk)
+      if (kk >= 1 && !mbar_wait(&sm.bar_H, (kk - 1) & 1, err, 39, abort_ptr)) return false;
       const Gate &g = sm.g[s];
       const float mrr = g.mr[pr];
       const float *so = SO + pi * 64;
@@ -601,7 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
 
     bool ok = true;
     for (int k = 0; ok && k < NC; ++k) {
-      if (!s_read(k) || !group_sync(&sm.grp[0], gph, err, 20, abort_ptr) || !p_form(k)) ok = false;
+      if (!s_read(k) || !k_pass(k) || !group_sync(&sm.grp[0], gph, err, 20, abort_ptr) || !p_form(k)) ok = false;
     }
     if (!ok) set_abort(sm);
   } else if (warp >= 16) {
@@ -681,10 +800,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
     // ------------------------------------------------------------------ warpgroup 2: state copy
     const int t = threadIdx.x - 256;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    constexpr int KCPR = DH / 8;     // 16-byte chunks per row of k
-    constexpr int KRG = 128 / KCPR;  // rows handled at once (column layout)
-    const int kcc = t % KCPR, krg = t / KCPR;
-    const int kcolb = (kcc >> 3) * 8192, kc8 = kcc & 7;
     uint32_t gph2 = 0;
     for (int c = 0; c < DH; c += 16) {
       uint32_t r[16];
@@ -699,7 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
     bool ok = true;
     for (int k = 0; k < NC; ++k) {
       const int s = k & 1;
-      if (!mbar_wait(&sm.g_full[s], (k >> 1) & 1, err, 31, abort_ptr)) { ok = false; break; }
+      if (!mbar_wait(&sm.g_full[s], (k >> 1) & 1, err, 40, abort_ptr)) { ok = false; break; }
       if (k >= 1 && !mbar_wait(&sm.bar_U, (k - 1) & 1, err, 32, abort_ptr)) { ok = false; break; }
       if (t == 0) TRACE(4, k, 0);
       tc_fence_after();
@@ -759,78 +874,20 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       tc_fence_before();
       if (t == 0) TRACE(4, k, 1);
       mbar_arrive(&sm.cready);
-      // ---- k: n-update partial sums and w_j k_j (frame of T) in fp16 (column layout)
-      if (!mbar_wait(&sm.qk_full, k & 1, err, 36, abort_ptr)) { ok = false; break; }
-      const float alpha = g.alpha;
-      {
-        // rows in batches of four: every load of a batch is issued before its stores
-        uint64_t acc[4] = {0, 0, 0, 0};
-#pragma unroll 1
-        for (int i0 = 0; i0 < 64 / KRG; i0 += 4) {
-          uint4 raw[4];
-          int off[4];
-          float wt[4], wk[4];
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            const int j = krg + KRG * (i0 + b);
-            off[b] = kcolb + j * 128 + ((kc8 ^ (j & 7)) << 4);
-            raw[b] = *reinterpret_cast<const uint4 *>(sRK + off[b]);
-            wt[b] = g.wt[j];
-            wk[b] = g.wk[j];
-          }
-          uint4 o4[4];
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            const uint64_t wt2 = f2pack(wt[b], wt[b]), wk2 = f2pack(wk[b], wk[b]);
-            const uint64_t x0 = bf2_to_f2(raw[b].x), x1 = bf2_to_f2(raw[b].y), x2 = bf2_to_f2(raw[b].z),
-                           x3 = bf2_to_f2(raw[b].w);
-            acc[0] = f2fma(wt2, x0, acc[0]);
-            acc[1] = f2fma(wt2, x1, acc[1]);
-            acc[2] = f2fma(wt2, x2, acc[2]);
-            acc[3] = f2fma(wt2, x3, acc[3]);
-            o4[b].x = f2_to_h2(f2mul(x0, wk2));
-            o4[b].y = f2_to_h2(f2mul(x1, wk2));
-            o4[b].z = f2_to_h2(f2mul(x2, wk2));
-            o4[b].w = f2_to_h2(f2mul(x3, wk2));
-          }
-#pragma unroll
-          for (int b = 0; b < 4; ++b) *reinterpret_cast<uint4 *>(sWK + off[b]) = o4[b];
-        }
-        mbar_arrive(&sm.qk_empty);  // raw k is no longer read here
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          *reinterpret_cast<uint64_t *>(&sm.npart[krg * DH + kcc * 8 + 2 * e]) = acc[e];
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&sm.opready);
-      // ---- n after chunk k: once warpgroup 3 has used n before it (n . q) and every partial is in
-      if (!mbar_wait(&sm.bar_nq[k & 1], (k >> 1) & 1, err, 37, abort_ptr)) { ok = false; break; }
-      if (!group_sync(&sm.grp[1], gph2, err, 38, abort_ptr)) { ok = false; break; }
-      for (int c = t; c < DH; c += 128) {
-        float a = 0.f;
-#pragma unroll
-        for (int gi = 0; gi < KRG; ++gi) a += sm.npart[gi * DH + c];
-        sm.n[c] = alpha * sm.n[c] + a;
-      }
-      if (!group_sync(&sm.grp[1], gph2, err, 39, abort_ptr)) { ok = false; break; }  // partials read
-      mbar_arrive(&sm.n_ready);
     }
-    if (ok && atile == 0) {
-      for (int c = t; c < DH; c += 128) n_last[(size_t)p * D + c0 + c] = sm.n[c];
-      if (rank == 0 && t == 0) m_last[p] = sm.m_fin;
-    }
+    if (ok && atile == 0 && rank == 0 && t == 0) m_last[p] = sm.m_fin;
     if (!ok) set_abort(sm);
     // final state C_last = exp(sigma) T, transposed through shared memory for coalesced stores
     if (ok && !mbar_wait(&sm.bar_U, (NC - 1) & 1, err, 33, abort_ptr)) ok = false;
     if (t == 0) TRACE(4, 511, 1);
     if (ok) {
       // C_last = exp(sigma) T, 32 columns at a time through two swizzled staging tiles
-      // [128 rows x 128 bytes] in the (now unused) raw q/k buffers, stored by TMA
+      // [128 rows x 128 bytes] in the (now unused) q/k stages, stored by TMA
       tc_fence_after();
       const float fr = __expf(sig_last);
 #pragma unroll 1
       for (int c = 0, slab = 0; c < DH; c += 32, ++slab) {
-        uint8_t *tile = sRQ + (slab & 1) * 16384;
+        uint8_t *tile = base + (slab & 1) * 16384;
         if (slab >= 2) {
           if (t == 0) bulk_wait_read<1>();  // the store that used this tile has read it
           if (!group_sync(&sm.grp[1], gph2, err, 34, abort_ptr)) break;
@@ -856,16 +913,36 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       set_abort(sm);
     }
   } else if (warp >= 12) {
-    // ------------------------------------------------------------------ warpgroup 3: v and q operands
+    // ------------------------------------------------------------------ warpgroup 3: n, v and beta q
     const int t = threadIdx.x - 384;
-    constexpr int CPR = DH / 8;  // 16-byte chunks per row
+    constexpr int CPR = DH / 8;      // 16-byte chunks per row
+    constexpr int KRG = 128 / CPR;   // row groups of warpgroup 1's n-update partial sums
     // row layout for q: two threads per row, each half of the row's chunks
     const int qr = t >> 1, qh = t & 1;
-    for (int c = t; c < DH; c += 128) sm.n[c] = n_init ? n_init[(size_t)p * D + c0 + c] : 0.f;
+    for (int c = t; c < DH; c += 128) sm.n[0][c] = n_init ? n_init[(size_t)p * D + c0 + c] : 0.f;
     uint32_t gph = 0;
+    float alpha_prev = 1.f;  // decay of the previous chunk
+    // n after chunk kk (into n[(kk + 1) & 1]): alpha n + the partial sums of the w k pass; each
+    // thread updates columns t and t + 128
+    auto n_update = [&](int kk) -> bool {
+      if (!mbar_wait(&sm.kready[kk & 1], (kk >> 1) & 1, err, 58, abort_ptr)) return false;
+      const float *src = sm.n[kk & 1];
+      float *dst = sm.n[(kk + 1) & 1];
+      for (int c = t; c < DH; c += 128) {
+        float a = 0.f;
+#pragma unroll
+        for (int gi = 0; gi < KRG; ++gi) a += sm.npart[gi * DH + c];
+        dst[c] = alpha_prev * src[c] + a;
+      }
+      mbar_arrive(&sm.npart_free);
+      if (t == 0) TRACE(7, kk, 2);
+      return true;
+    };
     bool ok = group_sync(&sm.grp[2], gph, err, 50, abort_ptr);
     for (int k = 0; ok && k < NC; ++k) {
       const int s = k & 1, par = k & 1;
+      // n entering chunk k (every thread's columns in before any row reads them)
+      if (k >= 1 && (!n_update(k - 1) || !group_sync(&sm.grp[2], gph, err, 59, abort_ptr))) { ok = false; break; }
       if (!mbar_wait(&sm.g_full[s], (k >> 1) & 1, err, 51, abort_ptr)) { ok = false; break; }
       if (!mbar_wait(&sm.v_full[s], (k >> 1) & 1, err, 55, abort_ptr)) { ok = false; break; }
       // v: bf16 -> fp16 (exact), in place
@@ -887,13 +964,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
           }
         }
       }
-      if (!mbar_wait(&sm.qk_full, k & 1, err, 52, abort_ptr)) { ok = false; break; }
-      // beta q is free once the previous chunk's products are done; n after the previous chunk
-      if (k >= 1 && !mbar_wait(&sm.bar_U, (k - 1) & 1, err, 56, abort_ptr)) { ok = false; break; }
-      if (k >= 1 && !mbar_wait(&sm.n_ready, (k - 1) & 1, err, 58, abort_ptr)) { ok = false; break; }
+      // raw q of the stage has landed and the S product has read it
+      if (!mbar_wait(&sm.qk_full[s], (k >> 1) & 1, err, 52, abort_ptr)) { ok = false; break; }
+      if (!mbar_wait(&sm.bar_S[k & 1], (k >> 1) & 1, err, 56, abort_ptr)) { ok = false; break; }
       if (t == 0) TRACE(5, k, 0);
       const Gate &g = sm.g[s];
-      // q: n . q_r over this CTA's columns and beta_r q_r in fp16 (row layout)
+      alpha_prev = g.alpha;
+      uint8_t *const qb = STQ(s);
+      const float *nk = sm.n[k & 1];
+      // q: n . q_r over this CTA's columns and beta_r q_r in fp16 in place (row layout)
       {
         const float bq = g.beta[qr];
         const uint64_t bq2 = f2pack(bq, bq);
@@ -907,9 +986,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
           for (int b = 0; b < 4; ++b) {
             const int ch = qh * (CPR / 2) + i0 + b;  // chunk of the row
             off[b] = (ch >> 3) * 8192 + qr * 128 + (((ch & 7) ^ (qr & 7)) << 4);
-            raw[b] = *reinterpret_cast<const uint4 *>(sRQ + off[b]);
-            na[b] = *reinterpret_cast<const uint4 *>(&sm.n[ch * 8]);
-            nb[b] = *reinterpret_cast<const uint4 *>(&sm.n[ch * 8 + 4]);
+            raw[b] = *reinterpret_cast<const uint4 *>(qb + off[b]);
+            na[b] = *reinterpret_cast<const uint4 *>(&nk[ch * 8]);
+            nb[b] = *reinterpret_cast<const uint4 *>(&nk[ch * 8 + 4]);
           }
           uint4 o4[4];
 #pragma unroll
@@ -926,7 +1005,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
             o4[b].w = f2_to_h2(f2mul(x3, bq2));
           }
 #pragma unroll
-          for (int b = 0; b < 4; ++b) *reinterpret_cast<uint4 *>(sBQ + off[b]) = o4[b];
+          for (int b = 0; b < 4; ++b) *reinterpret_cast<uint4 *>(qb + off[b]) = o4[b];
         }
         float part = f2sum(part2);
         part += __shfl_xor_sync(0xffffffffu, part, 1);
@@ -945,11 +1024,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       }
       if (t == 0) TRACE(5, k, 1);
       mbar_arrive(&sm.bar_nq[par]);
-      mbar_arrive(&sm.qk_empty);  // raw q is no longer read here
       fence_proxy_async_smem();
       if (t == 0) TRACE(5, k, 2);
-      mbar_arrive(&sm.opready);
+      mbar_arrive(&sm.xready[k & 1]);
     }
+    // n after the last chunk
+    if (ok && NC > 0) ok = n_update(NC - 1);
+    if (ok && atile == 0)
+      for (int c = t; c < DH; c += 128) n_last[(size_t)p * D + c0 + c] = sm.n[NC & 1][c];
     if (!ok) set_abort(sm);
   }
 
@@ -961,6 +1043,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
     tc_fence_after();
     tmem_dealloc(tm, 512);
   }
+  if (threadIdx.x == 0) SPAN(1);
 #undef STV
 }
 

@@ -83,17 +83,36 @@ __device__ __forceinline__ bool mbar_poll(uint64_t *bar, uint32_t parity) {
 #endif
   return ok != 0;
 }
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, int code,
-                                          const int *abort = nullptr) {
-  if (mbar_poll(bar, parity)) return true;
+// Non-blocking test of a phase (for loops that watch several barriers at once).
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+#ifndef MLSTM_POLL_HOOK
+#define MLSTM_POLL_HOOK()
+#endif
+static __device__ __forceinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, int *err, int code, const int *abort) {
   const long long t0 = clock64();
   for (;;) {
+    MLSTM_POLL_HOOK();
     if (mbar_poll(bar, parity)) return true;
     if ((abort && *(const volatile int *)abort) || clock64() - t0 > kWaitCycles) {
       if (err) atomicCAS(err, 0, code);
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, int code,
+                                          const int *abort = nullptr) {
+  if (mbar_poll(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, err, code, abort);
 }
 
 // ---------------------------------------------------------------- clusters / distributed smem
@@ -142,14 +161,7 @@ __device__ __forceinline__ bool mbar_poll_cluster(uint64_t *bar, uint32_t parity
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, int *err, int code,
                                                   const int *abort = nullptr) {
   if (mbar_poll_cluster(bar, parity)) return true;
-  const long long t0 = clock64();
-  for (;;) {
-    if (mbar_poll_cluster(bar, parity)) return true;
-    if ((abort && *(const volatile int *)abort) || clock64() - t0 > kWaitCycles) {
-      if (err) atomicCAS(err, 0, code);
-      return false;
-    }
-  }
+  return mbar_wait_slow(bar, parity, err, code, abort);
 }
 
 // ---------------------------------------------------------------- TMA
