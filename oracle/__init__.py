@@ -49,11 +49,11 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     i = ctypes.c_int
     lib.oracle_mlstm_recurrent.restype = i
     lib.oracle_mlstm_recurrent.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, dp, dp, dp,
-                                           dp, dp, dp, dp, dp, dp, dp, i, dp, dp, dp, i]
+                                           dp, dp, dp, dp, dp, dp, dp, i, dp, dp, dp, i, i]
     lib.oracle_mlstm_unstabilised.restype = i
-    lib.oracle_mlstm_unstabilised.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, dp, dp, dp, i]
+    lib.oracle_mlstm_unstabilised.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, dp, dp, dp, i, i]
     lib.oracle_mlstm_parallel.restype = i
-    lib.oracle_mlstm_parallel.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, dp, i]
+    lib.oracle_mlstm_parallel.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, dp, i, i]
     return lib
 
 
@@ -89,9 +89,21 @@ def _shapes(q, k, v, ig, fg):
     return B, NH, S, DQK, v.shape[3]
 
 
+FORGET_GATES = ("sigmoid", "exp")
+
+
+def _forget(forget):
+    if forget not in FORGET_GATES:
+        raise ValueError(f"forget gate must be one of {FORGET_GATES}")
+    return int(forget == "exp")
+
+
 def recurrent(q, k, v, ig, fg, C0=None, n0=None, m0=None, snap_every=0, want_h=True,
-              want_m_tok=False, want_den=False, nthreads=0, lib=None):
+              want_m_tok=False, want_den=False, nthreads=0, lib=None, forget="sigmoid"):
     """Stabilised step-by-step mLSTM in fp64.
+
+    ``forget`` selects the forget gate: "sigmoid" (f = sigmoid(f~), log f = log sigmoid(f~))
+    or "exp" (f = exp(f~), log f = f~).
 
     Returns a dict with ``h`` [B,NH,S,DV] (unless want_h is False), the final state ``C``
     [B,NH,DV,DQK], ``n`` [B,NH,DQK], ``m`` [B,NH]; ``m_tok`` [B,NH,S] if asked; and, when
@@ -129,14 +141,14 @@ def recurrent(q, k, v, ig, fg, C0=None, n0=None, m0=None, snap_every=0, want_h=T
         _ptr(C0), _ptr(n0), _ptr(m0), _ptr(out.get("h")), _ptr(out["C"]), _ptr(out["n"]),
         _ptr(out["m"]), _ptr(out.get("m_tok")), _ptr(out.get("den_tok")),
         _ptr(out.get("dabs_tok")), int(snap_every), _ptr(out.get("C_snap")),
-        _ptr(out.get("n_snap")), _ptr(out.get("m_snap")), int(nthreads))
+        _ptr(out.get("n_snap")), _ptr(out.get("m_snap")), int(nthreads), _forget(forget))
     if rc != 0:
         raise ValueError(f"oracle_mlstm_recurrent rejected its arguments (code {rc})")
     return out
 
 
-def unstabilised(q, k, v, ig, fg, nthreads=0, lib=None):
-    """Unstabilised recurrent mLSTM (f = sigmoid, i = exp, floor 1) in fp64."""
+def unstabilised(q, k, v, ig, fg, nthreads=0, lib=None, forget="sigmoid"):
+    """Unstabilised recurrent mLSTM (f = sigmoid or exp, i = exp, floor 1) in fp64."""
     lib = lib or load()
     q, k, v, ig, fg = (_f64(x) for x in (q, k, v, ig, fg))
     B, NH, S, DQK, DV = _shapes(q, k, v, ig, fg)
@@ -144,20 +156,20 @@ def unstabilised(q, k, v, ig, fg, nthreads=0, lib=None):
            "n": np.empty((B, NH, DQK))}
     rc = lib.oracle_mlstm_unstabilised(_ptr(q), _ptr(k), _ptr(v), _ptr(ig), _ptr(fg), B, NH, S,
                                        DQK, DV, _ptr(out["h"]), _ptr(out["C"]), _ptr(out["n"]),
-                                       int(nthreads))
+                                       int(nthreads), _forget(forget))
     if rc != 0:
         raise ValueError(f"oracle_mlstm_unstabilised rejected its arguments (code {rc})")
     return out
 
 
-def parallel(q, k, v, ig, fg, nthreads=0, lib=None):
+def parallel(q, k, v, ig, fg, nthreads=0, lib=None, forget="sigmoid"):
     """Fully parallel quadratic (dual) form from the zero state, fp64, O(S^2) per head."""
     lib = lib or load()
     q, k, v, ig, fg = (_f64(x) for x in (q, k, v, ig, fg))
     B, NH, S, DQK, DV = _shapes(q, k, v, ig, fg)
     h = np.empty((B, NH, S, DV))
     rc = lib.oracle_mlstm_parallel(_ptr(q), _ptr(k), _ptr(v), _ptr(ig), _ptr(fg), B, NH, S, DQK,
-                                   DV, _ptr(h), int(nthreads))
+                                   DV, _ptr(h), int(nthreads), _forget(forget))
     if rc != 0:
         raise ValueError(f"oracle_mlstm_parallel rejected its arguments (code {rc})")
     return h

@@ -14,8 +14,11 @@
  * "The Parallel Dual Form" (unrolled C_T, causal decay matrix S, H = ((Q K^T) o S) V).
  *
  * Readings taken where the page leaves a step open (each also listed in the design notes):
- *  - the forget gate is the sigmoid variant, used in log space: log f_t = log sigmoid(f~_t);
- *    the stabiliser of section 2 is carried over with f~_t replaced by log f_t;
+ *  - the forget gate is the sigmoid variant by default, used in log space:
+ *    log f_t = log sigmoid(f~_t); the stabiliser of section 2 is carried over with f~_t
+ *    replaced by log f_t.  The exponential variant (section 2 allows "exp or sigmoid" for f)
+ *    is selected per call: f_t = exp(f~_t), so log f_t = f~_t and section 2's stabiliser
+ *    applies exactly as printed;
  *  - the retrieval denominator is max(|n_t^T q_t|, exp(-m_t)) on stabilised states,
  *    which equals section 3's max(n^T q, 1) with an absolute value on unstabilised ones;
  *  - "d" in 1/sqrt(d) is the query/key head dimension d_qk; C_t is d_v x d_qk with
@@ -42,6 +45,7 @@ typedef struct {
   double *C_snap, *n_snap, *m_snap;
   int B, NH, S, DQK, DV, snap_every;
   int kind; /* 0 = stabilised recurrent, 1 = unstabilised recurrent, 2 = parallel dual form */
+  int exp_forget; /* 0: f_t = sigmoid(f~_t); 1: f_t = exp(f~_t) */
   int next_pair;
   pthread_mutex_t lock;
 } job_t;
@@ -53,6 +57,10 @@ static double log_sigmoid(double x) {
 }
 
 static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* log f_t and f_t of the selected forget-gate variant */
+static double log_forget(const job_t *J, double x) { return J->exp_forget ? x : log_sigmoid(x); }
+static double forget(const job_t *J, double x) { return J->exp_forget ? exp(x) : sigmoid(x); }
 
 /* Section 2 stabiliser + section 3 matrix memory, one (batch, head) pair, token by token. */
 static void recurrent_pair(const job_t *J, int pair) {
@@ -95,13 +103,13 @@ static void recurrent_pair(const job_t *J, int pair) {
     double fgate, igate; /* the multipliers applied to (C, n) and to the new v k^T */
     if (J->kind == 0) {
       /* log-space stabiliser: m_t = max(log f_t + m_{t-1}, i~_t) */
-      const double logf = log_sigmoid(fg[t]);
+      const double logf = log_forget(J, fg[t]);
       const double m_new = fmax(logf + m, ig[t]);
       fgate = exp(logf + m - m_new); /* exp(log f_t + m_{t-1} - m_t) */
       igate = exp(ig[t] - m_new);    /* exp(i~_t - m_t) */
       m = m_new;
     } else {
-      fgate = sigmoid(fg[t]); /* f_t = sigmoid(f~_t) */
+      fgate = forget(J, fg[t]); /* f_t = sigmoid(f~_t) or exp(f~_t) */
       igate = exp(ig[t]);     /* i_t = exp(i~_t) */
     }
 
@@ -166,7 +174,7 @@ static void parallel_pair(const job_t *J, int pair) {
     for (int a = 0; a < DV; ++a) num[a] = 0.0;
     for (int j = 0; j <= t; ++j) {
       double Stj = exp(ig[j]); /* i_j */
-      for (int tau = j + 1; tau <= t; ++tau) Stj *= sigmoid(fg[tau]);
+      for (int tau = j + 1; tau <= t; ++tau) Stj *= forget(J, fg[tau]);
       double qk = 0.0;
       for (int c = 0; c < DQK; ++c) qk += q[(size_t)t * DQK + c] * (k[(size_t)j * DQK + c] * scale);
       den += Stj * qk;
@@ -216,13 +224,14 @@ static int run(job_t *J, int nthreads) {
  * the denominator sums, so dabs / max(|den|, exp(-m)) is its condition number.
  * If snap_every > 0 (must divide S), C_snap [B,NH,S/snap_every+1,DV,DQK], n_snap and
  * m_snap receive the state at t = 0, snap_every, 2*snap_every, ..., S.
+ * exp_forget selects f_t = exp(f~_t) instead of sigmoid(f~_t) (likewise in the routines below).
  * Returns 0 on success, nonzero on a bad argument.  nthreads <= 0 uses every core. */
 int oracle_mlstm_recurrent(const double *q, const double *k, const double *v, const double *ig,
                            const double *fg, int B, int NH, int S, int DQK, int DV,
                            const double *C0, const double *n0, const double *m0, double *h,
                            double *C_out, double *n_out, double *m_out, double *m_tok,
                            double *den_tok, double *dabs_tok, int snap_every, double *C_snap,
-                           double *n_snap, double *m_snap, int nthreads) {
+                           double *n_snap, double *m_snap, int nthreads, int exp_forget) {
   job_t J;
   memset(&J, 0, sizeof(J));
   J.q = q; J.k = k; J.v = v; J.ig = ig; J.fg = fg;
@@ -232,32 +241,36 @@ int oracle_mlstm_recurrent(const double *q, const double *k, const double *v, co
   J.C_snap = C_snap; J.n_snap = n_snap; J.m_snap = m_snap;
   J.B = B; J.NH = NH; J.S = S; J.DQK = DQK; J.DV = DV; J.snap_every = snap_every;
   J.kind = 0;
+  J.exp_forget = exp_forget != 0;
   return run(&J, nthreads);
 }
 
-/* Unstabilised recurrent mLSTM: f_t = sigmoid(f~_t), i_t = exp(i~_t), floor 1.
+/* Unstabilised recurrent mLSTM: f_t = sigmoid(f~_t) (or exp(f~_t)), i_t = exp(i~_t), floor 1.
  * Overflows for large gate sums: use only where exp() stays finite. */
 int oracle_mlstm_unstabilised(const double *q, const double *k, const double *v,
                               const double *ig, const double *fg, int B, int NH, int S, int DQK,
-                              int DV, double *h, double *C_out, double *n_out, int nthreads) {
+                              int DV, double *h, double *C_out, double *n_out, int nthreads,
+                              int exp_forget) {
   job_t J;
   memset(&J, 0, sizeof(J));
   J.q = q; J.k = k; J.v = v; J.ig = ig; J.fg = fg;
   J.h = h; J.C_out = C_out; J.n_out = n_out;
   J.B = B; J.NH = NH; J.S = S; J.DQK = DQK; J.DV = DV;
   J.kind = 1;
+  J.exp_forget = exp_forget != 0;
   return run(&J, nthreads);
 }
 
 /* Fully parallel quadratic (dual) form from the zero state, O(S^2) per head. */
 int oracle_mlstm_parallel(const double *q, const double *k, const double *v, const double *ig,
                           const double *fg, int B, int NH, int S, int DQK, int DV, double *h,
-                          int nthreads) {
+                          int nthreads, int exp_forget) {
   job_t J;
   memset(&J, 0, sizeof(J));
   J.q = q; J.k = k; J.v = v; J.ig = ig; J.fg = fg;
   J.h = h;
   J.B = B; J.NH = NH; J.S = S; J.DQK = DQK; J.DV = DV;
   J.kind = 2;
+  J.exp_forget = exp_forget != 0;
   return run(&J, nthreads);
 }

@@ -236,6 +236,75 @@ def pin_denominator_brute_force(lib):
     return err <= 1e-13, f"denominator brute force err {err:.3e}"
 
 
+# ---------------------------------------------------------------- exponential forget gate
+# Section 2 allows f = exp(f~) as well as sigmoid(f~); then log f = f~ and the stabiliser is
+# the printed m_t = max(f~_t + m_{t-1}, i~_t).
+def pin_exp_forget_is_a_rescaling(lib):
+    """Exponential forget gate: stabilised h == unstabilised h (f = exp(f~), i = exp(i~),
+    floor 1), C_stab e^m == C_unstab, n likewise.  f~ around -0.1 keeps the unstabilised
+    products finite; i~ spread keeps the stabiliser moving."""
+    worst = 0.0
+    for seed in (21, 22):
+        q, k, v, ig, fg = rand_inputs(2, 2, 40, 6, 5, seed, ig=(0.0, 1.5), fg=(-0.1, 0.2))
+        st = oracle.recurrent(q, k, v, ig, fg, lib=lib, forget="exp")
+        un = oracle.unstabilised(q, k, v, ig, fg, lib=lib, forget="exp")
+        e = np.exp(st["m"])
+        worst = max(worst, rel(st["h"], un["h"]), rel(st["C"] * e[..., None, None], un["C"]),
+                    rel(st["n"] * e[..., None], un["n"]))
+    return worst <= 1e-11, f"exp forget: stabilised vs unstabilised rel err {worst:.3e}"
+
+
+def pin_exp_forget_dual_form(lib):
+    """Exponential forget gate: recurrent == parallel dual form with S_tj = prod exp(f~) i_j."""
+    worst = 0.0
+    for seed in (23, 24):
+        q, k, v, ig, fg = rand_inputs(1, 2, 18, 6, 5, seed, fg=(-0.2, 0.3))
+        worst = max(worst, rel(oracle.recurrent(q, k, v, ig, fg, lib=lib, forget="exp")["h"],
+                               oracle.parallel(q, k, v, ig, fg, lib=lib, forget="exp")))
+    return worst <= 1e-11, f"exp forget: recurrent vs parallel rel err {worst:.3e}"
+
+
+def pin_exp_forget_equals_sigmoid_in_log_space(lib):
+    """The two variants differ only in log f: the exponential gate fed f~' = log sigmoid(f~)
+    (computed by numpy's logaddexp) gives the sigmoid gate's outputs at f~, state included."""
+    q, k, v, ig, fg = rand_inputs(2, 2, 30, 5, 4, 25, ig=(0.0, 2.0), fg=(1.0, 2.0))
+    a = oracle.recurrent(q, k, v, ig, fg, lib=lib)
+    b = oracle.recurrent(q, k, v, ig, log_sigmoid_np(fg), lib=lib, forget="exp")
+    err = max(rel(b["h"], a["h"]), rel(b["C"], a["C"]), rel(b["n"], a["n"]),
+              float(np.max(np.abs(b["m"] - a["m"]))))
+    # and the variants are not the same map: the exponential gate at f~ itself differs
+    c = oracle.recurrent(q, k, v, ig, fg, lib=lib, forget="exp")
+    differs = rel(c["h"], a["h"]) > 1e-3
+    return err <= 1e-12 and differs, f"exp(log sigmoid) vs sigmoid err {err:.3e}, distinct {differs}"
+
+
+def pin_exp_forget_two_token_scalar(lib):
+    """d_qk = d_v = 1, two tokens, written out by hand: C_1 = i_1 v_1 k_1, n_1 = i_1 k_1,
+    C_2 = f_2 C_1 + i_2 v_2 k_2, n_2 = f_2 n_1 + i_2 k_2 with f_2 = e^{f~_2}, i_t = e^{i~_t};
+    h_t = C_t q_t / max(|n_t q_t|, 1); m_1 = max(f~_1, i~_1), m_2 = max(f~_2 + m_1, i~_2).
+    Cases cover both sides of the max in the denominator and in the stabiliser."""
+    worst = 0.0
+    cases = [((0.7, -1.3), (1.5, 0.4), (-0.8, 2.0), (0.3, -0.2), (-0.5, 0.6)),
+             ((2.0, 0.5), (-1.0, 3.0), (0.9, -0.4), (1.2, -2.5), (0.1, -1.7)),
+             ((-0.3, 1.1), (0.6, 0.8), (1.4, 1.9), (-1.5, 0.2), (2.2, 0.05))]
+    for qq, kk, vv, ii, ff in cases:
+        q = np.array(qq).reshape(1, 1, 2, 1); k = np.array(kk).reshape(1, 1, 2, 1)
+        v = np.array(vv).reshape(1, 1, 2, 1)
+        ig = np.array(ii).reshape(1, 1, 2); fg = np.array(ff).reshape(1, 1, 2)
+        i1, i2 = np.exp(ii[0]), np.exp(ii[1])
+        f2 = np.exp(ff[1])
+        C1, n1 = i1 * vv[0] * kk[0], i1 * kk[0]
+        C2, n2 = f2 * C1 + i2 * vv[1] * kk[1], f2 * n1 + i2 * kk[1]
+        h1 = C1 * qq[0] / max(abs(n1 * qq[0]), 1.0)
+        h2 = C2 * qq[1] / max(abs(n2 * qq[1]), 1.0)
+        m1 = max(ff[0], ii[0]); m2 = max(ff[1] + m1, ii[1])
+        out = oracle.recurrent(q, k, v, ig, fg, lib=lib, forget="exp")
+        worst = max(worst, rel(out["h"].ravel(), np.array([h1, h2])),
+                    abs(float(out["m"].ravel()[0]) - m2),
+                    rel(out["C"].ravel() * np.exp(m2), np.array([C2])))
+    return worst <= 1e-13, f"exp forget two-token closed form err {worst:.3e}"
+
+
 ALL_PINS = [
     pin_recurrent_equals_parallel,
     pin_stabiliser_is_a_rescaling,
@@ -248,6 +317,10 @@ ALL_PINS = [
     pin_snapshots,
     pin_causality_and_linearity,
     pin_denominator_brute_force,
+    pin_exp_forget_is_a_rescaling,
+    pin_exp_forget_dual_form,
+    pin_exp_forget_equals_sigmoid_in_log_space,
+    pin_exp_forget_two_token_scalar,
 ]
 
 

@@ -25,7 +25,10 @@ MUTANTS = [
     ("forget factor drops m_{t-1}", "fgate = exp(logf + m - m_new);", "fgate = exp(logf - m_new);"),
     ("input factor uses old m", "igate = exp(ig[t] - m_new);", "igate = exp(ig[t] - m);"),
     ("log-sigmoid sign", "if (x >= 0.0) return -log1p(exp(-x));", "if (x >= 0.0) return -log1p(exp(x));"),
-    ("forget gate exp instead of sigmoid", "fgate = sigmoid(fg[t]); /* f_t = sigmoid(f~_t) */", "fgate = exp(fg[t]);"),
+    ("forget gate exp instead of sigmoid", "return J->exp_forget ? exp(x) : sigmoid(x);", "return exp(x);"),
+    ("log forget ignores the variant", "return J->exp_forget ? x : log_sigmoid(x);", "return log_sigmoid(x);"),
+    ("log forget always raw", "return J->exp_forget ? x : log_sigmoid(x);", "return x;"),
+    ("exp forget gate as sigmoid", "return J->exp_forget ? exp(x) : sigmoid(x);", "return sigmoid(x);"),
     ("key scale 1/d", "1.0 / sqrt((double)DQK); /* k_t", "1.0 / ((double)DQK); /* k_t"),
     ("transposed outer product", "igate * vt[a] * khat[c]", "igate * vt[c % DV] * khat[a % DQK]"),
     ("normaliser with unscaled key", "n[c] = fgate * n[c] + igate * khat[c];", "n[c] = fgate * n[c] + igate * kt[c];"),
