@@ -8,7 +8,8 @@
  *       h_t = C_t q_t / max(|n_t^T q_t|, exp(-m_t))          (stabilised form);
  *   section 2 "The Normalizer State and Numerical Stabilization": the log-space max
  *       stabiliser m_t = max(log f_t + m_{t-1}, i~_t), with i_t = exp(i~_t) and the
- *       sigmoid forget gate used in log space, log f_t = log sigmoid(f~_t);
+ *       sigmoid forget gate used in log space, log f_t = log sigmoid(f~_t) (or, with
+ *       MLSTM_FORGET_EXP, the exponential gate: log f_t = f~_t);
  *   section 3 "The Parallel Dual Form" and section 5 (chunkwise scans): the forward is
  *       computed chunk by chunk -- the quadratic form inside each chunk, the recurrent
  *       state (C, n, m) passed across chunks;
@@ -54,7 +55,15 @@ typedef enum {
   MLSTM_ERR_DEVICE = 8     /* no usable device, or the device is not sm_103 */
 } mlstm_status;
 
-typedef enum { MLSTM_F32 = 0, MLSTM_BF16 = 1 } mlstm_dtype;
+/* Element type of q, k, v (and of h in h_dt).  The calls that read raw gate pre-activations
+ * (mlstm_fwd_chunkwise, mlstm_fwd_chunkwise_noalloc, mlstm_fwd_chunk_states, mlstm_step,
+ * mlstm_step_multi) also take MLSTM_FORGET_EXP OR-ed into `dt`: the forget gate is then the
+ * exponential variant f_t = exp(f~_t), log f_t = f~_t (section 2 of the page allows "exp or
+ * sigmoid"; the default is sigmoid).  The sizing and path queries accept and ignore it;
+ * mlstm_fwd_from_gates uses whatever variant filled its workspace; mlstm_fwd_gates (which
+ * has no dtype argument) is the sigmoid variant only.  In C++ the combined value needs a
+ * cast: (mlstm_dtype)(MLSTM_BF16 | MLSTM_FORGET_EXP). */
+typedef enum { MLSTM_F32 = 0, MLSTM_BF16 = 1, MLSTM_FORGET_EXP = 0x100 } mlstm_dtype;
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *mlstm_status_str(mlstm_status s);

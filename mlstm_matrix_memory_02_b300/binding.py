@@ -69,6 +69,17 @@ EXPORTED = ["mlstm_status_str", "mlstm_last_cuda_error", "mlstm_kernel_launches"
 # Bytes of the fixed scratch array behind mlstm_fwd_chunkwise_noalloc (include/mlstm.h).
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
+# Forget-gate variants: "sigmoid" (f = sigmoid(f~), the default) or "exp" (f = exp(f~)); the
+# variant is passed to the library OR-ed into the dtype code.
+FORGET_EXP = 0x100
+FORGET_GATES = ("sigmoid", "exp")
+
+
+def _dt_code(dtype, forget="sigmoid"):
+    if forget not in FORGET_GATES:
+        raise ValueError(f"forget must be one of {FORGET_GATES}")
+    return _DT[dtype] | (FORGET_EXP if forget == "exp" else 0)
+
 
 class MlstmError(RuntimeError):
     def __init__(self, code: int, where: str):
@@ -128,9 +139,11 @@ def alloc_workspace(B, NH, S, DQK, DV, chunk, dtype=torch.bfloat16, device=None)
 
 
 def mlstm_fwd_chunkwise(q, k, v, igate_pre, fgate_pre, chunk, h_dtype=None, C_init=None,
-                        n_init=None, m_init=None, out=None, workspace=None, stream=None):
+                        n_init=None, m_init=None, out=None, workspace=None, stream=None,
+                        forget="sigmoid"):
     """Chunkwise forward.  q, k [B,NH,S,DQK], v [B,NH,S,DV] (fp32 or bf16), gates [B,NH,S]
-    fp32.  Returns (h, C_last, n_last, m_last); ``out`` may supply those four tensors."""
+    fp32.  Returns (h, C_last, n_last, m_last); ``out`` may supply those four tensors.
+    ``forget`` is the forget-gate variant ("sigmoid" or "exp")."""
     B, NH, S, DQK = q.shape
     DV = v.shape[-1]
     dt = q.dtype
@@ -162,13 +175,13 @@ def mlstm_fwd_chunkwise(q, k, v, igate_pre, fgate_pre, chunk, h_dtype=None, C_in
         workspace = alloc_workspace(B, NH, S, DQK, DV, chunk, dt, q.device)
     code = _lib.mlstm_fwd_chunkwise(
         _ptr(q), _ptr(k), _ptr(v), _ptr(igate_pre), _ptr(fgate_pre), B, NH, S, DQK, DV, chunk,
-        _DT[dt], _ptr(C_init), _ptr(n_init), _ptr(m_init), _ptr(h), _DT[h_dtype], _ptr(C_last),
-        _ptr(n_last), _ptr(m_last), _ptr(workspace), workspace.numel(), _stream(stream))
+        _dt_code(dt, forget), _ptr(C_init), _ptr(n_init), _ptr(m_init), _ptr(h), _DT[h_dtype],
+        _ptr(C_last), _ptr(n_last), _ptr(m_last), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(code, "mlstm_fwd_chunkwise")
     return h, C_last, n_last, m_last
 
 
-def mlstm_step_multi(q, k, v, ig, fg, C, n, m, h=None, h_dtype=None, stream=None):
+def mlstm_step_multi(q, k, v, ig, fg, C, n, m, h=None, h_dtype=None, stream=None, forget="sigmoid"):
     """T consecutive decode steps in one launch, in place on (C, n, m).  q, k [B,NH,T,DQK],
     v [B,NH,T,DV], ig, fg [B,NH,T]; returns h [B,NH,T,DV]."""
     B, NH, T, DQK = q.shape
@@ -187,14 +200,14 @@ def mlstm_step_multi(q, k, v, ig, fg, C, n, m, h=None, h_dtype=None, stream=None
         h = torch.empty((B, NH, T, DV), dtype=h_dtype, device=q.device)
     _dev(h, "h", h_dtype, (B, NH, T, DV))
     code = _lib.mlstm_step_multi(_ptr(q), _ptr(k), _ptr(v), _ptr(ig), _ptr(fg), _ptr(C), _ptr(n),
-                                 _ptr(m), _ptr(h), B, NH, T, DQK, DV, _DT[dt], _DT[h_dtype],
-                                 _stream(stream))
+                                 _ptr(m), _ptr(h), B, NH, T, DQK, DV, _dt_code(dt, forget),
+                                 _DT[h_dtype], _stream(stream))
     _check(code, "mlstm_step_multi")
     return h
 
 
 def mlstm_fwd_chunkwise_noalloc(q, k, v, igate_pre, fgate_pre, chunk, out, C_init=None, n_init=None,
-                                m_init=None, stream=None):
+                                m_init=None, stream=None, forget="sigmoid"):
     """The chunkwise forward without any device allocation, for callers that cannot allocate
     (a host application that owns all device memory, a serving loop where cudaMalloc could
     synchronise the device): the library uses its own fixed scratch array.  The four outputs
@@ -223,8 +236,8 @@ def mlstm_fwd_chunkwise_noalloc(q, k, v, igate_pre, fgate_pre, chunk, out, C_ini
     _dev(m_last, "m_last", torch.float32, (B, NH))
     code = _lib.mlstm_fwd_chunkwise_noalloc(
         _ptr(q), _ptr(k), _ptr(v), _ptr(igate_pre), _ptr(fgate_pre), B, NH, S, DQK, DV, chunk,
-        _DT[dt], _ptr(C_init), _ptr(n_init), _ptr(m_init), _ptr(h), _DT[h.dtype], _ptr(C_last),
-        _ptr(n_last), _ptr(m_last), _stream(stream))
+        _dt_code(dt, forget), _ptr(C_init), _ptr(n_init), _ptr(m_init), _ptr(h), _DT[h.dtype],
+        _ptr(C_last), _ptr(n_last), _ptr(m_last), _stream(stream))
     _check(code, "mlstm_fwd_chunkwise_noalloc")
     return h, C_last, n_last, m_last
 
@@ -257,7 +270,7 @@ def mlstm_fwd_from_gates(q, k, v, chunk, workspace, out, C_init=None, n_init=Non
 
 
 def mlstm_fwd_chunk_states(k, v, igate_pre, fgate_pre, chunk, C_init=None, n_init=None,
-                           m_init=None, workspace=None, stream=None):
+                           m_init=None, workspace=None, stream=None, forget="sigmoid"):
     """Boundary states after every chunk: (C_states [B,NH,NC+1,DV,DQK], n_states
     [B,NH,NC+1,DQK], m_states [B,NH,NC+1])."""
     B, NH, S, DQK = k.shape
@@ -274,8 +287,9 @@ def mlstm_fwd_chunk_states(k, v, igate_pre, fgate_pre, chunk, C_init=None, n_ini
     if workspace is None:
         workspace = alloc_workspace(B, NH, S, DQK, DV, chunk, dt, k.device)
     code = _lib.mlstm_fwd_chunk_states(
-        _ptr(k), _ptr(v), _ptr(igate_pre), _ptr(fgate_pre), B, NH, S, DQK, DV, chunk, _DT[dt],
-        _ptr(C_init), _ptr(n_init), _ptr(m_init), _ptr(Cs), _ptr(ns), _ptr(ms), _ptr(workspace),
+        _ptr(k), _ptr(v), _ptr(igate_pre), _ptr(fgate_pre), B, NH, S, DQK, DV, chunk,
+        _dt_code(dt, forget), _ptr(C_init), _ptr(n_init), _ptr(m_init), _ptr(Cs), _ptr(ns), _ptr(ms),
+        _ptr(workspace),
         workspace.numel(), _stream(stream))
     _check(code, "mlstm_fwd_chunk_states")
     return Cs, ns, ms
@@ -310,7 +324,7 @@ def mlstm_fwd_check(workspace, B, NH, S, DQK, DV, chunk, dtype=torch.bfloat16, s
     _check(code, "mlstm_fwd_check")
 
 
-def mlstm_step(q, k, v, ig, fg, C, n, m, h=None, h_dtype=None, stream=None):
+def mlstm_step(q, k, v, ig, fg, C, n, m, h=None, h_dtype=None, stream=None, forget="sigmoid"):
     """One decode step, in place on (C, n, m).  q, k [B,NH,DQK], v [B,NH,DV]; returns h."""
     B, NH, DQK = q.shape
     DV = v.shape[-1]
@@ -328,7 +342,7 @@ def mlstm_step(q, k, v, ig, fg, C, n, m, h=None, h_dtype=None, stream=None):
         h = torch.empty((B, NH, DV), dtype=h_dtype, device=q.device)
     _dev(h, "h", h_dtype, (B, NH, DV))
     code = _lib.mlstm_step(_ptr(q), _ptr(k), _ptr(v), _ptr(ig), _ptr(fg), _ptr(C), _ptr(n),
-                           _ptr(m), _ptr(h), B, NH, DQK, DV, _DT[dt], _DT[h_dtype],
+                           _ptr(m), _ptr(h), B, NH, DQK, DV, _dt_code(dt, forget), _DT[h_dtype],
                            _stream(stream))
     _check(code, "mlstm_step")
     return h

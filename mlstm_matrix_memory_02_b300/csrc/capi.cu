@@ -69,6 +69,13 @@ Layout layout(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) 
 
 inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+// The forget-gate variant rides in the dtype argument of the calls that read raw gate
+// pre-activations: MLSTM_FORGET_EXP OR-ed into dt selects f = exp(f~) (log f = f~).
+inline mlstm_dtype split_forget(mlstm_dtype dt, bool &exp_fg) {
+  exp_fg = ((int)dt & (int)MLSTM_FORGET_EXP) != 0;
+  return (mlstm_dtype)((int)dt & ~(int)MLSTM_FORGET_EXP);
+}
+
 thread_local int g_last_cuda_error = 0;
 unsigned long long g_launches = 0;  // kernels launched by this library (all host threads)
 
@@ -121,6 +128,8 @@ int mlstm_last_cuda_error(void) { return g_last_cuda_error; }
 unsigned long long mlstm_kernel_launches(void) { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
 
 int mlstm_fwd_path(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) {
+  bool exp_fg;
+  dt = split_forget(dt, exp_fg);
   if (dt != MLSTM_F32 && dt != MLSTM_BF16) return -1;
   if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return -1;
   if (!use_tc(B, NH, S, DQK, DV, chunk, dt)) return 0;
@@ -128,6 +137,8 @@ int mlstm_fwd_path(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype
 }
 
 size_t mlstm_fwd_workspace_bytes(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) {
+  bool exp_fg;
+  dt = split_forget(dt, exp_fg);
   if (dt != MLSTM_F32 && dt != MLSTM_BF16) return 0;
   if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return 0;
   return layout(B, NH, S, DQK, DV, chunk, dt).total;
@@ -167,7 +178,7 @@ static mlstm_status run_from_gates(const void *q, const void *k, const void *v, 
                                    const float *n_init, void *h, mlstm_dtype h_dt, float *C_last,
                                    float *n_last, float *m_last, void *workspace, cudaStream_t s,
                                    const float *ig = nullptr, const float *fg = nullptr,
-                                   const float *m_init = nullptr) {
+                                   const float *m_init = nullptr, bool exp_fg = false) {
   const Layout Lw = layout(B, NH, S, DQK, DV, chunk, dt);
   char *ws = (char *)workspace;
   float *gb = (float *)(ws + Lw.gb), *gx = (float *)(ws + Lw.gx), *gu = (float *)(ws + Lw.gu);
@@ -183,7 +194,7 @@ static mlstm_status run_from_gates(const void *q, const void *k, const void *v, 
       n_init = ncopy;
     }
     return launch_status(launch_fwd_tc(q, k, v, h_dt == MLSTM_BF16, gb, gx, gu, cm, ig, fg, m_init, P, S, DQK,
-                                       DV, C_init, n_init, h, C_last, n_last, m_last, err, s));
+                                       DV, C_init, n_init, h, C_last, n_last, m_last, err, s, exp_fg));
   }
   if (mlstm_status st = launch_status(launch_states_simt(k, v, bf16, gb, gx, cm, P, S, chunk, DQK, DV, C_init,
                                                          n_init, Cs, ns, C_last, n_last, s)))
@@ -201,6 +212,8 @@ mlstm_status mlstm_fwd_from_gates(const void *q, const void *k, const void *v, i
                                   const float *n_init, void *h, mlstm_dtype h_dt, float *C_last,
                                   float *n_last, float *m_last, void *workspace, size_t ws_bytes,
                                   void *stream) {
+  bool exp_fg;  // the variant is that of the gates already in the workspace
+  dt = split_forget(dt, exp_fg);
   if (mlstm_status st = check_fwd_args(q, k, v, B, NH, S, DQK, DV, chunk, dt, C_init, n_init, h, h_dt,
                                        C_last, n_last, m_last, workspace, ws_bytes))
     return st;
@@ -215,6 +228,8 @@ mlstm_status mlstm_fwd_chunkwise(const void *q, const void *k, const void *v, co
                                  const float *m_init, void *h, mlstm_dtype h_dt, float *C_last,
                                  float *n_last, float *m_last, void *workspace, size_t ws_bytes,
                                  void *stream) {
+  bool exp_fg;
+  dt = split_forget(dt, exp_fg);
   if (mlstm_status st = check_fwd_args(q, k, v, B, NH, S, DQK, DV, chunk, dt, C_init, n_init, h, h_dt,
                                        C_last, n_last, m_last, workspace, ws_bytes))
     return st;
@@ -229,10 +244,10 @@ mlstm_status mlstm_fwd_chunkwise(const void *q, const void *k, const void *v, co
   const int P = B * NH;
   if (Lw.tc)  // the fused kernel preprocesses the gates itself
     return run_from_gates(q, k, v, B, NH, S, DQK, DV, chunk, dt, C_init, n_init, h, h_dt, C_last, n_last,
-                          m_last, workspace, s, igate_pre, fgate_pre, m_init);
+                          m_last, workspace, s, igate_pre, fgate_pre, m_init, exp_fg);
   if (mlstm_status st = launch_status(launch_gates(igate_pre, fgate_pre, P, S, chunk, m_init, (float *)(ws + Lw.gb),
                                                    (float *)(ws + Lw.gx), (float *)(ws + Lw.gu),
-                                                   (float *)(ws + Lw.cm), nullptr, s)))
+                                                   (float *)(ws + Lw.cm), nullptr, s, exp_fg)))
     return st;
   return run_from_gates(q, k, v, B, NH, S, DQK, DV, chunk, dt, C_init, n_init, h, h_dt, C_last, n_last,
                         m_last, workspace, s);
@@ -243,6 +258,8 @@ mlstm_status mlstm_fwd_chunk_states(const void *k, const void *v, const float *i
                                     int chunk, mlstm_dtype dt, const float *C_init, const float *n_init,
                                     const float *m_init, float *C_states, float *n_states,
                                     float *m_states, void *workspace, size_t ws_bytes, void *stream) {
+  bool exp_fg;
+  dt = split_forget(dt, exp_fg);
   if (dt != MLSTM_F32 && dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
   if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return MLSTM_ERR_SHAPE;
   if (S > 0 && (!k || !v || !igate_pre || !fgate_pre)) return MLSTM_ERR_NULL;
@@ -261,7 +278,8 @@ mlstm_status mlstm_fwd_chunk_states(const void *k, const void *v, const float *i
   float *gb = (float *)(ws + Lw.gb), *gx = (float *)(ws + Lw.gx), *gu = (float *)(ws + Lw.gu);
   float *cm = (float *)(ws + Lw.cm);
   const int P = B * NH, NC = S / chunk;
-  if (mlstm_status st = launch_status(launch_gates(igate_pre, fgate_pre, P, S, chunk, m_init, gb, gx, gu, cm, nullptr, s)))
+  if (mlstm_status st = launch_status(launch_gates(igate_pre, fgate_pre, P, S, chunk, m_init, gb, gx, gu, cm, nullptr, s,
+                                                   exp_fg)))
     return st;
   if (mlstm_status st = launch_status(launch_states_simt(k, v, dt == MLSTM_BF16, gb, gx, cm, P, S, chunk, DQK,
                                                          DV, C_init, n_init, C_states, n_states, nullptr,
@@ -299,6 +317,8 @@ mlstm_status mlstm_fwd_gates(const float *igate_pre, const float *fgate_pre, int
 
 mlstm_status mlstm_fwd_check(const void *workspace, size_t ws_bytes, int B, int NH, int S, int DQK, int DV,
                              int chunk, mlstm_dtype dt, void *stream) {
+  bool exp_fg;
+  dt = split_forget(dt, exp_fg);
   if (dt != MLSTM_F32 && dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
   if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return MLSTM_ERR_SHAPE;
   if (!workspace) return MLSTM_ERR_NULL;
@@ -322,6 +342,8 @@ mlstm_status mlstm_fwd_check(const void *workspace, size_t ws_bytes, int B, int 
 mlstm_status mlstm_step(const void *q, const void *k, const void *v, const float *ig, const float *fg,
                         float *C, float *n, float *m, void *h, int B, int NH, int DQK, int DV,
                         mlstm_dtype dt, mlstm_dtype h_dt, void *stream) {
+  bool exp_fg;
+  dt = split_forget(dt, exp_fg);
   if (dt != MLSTM_F32 && dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
   if (h_dt != MLSTM_F32 && h_dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
   if (!sizes_ok(B, NH, 0, DQK, DV, 16)) return MLSTM_ERR_SHAPE;
@@ -331,12 +353,14 @@ mlstm_status mlstm_step(const void *q, const void *k, const void *v, const float
     if (!aligned16(ptr)) return MLSTM_ERR_ALIGN;
   if (mlstm_status st = check_device()) return st;
   return launch_status(launch_step(q, k, v, dt == MLSTM_BF16, h_dt == MLSTM_BF16, ig, fg, C, n, m, h,
-                                   B * NH, DQK, DV, (cudaStream_t)stream));
+                                   B * NH, DQK, DV, (cudaStream_t)stream, exp_fg));
 }
 
 mlstm_status mlstm_step_multi(const void *q, const void *k, const void *v, const float *ig, const float *fg,
                               float *C, float *n, float *m, void *h, int B, int NH, int T, int DQK, int DV,
                               mlstm_dtype dt, mlstm_dtype h_dt, void *stream) {
+  bool exp_fg;
+  dt = split_forget(dt, exp_fg);
   if (dt != MLSTM_F32 && dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
   if (h_dt != MLSTM_F32 && h_dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
   if (!sizes_ok(B, NH, 0, DQK, DV, 16) || T < 1 || T > step_multi_max_tokens()) return MLSTM_ERR_SHAPE;
@@ -346,7 +370,7 @@ mlstm_status mlstm_step_multi(const void *q, const void *k, const void *v, const
     if (!aligned16(ptr)) return MLSTM_ERR_ALIGN;
   if (mlstm_status st = check_device()) return st;
   return launch_status(launch_step_multi(q, k, v, dt == MLSTM_BF16, h_dt == MLSTM_BF16, ig, fg, C, n, m, h,
-                                         B * NH, T, DQK, DV, (cudaStream_t)stream));
+                                         B * NH, T, DQK, DV, (cudaStream_t)stream, exp_fg));
 }
 
 // ---------------------------------------------------------------- forward without allocation
@@ -365,10 +389,12 @@ mlstm_status mlstm_fwd_chunkwise_noalloc(const void *q, const void *k, const voi
                                          const float *m_init, void *h, mlstm_dtype h_dt,
                                          float *C_last, float *n_last, float *m_last,
                                          void *stream) {
-  if (dt != MLSTM_F32 && dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
+  bool exp_fg;
+  const mlstm_dtype bare = split_forget(dt, exp_fg);  // dt itself (variant included) is passed on
+  if (bare != MLSTM_F32 && bare != MLSTM_BF16) return MLSTM_ERR_DTYPE;
   if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return MLSTM_ERR_SHAPE;
   // sizes whose scratch would not fit in the fixed array are refused before anything runs
-  if (layout(B, NH, S, DQK, DV, chunk, dt).total > (size_t)MLSTM_NOALLOC_SCRATCH_BYTES)
+  if (layout(B, NH, S, DQK, DV, chunk, bare).total > (size_t)MLSTM_NOALLOC_SCRATCH_BYTES)
     return MLSTM_ERR_WORKSPACE;
   if (mlstm_status st = check_device()) return st;
   int dev = 0;

@@ -25,6 +25,8 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { retu
 // ---------------------------------------------------------------- gate math
 // log sigmoid(x) = min(x, 0) - log(1 + exp(-|x|)): the exponent is never positive.
 __device__ __forceinline__ float log_sigmoid(float x) { return fminf(x, 0.f) - log1pf(expf(-fabsf(x))); }
+// log f of the forget-gate variant: f = sigmoid(f~) (log sigmoid(f~)) or f = exp(f~) (f~ itself)
+__device__ __forceinline__ float log_forget(float x, int exp_fg) { return exp_fg ? x : log_sigmoid(x); }
 
 // ---------------------------------------------------------------- warp reductions
 __device__ __forceinline__ float warp_sum(float x) {

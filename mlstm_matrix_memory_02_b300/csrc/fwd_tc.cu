@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
     const float *__restrict__ cm, const float *__restrict__ igp, const float *__restrict__ fgp,
     const float *__restrict__ m_init, int S, int DV, float scale, const float *__restrict__ C_init,
     const float *__restrict__ n_init, TO *__restrict__ h, float *__restrict__ n_last, float *__restrict__ m_last,
-    int *__restrict__ err) {
+    int *__restrict__ err, int exp_fg) {
   constexpr int D = PAIR ? 2 * DH : DH;  // d_qk
   constexpr int QB = DH * 128;           // bytes of a [64 x DH] 2-byte tile (DH / 64 swizzled blocks)
   constexpr uint32_t kColC16 = DH;
@@ -444,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
           f2n = *reinterpret_cast<const float2 *>(fgp + tok0 + kL + 2 * lane);
           i2n = *reinterpret_cast<const float2 *>(igp + tok0 + kL + 2 * lane);
         }
-        float lf0 = log_sigmoid(f2.x), lf1 = log_sigmoid(f2.y);
+        float lf0 = log_forget(f2.x, exp_fg), lf1 = log_forget(f2.y, exp_fg);
         float bsum = lf0;
         bsum += lf1;
         lf1 = bsum;
@@ -1062,7 +1062,7 @@ cudaError_t launch_one(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
                        const float *gb, const float *gx, const float *gu, const float *cm, const float *ig,
                        const float *fg, const float *m_init, int P, int S, int DV, float scale,
                        const float *C_init, const float *n_init, void *h, float *n_last, float *m_last, int *err,
-                       cudaStream_t stream) {
+                       int exp_fg, cudaStream_t stream) {
   auto kern = fwd_tc_kernel<DH, PAIR, TO>;
   const size_t smem = smem_bytes<DH, PAIR>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1080,7 +1080,7 @@ cudaError_t launch_one(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mc, gb, gx, gu, cm, ig, fg, m_init, S, DV, scale, C_init, n_init,
-                            static_cast<TO *>(h), n_last, m_last, err);
+                            static_cast<TO *>(h), n_last, m_last, err, exp_fg);
 }
 
 template <typename TO>
@@ -1088,11 +1088,11 @@ cudaError_t launch_dispatch(int DH, bool pair, const CUtensorMap &mq, const CUte
                             const CUtensorMap &mc, const float *gb, const float *gx, const float *gu,
                             const float *cm, const float *ig, const float *fg, const float *m_init, int P, int S,
                             int DV, float scale, const float *C_init, const float *n_init, void *h, float *n_last,
-                            float *m_last, int *err, cudaStream_t stream) {
+                            float *m_last, int *err, int exp_fg, cudaStream_t stream) {
 #define MLSTM_TC_CASE(dh_, pr_)                                                                                  \
   if (DH == dh_ && pair == pr_)                                                                                  \
     return launch_one<dh_, pr_, TO>(mq, mk, mv, mc, gb, gx, gu, cm, ig, fg, m_init, P, S, DV, scale, C_init,    \
-                                    n_init, h, n_last, m_last, err, stream);
+                                    n_init, h, n_last, m_last, err, exp_fg, stream);
   MLSTM_TC_CASE(64, false)
   MLSTM_TC_CASE(128, false)
   MLSTM_TC_CASE(256, false)
@@ -1119,7 +1119,7 @@ cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, bool out_
                           const float *gx, const float *gu, const float *cm, const float *ig, const float *fg,
                           const float *m_init, int P, int S, int D, int DV, const float *C_init,
                           const float *n_init, void *h, float *C_last, float *n_last, float *m_last, int *err,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, bool exp_fg) {
   const bool pair = fwd_tc_pair(P, D, DV);
   const int DH = pair ? D / 2 : D;
   CUtensorMap mq, mk, mv, mc;
@@ -1130,9 +1130,9 @@ cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, bool out_
   const float scale = (float)(1.0 / __builtin_sqrt((double)D));
   if (out_bf16)
     return launch_dispatch<__nv_bfloat16>(DH, pair, mq, mk, mv, mc, gb, gx, gu, cm, ig, fg, m_init, P, S, DV, scale,
-                                          C_init, n_init, h, n_last, m_last, err, stream);
+                                          C_init, n_init, h, n_last, m_last, err, exp_fg ? 1 : 0, stream);
   return launch_dispatch<float>(DH, pair, mq, mk, mv, mc, gb, gx, gu, cm, ig, fg, m_init, P, S, DV, scale, C_init,
-                                n_init, h, n_last, m_last, err, stream);
+                                n_init, h, n_last, m_last, err, exp_fg ? 1 : 0, stream);
 }
 
 }  // namespace mlstm

@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(256) gates_kernel(const float *__restrict__ ig
                                                     const float *__restrict__ m_init,
                                                     float *__restrict__ gb, float *__restrict__ gx,
                                                     float *__restrict__ gu, float *__restrict__ cm,
-                                                    float *__restrict__ m_tok) {
+                                                    float *__restrict__ m_tok, int exp_fg) {
   const int p = blockIdx.x;
   const int NC = S / L;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(256) gates_kernel(const float *__restrict__ ig
     float lf[4], xi[4];
     float bsum = 0.f;
     for (int e = 0; e < E; ++e) {
-      lf[e] = active ? log_sigmoid(fg[t0 + e]) : 0.f;
+      lf[e] = active ? log_forget(fg[t0 + e], exp_fg) : 0.f;
       bsum += lf[e];
       lf[e] = bsum;  // lane-local inclusive prefix
     }
@@ -111,9 +111,9 @@ __global__ void __launch_bounds__(256) gates_kernel(const float *__restrict__ ig
 
 cudaError_t launch_gates(const float *ig, const float *fg, int P, int S, int L, const float *m_init,
                          float *gb, float *gx, float *gu, float *cm, float *m_tok,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, bool exp_fg) {
   if (P == 0) return cudaSuccess;
-  gates_kernel<<<P, 256, 0, stream>>>(ig, fg, S, L, m_init, gb, gx, gu, cm, m_tok);
+  gates_kernel<<<P, 256, 0, stream>>>(ig, fg, S, L, m_init, gb, gx, gu, cm, m_tok, exp_fg ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -5,10 +5,12 @@
 
 namespace mlstm {
 
+// exp_fg selects the exponential forget gate f = exp(f~) (log f = f~) instead of sigmoid(f~).
+//
 // (a) gate preprocessing: per-token b, x, u [P, S] and per-chunk m [P, NC+1].
 cudaError_t launch_gates(const float *ig, const float *fg, int P, int S, int L, const float *m_init,
                          float *gb, float *gx, float *gu, float *cm, float *m_tok,
-                         cudaStream_t stream);
+                         cudaStream_t stream, bool exp_fg = false);
 
 // (b) inter-chunk recurrence on CUDA cores; Cs/ns [P, NC+1, ...] (optional) and the final state.
 cudaError_t launch_states_simt(const void *k, const void *v, bool bf16, const float *gb,
@@ -25,7 +27,7 @@ cudaError_t launch_output_simt(const void *q, const void *k, const void *v, bool
 // (d) single decode step, in place.
 cudaError_t launch_step(const void *q, const void *k, const void *v, bool bf16, bool out_bf16,
                         const float *ig, const float *fg, float *C, float *n, float *m, void *h,
-                        int P, int DQK, int DV, cudaStream_t stream);
+                        int P, int DQK, int DV, cudaStream_t stream, bool exp_fg = false);
 
 // (b)+(c) fused on tensor cores (fwd_tc.cu): bf16 inputs, chunk 64, d_qk in {64, 128, 256, 512},
 // d_v a multiple of 128.  fwd_tc_pair says whether a head's d_qk is split over a CTA pair.
@@ -37,13 +39,13 @@ cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, bool out_
                           const float *gx, const float *gu, const float *cm, const float *ig, const float *fg,
                           const float *m_init, int P, int S, int D, int DV, const float *C_init,
                           const float *n_init, void *h, float *C_last, float *n_last, float *m_last, int *err,
-                          cudaStream_t stream);
+                          cudaStream_t stream, bool exp_fg = false);
 
 // (d') T consecutive decode steps in one launch, in place (T <= step_multi_max_tokens()).
 int step_multi_max_tokens();
 cudaError_t launch_step_multi(const void *q, const void *k, const void *v, bool bf16, bool out_bf16,
                               const float *ig, const float *fg, float *C, float *n, float *m, void *h, int P,
-                              int NT, int DQK, int DV, cudaStream_t stream);
+                              int NT, int DQK, int DV, cudaStream_t stream, bool exp_fg = false);
 
 // small helpers
 cudaError_t launch_copy_chunk_m(const float *cm, int P, int NC, float *m_last, cudaStream_t stream);

@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const T *__restrict__ qi
                                                         const T *__restrict__ vin, const float *__restrict__ ig,
                                                         const float *__restrict__ fg, float *__restrict__ C,
                                                         float *__restrict__ n, float *__restrict__ m,
-                                                        TO *__restrict__ h, int DQK, int DV) {
+                                                        TO *__restrict__ h, int DQK, int DV, int exp_fg) {
   __shared__ __align__(16) float sq[kMaxD];
   __shared__ __align__(16) float sk[kMaxD];  // w * khat
   __shared__ float sv[kMaxD];
@@ -38,7 +38,7 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const T *__restrict__ qi
   const float scale = rsqrtf((float)DQK);
 
   const float m_old = m[p];
-  const float lf = log_sigmoid(fg[p]);
+  const float lf = log_forget(fg[p], exp_fg);
   const float m_new = fmaxf(lf + m_old, ig[p]);
   const float alpha = expf(lf + m_old - m_new);
   const float w = expf(ig[p] - m_new);
@@ -125,26 +125,27 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const T *__restrict__ qi
 
 cudaError_t launch_step(const void *q, const void *k, const void *v, bool bf16, bool out_bf16,
                         const float *ig, const float *fg, float *C, float *n, float *m, void *h,
-                        int P, int DQK, int DV, cudaStream_t stream) {
+                        int P, int DQK, int DV, cudaStream_t stream, bool exp_fg) {
   if (P == 0) return cudaSuccess;
+  const int ef = exp_fg ? 1 : 0;
   if (bf16) {
     if (out_bf16)
       step_kernel<__nv_bfloat16, __nv_bfloat16><<<P, kThreads, 0, stream>>>(
           (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, ig, fg, C, n,
-          m, (__nv_bfloat16 *)h, DQK, DV);
+          m, (__nv_bfloat16 *)h, DQK, DV, ef);
     else
       step_kernel<__nv_bfloat16, float><<<P, kThreads, 0, stream>>>(
           (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, ig, fg, C, n,
-          m, (float *)h, DQK, DV);
+          m, (float *)h, DQK, DV, ef);
   } else {
     if (out_bf16)
       step_kernel<float, __nv_bfloat16><<<P, kThreads, 0, stream>>>(
           (const float *)q, (const float *)k, (const float *)v, ig, fg, C, n, m, (__nv_bfloat16 *)h,
-          DQK, DV);
+          DQK, DV, ef);
     else
       step_kernel<float, float><<<P, kThreads, 0, stream>>>((const float *)q, (const float *)k,
                                                             (const float *)v, ig, fg, C, n, m,
-                                                            (float *)h, DQK, DV);
+                                                            (float *)h, DQK, DV, ef);
   }
   return cudaGetLastError();
 }

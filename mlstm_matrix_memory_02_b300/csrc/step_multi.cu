@@ -63,7 +63,7 @@ template <typename T, typename TO, bool BUTTERFLY>
 __global__ void __launch_bounds__(kThreads) step_multi_kernel(
     const T *__restrict__ qin, const T *__restrict__ kin, const T *__restrict__ vin, const float *__restrict__ ig,
     const float *__restrict__ fg, float *__restrict__ C, float *__restrict__ n, float *__restrict__ m,
-    TO *__restrict__ h, int NT, int DQK, int DV) {
+    TO *__restrict__ h, int NT, int DQK, int DV, int exp_fg) {
   extern __shared__ __align__(16) float dsm[];
   float *sq = dsm;                // [NT][DQK]  q_t
   float *sk = dsm + NT * DQK;     // [NT][DQK]  w_t khat_t
@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(kThreads) step_multi_kernel(
   if (tid == 0) {
     float mm = m[p];
     for (int t = 0; t < NT; ++t) {
-      const float lf = log_sigmoid(fg[(size_t)p * NT + t]);
+      const float lf = log_forget(fg[(size_t)p * NT + t], exp_fg);
       const float it = ig[(size_t)p * NT + t];
       const float mn = fmaxf(lf + mm, it);
       s_alpha[t] = expf(lf + mm - mn);
@@ -232,13 +232,13 @@ __global__ void __launch_bounds__(kThreads) step_multi_kernel(
 template <typename T, typename TO>
 cudaError_t launch_step_multi_t(const void *q, const void *k, const void *v, const float *ig, const float *fg,
                                 float *C, float *n, float *m, void *h, int P, int NT, int DQK, int DV,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, bool exp_fg) {
   auto kern = NT >= 8 ? step_multi_kernel<T, TO, true> : step_multi_kernel<T, TO, false>;
   const size_t smem = (size_t)NT * (2 * DQK + DV) * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<P, kThreads, smem, stream>>>((const T *)q, (const T *)k, (const T *)v, ig, fg, C, n, m, (TO *)h, NT, DQK,
-                                      DV);
+                                      DV, exp_fg ? 1 : 0);
   return cudaGetLastError();
 }
 
@@ -246,14 +246,16 @@ int step_multi_max_tokens() { return kMaxT; }
 
 cudaError_t launch_step_multi(const void *q, const void *k, const void *v, bool bf16, bool out_bf16,
                               const float *ig, const float *fg, float *C, float *n, float *m, void *h, int P,
-                              int NT, int DQK, int DV, cudaStream_t stream) {
+                              int NT, int DQK, int DV, cudaStream_t stream, bool exp_fg) {
   if (P == 0 || NT == 0) return cudaSuccess;
   if (bf16)
     return out_bf16 ? launch_step_multi_t<__nv_bfloat16, __nv_bfloat16>(q, k, v, ig, fg, C, n, m, h, P, NT, DQK, DV,
-                                                                         stream)
-                    : launch_step_multi_t<__nv_bfloat16, float>(q, k, v, ig, fg, C, n, m, h, P, NT, DQK, DV, stream);
-  return out_bf16 ? launch_step_multi_t<float, __nv_bfloat16>(q, k, v, ig, fg, C, n, m, h, P, NT, DQK, DV, stream)
-                  : launch_step_multi_t<float, float>(q, k, v, ig, fg, C, n, m, h, P, NT, DQK, DV, stream);
+                                                                         stream, exp_fg)
+                    : launch_step_multi_t<__nv_bfloat16, float>(q, k, v, ig, fg, C, n, m, h, P, NT, DQK, DV, stream,
+                                                               exp_fg);
+  return out_bf16 ? launch_step_multi_t<float, __nv_bfloat16>(q, k, v, ig, fg, C, n, m, h, P, NT, DQK, DV, stream,
+                                                               exp_fg)
+                  : launch_step_multi_t<float, float>(q, k, v, ig, fg, C, n, m, h, P, NT, DQK, DV, stream, exp_fg);
 }
 
 }  // namespace mlstm

@@ -96,6 +96,10 @@ def test_fwd_argument_errors(lib):
     assert _fwd(lib, q=FAKE + 4) == ERR_ALIGN
     assert _fwd(lib, init=(FAKE, FAKE + 8, FAKE)) == ERR_ALIGN
     assert _fwd(lib, ws_bytes=16) == ERR_WS
+    # the exponential forget-gate flag rides in dt: accepted, and the other checks still apply
+    assert _fwd(lib, dt=0x100 | 5) == ERR_DTYPE
+    assert _fwd(lib, dt=0x100 | 1, S=100) == ERR_SHAPE
+    assert _fwd(lib, dt=0x100 | 1, ws_bytes=16) == ERR_WS
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device status")
@@ -111,6 +115,8 @@ def test_step_argument_errors(lib):
                               p(FAKE), 2, 2, DQK, DV, dt, hdt, p(None))
 
     assert step(dt=3) == ERR_DTYPE
+    assert step(dt=0x100 | 3) == ERR_DTYPE
+    assert step(dt=0x100 | 1, DQK=16) == ERR_SHAPE
     assert step(DQK=16) == ERR_SHAPE
     assert step(DV=544) == ERR_SHAPE
     assert step(q=None) == ERR_NULL

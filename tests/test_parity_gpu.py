@@ -452,6 +452,92 @@ def test_error_codes_do_not_launch(B):
     assert bool((h == 7).all() and (C == 7).all() and (n == 7).all() and (m == 7).all())
 
 
+# ----------------------------------------------------------------------------- exponential forget gate
+def exp_forget_inputs(inp, seed=7):
+    """Pre-activations for the exponential gate f = exp(f~): log sigmoid of the workload's
+    sigmoid-gate draws plus N(0, 0.05) noise, so that f is mostly just below 1 and sometimes
+    above it (the stabiliser then has to absorb growth as well as decay)."""
+    rng = np.random.default_rng(seed)
+    out = dict(inp)
+    fg = inp["fg"].astype(np.float64)
+    out["fg"] = (-np.logaddexp(0.0, -fg) + 0.05 * rng.standard_normal(fg.shape)).astype(np.float32)
+    return out
+
+
+EXP_CASES = [
+    # (dtype, DQK, DV, B, NH, S, chunk): CUDA-core path, tensor-core single CTA, CTA pair
+    ("f32", 32, 64, 1, 2, 96, 16),
+    ("bf16", 64, 128, 2, 1, 192, 64),
+    ("bf16", 256, 256, 1, 2, 256, 64),
+    ("bf16", 512, 256, 1, 1, 192, 64),
+]
+
+
+@pytest.mark.parametrize("dtype,dqk,dv,b,nh,s,chunk", EXP_CASES)
+def test_exp_forget_gate_forward(B, dtype, dqk, dv, b, nh, s, chunk):
+    """Forward with f = exp(f~) against the oracle's exponential variant; the same inputs
+    through the sigmoid variant must give a different answer (the flag reaches the kernel)."""
+    w = (W.TINY_F32 if dtype == "f32" else W.LAYER_350M).with_(B=b, NH=nh, S=s, DQK=dqk, DV=dv,
+                                                                chunk=chunk)
+    inp = exp_forget_inputs(W.make_inputs(w))
+    ora = oracle.recurrent(**inp, forget="exp", want_m_tok=True, want_den=True)
+    d = dev(inp, tdt(w))
+    h, C, n, m = B.mlstm_fwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], chunk,
+                                       h_dtype=torch.float32, forget="exp")
+    hs, _, _, ms = B.mlstm_fwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], chunk,
+                                         h_dtype=torch.float32)
+    torch.cuda.synchronize()
+    h = npy(h)
+    assert np.all(np.isfinite(h))
+    if dtype == "f32":
+        assert rel_err(h, ora["h"]) <= TOL_F32
+        tol = TOL_F32
+    else:
+        ok, worst, stats = conditioned_ok(h, ora, inp["v"], TOL_BF16, 4 * 2.0 ** -11,
+                                          (dqk + 64) * 2.0 ** -24)
+        assert ok, (worst, stats)
+        assert stats["rel_err_kappa_le_100"] <= TOL_BF16, stats
+        tol = TOL_BF16
+    eC, en, em = state_errs(npy(C), npy(n), npy(m), ora["C"], ora["n"], ora["m"])
+    assert eC <= tol and en <= tol and em <= 1e-4, (eC, en, em)
+    assert rel_err(npy(hs), ora["h"]) > 10 * tol  # the sigmoid reading of the same f~ differs
+
+
+@pytest.mark.parametrize("T", [1, 4, 16])
+def test_exp_forget_gate_decode(B, T):
+    """Decode steps with f = exp(f~): one token per launch (T = 1 through mlstm_step) and T
+    tokens per launch, from an exponential-gate prefill state built by the oracle."""
+    w = W.DECODE.with_(B=3, NH=2, S=T, prior=40, DQK=96, DV=64, dtype="f32")
+    prior, steps = W.make_decode_inputs(w)
+    prior, steps = exp_forget_inputs(prior, 8), exp_forget_inputs(steps, 9)
+    o_prior = oracle.recurrent(**prior, want_h=False, forget="exp")
+    o = oracle.recurrent(**steps, C0=o_prior["C"], n0=o_prior["n"], m0=o_prior["m"], forget="exp")
+    C = torch.from_numpy(o_prior["C"].astype(np.float32)).cuda()
+    n = torch.from_numpy(o_prior["n"].astype(np.float32)).cuda()
+    m = torch.from_numpy(o_prior["m"].astype(np.float32)).cuda()
+    s = dev(steps, torch.float32)
+    if T == 1:
+        h = B.mlstm_step(*(s[k_][:, :, 0].contiguous() for k_ in ("q", "k", "v", "ig", "fg")), C, n, m,
+                         forget="exp")[:, :, None]
+    else:
+        h = B.mlstm_step_multi(s["q"], s["k"], s["v"], s["ig"], s["fg"], C, n, m, h_dtype=torch.float32,
+                               forget="exp")
+    torch.cuda.synchronize()
+    assert rel_err(npy(h), o["h"]) <= TOL_F32
+    eC, en, em = state_errs(npy(C), npy(n), npy(m), o["C"], o["n"], o["m"])
+    assert eC <= TOL_F32 and en <= TOL_F32 and em <= 1e-5
+
+
+def test_exp_forget_gate_flag_in_sizing_queries(B):
+    """The sizing and path queries accept the forget-gate flag and ignore it."""
+    lib = B.library()
+    for dt in (0, 1):
+        assert lib.mlstm_fwd_path(1, 2, 256, 256, 256, 64, dt | B.FORGET_EXP) == lib.mlstm_fwd_path(1, 2, 256, 256, 256, 64, dt)
+        assert (lib.mlstm_fwd_workspace_bytes(1, 2, 256, 256, 256, 64, dt | B.FORGET_EXP)
+                == lib.mlstm_fwd_workspace_bytes(1, 2, 256, 256, 256, 64, dt))
+    assert lib.mlstm_fwd_path(1, 2, 256, 256, 256, 64, 2 | B.FORGET_EXP) == -1
+
+
 # ----------------------------------------------------------------------------- tensor-core path
 TC_CASES = [
     # (DQK, DV, B, NH, S, gates, init)
