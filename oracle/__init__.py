@@ -11,8 +11,9 @@ The arithmetic lives in ``mlstm_oracle.c`` (plain C, fp64, one POSIX thread per
 Scale Recurrent Neural Networks" (llms.blog): section 2 "The Normalizer State and Numerical
 Stabilization" for the log-space max stabiliser, section 3 "Associative Matrix Cell State"
 for the key scale, the C_t / n_t updates and the retrieval, and section 3 "The Parallel
-Dual Form" for the quadratic form.  Pins against closed forms, exact rational arithmetic and
-library routines are in ``tests/test_oracle_pins.py``.
+Dual Form" for the quadratic form.  ``groupnorm_gate`` (numpy) is the block step after the
+cell: per-head group normalisation and the output gate.  Pins against closed forms, exact
+rational arithmetic and library routines are in ``tests/test_oracle_pins.py``.
 
 Parity pinning: every routine here is pinned (no routine is "parity unpinned").
 """
@@ -173,3 +174,25 @@ def parallel(q, k, v, ig, fg, nthreads=0, lib=None, forget="sigmoid"):
     if rc != 0:
         raise ValueError(f"oracle_mlstm_parallel rejected its arguments (code {rc})")
     return h
+
+
+def groupnorm_gate(h, o_pre, gamma, beta, eps=1e-5):
+    """The block's step after the cell (page section 4 "xLSTM Block Architecture and Residual
+    Stacking", the mLSTM block's item 5 "Group Normalization and Output Gating"; section 3
+    "Associative Matrix Cell State": h_t = o_t (.) h~_t), in fp64 with numpy.
+
+    h, o_pre: [B, NH, S, DV] (the cell output h~ and the output-gate pre-activation);
+    gamma, beta: [NH, DV].  Each head is one group: for every (b, head, t),
+        mu = mean_c h~_c,  var = mean_c (h~_c - mu)^2,
+        y_c = sigmoid(o~_c) * (gamma_c (h~_c - mu) / sqrt(var + eps) + beta_c).
+    Readings: the output gate is the LSTM sigmoid gate o = sigmoid(o~); the normalisation is
+    applied before the gate; the variance is the biased one (divide by DV)."""
+    h = np.asarray(h, np.float64)
+    o = np.asarray(o_pre, np.float64)
+    g = np.asarray(gamma, np.float64)[None, :, None, :]
+    b = np.asarray(beta, np.float64)[None, :, None, :]
+    mu = h.mean(axis=-1, keepdims=True)
+    var = ((h - mu) ** 2).mean(axis=-1, keepdims=True)
+    norm = (h - mu) / np.sqrt(var + eps)
+    gate = 1.0 / (1.0 + np.exp(-o))
+    return gate * (g * norm + b)

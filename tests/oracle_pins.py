@@ -305,6 +305,51 @@ def pin_exp_forget_two_token_scalar(lib):
     return worst <= 1e-13, f"exp forget two-token closed form err {worst:.3e}"
 
 
+# ---------------------------------------------------------------- group norm and output gate
+def _gn_inputs(seed, B=2, NH=3, S=5, DV=40):
+    rng = np.random.default_rng(seed)
+    h = 2.0 * rng.standard_normal((B, NH, S, DV)) + 0.7
+    o = 1.5 * rng.standard_normal((B, NH, S, DV))
+    g = 1.0 + 0.3 * rng.standard_normal((NH, DV))
+    b = 0.2 * rng.standard_normal((NH, DV))
+    return h, o, g, b
+
+
+def pin_groupnorm_matches_torch(lib):
+    """The normalisation is torch's group_norm with one group per head (a library routine,
+    fp64 on the CPU): per token, the NH * DV channels split into NH groups of DV."""
+    import torch
+    h, o, g, b = _gn_inputs(31)
+    B, NH, S, DV = h.shape
+    big = np.full_like(o, 60.0)  # sigmoid(60) == 1 in fp64: the gate is the identity
+    y = oracle.groupnorm_gate(h, big, g, b, eps=1e-5)
+    x = torch.from_numpy(np.ascontiguousarray(h.transpose(0, 2, 1, 3).reshape(B * S, NH * DV)))
+    ref = torch.nn.functional.group_norm(x, NH, torch.from_numpy(g.reshape(-1)),
+                                         torch.from_numpy(b.reshape(-1)), eps=1e-5)
+    ref = ref.numpy().reshape(B, S, NH, DV).transpose(0, 2, 1, 3)
+    err = rel(y, ref)
+    return err <= 1e-13, f"group norm vs torch err {err:.3e}"
+
+
+def pin_groupnorm_gate_invariants(lib):
+    """gamma = 1, beta = 0, open gate: every (b, head, t) row has mean 0 and variance
+    var / (var + eps); a shut-half gate (o~ = 0, sigmoid = 1/2) halves the output; a constant
+    row normalises to 0, leaving sigmoid(o~) beta."""
+    h, o, g, b = _gn_inputs(32)
+    NH, DV = g.shape
+    ones, zeros = np.ones((NH, DV)), np.zeros((NH, DV))
+    y = oracle.groupnorm_gate(h, np.full_like(o, 60.0), ones, zeros, eps=1e-3)
+    var = h.var(axis=-1)
+    err = max(float(np.max(np.abs(y.mean(axis=-1)))),
+              float(np.max(np.abs(y.var(axis=-1) - var / (var + 1e-3)))))
+    half = oracle.groupnorm_gate(h, np.zeros_like(o), g, b)
+    full = oracle.groupnorm_gate(h, np.full_like(o, 60.0), g, b)
+    err = max(err, rel(half, 0.5 * full))
+    const = oracle.groupnorm_gate(np.full_like(h, 3.25), o, g, b)
+    err = max(err, rel(const, b[None, :, None, :] / (1.0 + np.exp(-o))))
+    return err <= 1e-13, f"group norm / gate invariants err {err:.3e}"
+
+
 ALL_PINS = [
     pin_recurrent_equals_parallel,
     pin_stabiliser_is_a_rescaling,
@@ -321,6 +366,8 @@ ALL_PINS = [
     pin_exp_forget_dual_form,
     pin_exp_forget_equals_sigmoid_in_log_space,
     pin_exp_forget_two_token_scalar,
+    pin_groupnorm_matches_torch,
+    pin_groupnorm_gate_invariants,
 ]
 
 
