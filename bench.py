@@ -417,6 +417,38 @@ def run_ours(args, rank, local, world):
               "multi_token": multi}
     del Cd, nd, md
 
+    # ---- block step after the cell: group norm + output gate on the layer's h (fp32 h, bf16
+    # o~ and y: 134 MB per launch, larger than L2, so consecutive launches do not hit in L2)
+    g_rng = torch.Generator(device=dev).manual_seed(3)
+    o_pre = torch.randn(h.shape, device=dev, generator=g_rng).to(torch.bfloat16)
+    gam = 1.0 + 0.3 * torch.randn((w.NH, w.DV), device=dev, generator=g_rng)
+    bet = 0.2 * torch.randn((w.NH, w.DV), device=dev, generator=g_rng)
+    y_gn = torch.empty(h.shape, dtype=torch.bfloat16, device=dev)
+    for _ in range(max(args.warmup, 3)):
+        B.mlstm_groupnorm_gate(h, o_pre, gam, bet, 1e-5, out=y_gn)
+    torch.cuda.synchronize()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    l0 = B.mlstm_kernel_launches()
+    g0.record(stream)
+    for _ in range(args.steps):
+        B.mlstm_groupnorm_gate(h, o_pre, gam, bet, 1e-5, out=y_gn)
+    g1.record(stream)
+    torch.cuda.synchronize()
+    launches_gn = B.mlstm_kernel_launches() - l0
+    gn_us = g0.elapsed_time(g1) / max(args.steps, 1) * 1e3
+    gn_bytes = float(h.numel() * (4 + 2 + 2) + 2 * w.NH * w.DV * 4)
+    gn_gbs = gn_bytes / (gn_us * 1e-6) / 1e9
+    block_epilogue = {"metric": "group norm + output gate GB/s (1.3B-style layer h: fp32 in, bf16 o~ and y)",
+                      "value": gn_gbs, "unit": "GB/s", "us_per_launch": gn_us,
+                      "roofline": {"bound": "hbm", "achieved": gn_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                   "frac": gn_gbs / peaks["hbm_gbs"],
+                                   "traffic": captured_traffic("groupnorm_gate_kernel"),
+                                   "kernel": "groupnorm_gate_kernel", "algorithmic_bytes_per_launch": gn_bytes,
+                                   "peak_source": peaks["source"] + " HBM copy"},
+                      "l2": "134 MB per launch, larger than L2 (no flush)"}
+    del o_pre, y_gn
+
     # ---- end to end through the public API: pinned host inputs in, h back to the host
     pin = {key: torch.from_numpy(inp[key]).to(torch.bfloat16 if key in "qkv" else torch.float32).pin_memory()
            for key in ("q", "k", "v", "ig", "fg")}
@@ -445,9 +477,10 @@ def run_ours(args, rank, local, world):
         "metric": f"mLSTM chunkwise forward tokens/s ({w.name})",
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_max, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "NH": w.NH, "S": w.S, "DQK": w.DQK, "DV": w.DV,
                    "chunk": w.chunk, "qkv": "bf16", "gates": "fp32", "h": "fp32",
+                   "mma": "fp16 operands (bf16 for Q K^T), fp32 accumulation in tensor memory",
                    "kernel_path": {0: "CUDA cores", 1: "tensor cores (tcgen05, fused, one CTA per d_v tile)",
                                    2: "tensor cores (tcgen05, fused, d_qk split over a CTA pair)"}[
                        B.mlstm_fwd_path(w.B, w.NH, w.S, w.DQK, w.DV, w.chunk)],
@@ -455,9 +488,10 @@ def run_ours(args, rank, local, world):
                    "per_rank": "each rank runs the full layer batch (weak scaling)"},
         "roofline": roofline,
         "decode": decode,
+        "block_epilogue": block_epilogue,
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": int(launches_fwd + launches_dec),
+        "gpu_launches": int(launches_fwd + launches_dec + launches_gn),
         "clocks": clk.summary(),
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -475,7 +509,8 @@ def run_profile(kind: str):
 
     fwd:          the --workload forward (one fused launch on the tensor-core path)
     decode:       one decode step of the B=256, NH=8, d=256 state (state initialised randomly)
-    decode_multi: 16 decode steps in one launch on the same state"""
+    decode_multi: 16 decode steps in one launch on the same state
+    gn:           group norm + output gate on a 1.3B-layer-shaped h (fp32 h, bf16 o~ and y)"""
     import torch
     from mlstm_matrix_memory_02_b300 import binding as B
     dev = torch.device("cuda", 0)
@@ -486,6 +521,16 @@ def run_profile(kind: str):
         ig, fg = (torch.from_numpy(inp[x]).to(dev) for x in ("ig", "fg"))
         for _ in range(2):
             B.mlstm_fwd_chunkwise(q, k, v, ig, fg, w.chunk, h_dtype=torch.float32)
+    elif kind == "gn":
+        w = FWD
+        g = torch.Generator(device=dev).manual_seed(3)
+        h = torch.randn((w.B, w.NH, w.S, w.DV), device=dev, generator=g)
+        o = torch.randn(h.shape, device=dev, generator=g).to(torch.bfloat16)
+        gam = torch.ones((w.NH, w.DV), device=dev)
+        bet = torch.zeros((w.NH, w.DV), device=dev)
+        y = torch.empty(h.shape, dtype=torch.bfloat16, device=dev)
+        for _ in range(2):
+            B.mlstm_groupnorm_gate(h, o, gam, bet, 1e-5, out=y)
     elif kind == "decode_multi":
         w = DEC
         T = 16
@@ -524,7 +569,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["1p3b", "350m", "stress"], default="1p3b",
                     help="forward workload (default: the 1.3B-style layer)")
-    ap.add_argument("--profile", choices=["fwd", "decode", "decode_multi"], default=None,
+    ap.add_argument("--profile", choices=["fwd", "decode", "decode_multi", "gn"], default=None,
                     help="run one small forward or decode step for ncu captures and exit")
     args = ap.parse_args()
     global FWD

@@ -173,6 +173,24 @@ mlstm_status mlstm_step_multi(const void *q, const void *k, const void *v, const
                               const float *fg, float *C, float *n, float *m, void *h, int B, int NH,
                               int T, int DQK, int DV, mlstm_dtype dt, mlstm_dtype h_dt, void *stream);
 
+/* The mLSTM block's step after the cell (section 4 "xLSTM Block Architecture and Residual
+ * Stacking", the mLSTM block's item 5 "Group Normalization and Output Gating"; section 3
+ * "Associative Matrix Cell State": h_t = o_t (.) h~_t).  For every (batch, head, token) row of
+ * DV channels, with the head as the normalisation group:
+ *   mu = mean_c h~_c, var = mean_c (h~_c - mu)^2 (biased),
+ *   y_c = sigmoid(o~_c) * (gamma_c (h~_c - mu) / sqrt(var + eps) + beta_c)
+ *   h  [B, NH, S, DV] (h_dt): the cell output h~, e.g. mlstm_fwd_chunkwise's h
+ *   o_pre [B, NH, S, DV] (o_dt): the output-gate pre-activations o~
+ *   gamma, beta [NH, DV] float32: per-channel scale and shift
+ *   y  [B, NH, S, DV] (y_dt) output; y may be h itself when y_dt == h_dt (each row is read
+ *      completely before it is written).
+ * eps > 0.  DV a multiple of 32 in [32, 512]; S >= 0 (S = 0 launches nothing).  The pages do
+ * not fix the gate's form or the epsilon: the sigmoid output gate of the LSTM and the caller's
+ * eps are used.  Memory bound: one read of h and o_pre and one write of y. */
+mlstm_status mlstm_groupnorm_gate(const void *h, const void *o_pre, const float *gamma, const float *beta,
+                                  float eps, void *y, int B, int NH, int S, int DV, mlstm_dtype h_dt,
+                                  mlstm_dtype o_dt, mlstm_dtype y_dt, void *stream);
+
 /* Forward without any device allocation (no counterpart on the source pages: an interface
  * addition of this library).
  *

@@ -31,6 +31,8 @@ _lib.mlstm_status_str.restype = ctypes.c_char_p
 _lib.mlstm_status_str.argtypes = [_i]
 _lib.mlstm_last_cuda_error.restype = _i
 _lib.mlstm_last_cuda_error.argtypes = []
+_lib.mlstm_groupnorm_gate.restype = _i
+_lib.mlstm_groupnorm_gate.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _i, _i, _i, _i, _i, _i, _i, _vp]
 _lib.mlstm_kernel_launches.restype = ctypes.c_ulonglong
 _lib.mlstm_kernel_launches.argtypes = []
 _lib.mlstm_fwd_from_gates.restype = _i
@@ -64,7 +66,7 @@ _lib.mlstm_fwd_chunkwise_noalloc.argtypes = [_vp, _vp, _vp, _fp, _fp, _i, _i, _i
 EXPORTED = ["mlstm_status_str", "mlstm_last_cuda_error", "mlstm_kernel_launches",
             "mlstm_fwd_workspace_bytes", "mlstm_fwd_chunkwise", "mlstm_fwd_from_gates",
             "mlstm_fwd_chunk_states", "mlstm_fwd_gates", "mlstm_fwd_check", "mlstm_fwd_path",
-            "mlstm_step", "mlstm_step_multi", "mlstm_fwd_chunkwise_noalloc"]
+            "mlstm_step", "mlstm_step_multi", "mlstm_fwd_chunkwise_noalloc", "mlstm_groupnorm_gate"]
 
 # Bytes of the fixed scratch array behind mlstm_fwd_chunkwise_noalloc (include/mlstm.h).
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -346,3 +348,26 @@ def mlstm_step(q, k, v, ig, fg, C, n, m, h=None, h_dtype=None, stream=None, forg
                            _stream(stream))
     _check(code, "mlstm_step")
     return h
+
+
+def mlstm_groupnorm_gate(h, o_pre, gamma, beta, eps=1e-5, out=None, y_dtype=None, stream=None):
+    """The block step after the cell: per-head group normalisation of h [B,NH,S,DV] and the
+    output gate, y = sigmoid(o_pre) * (gamma * (h - mean) / sqrt(var + eps) + beta), with
+    gamma, beta [NH, DV] float32.  ``out`` may be h itself (same dtype) for an in-place pass."""
+    B, NH, S, DV = h.shape
+    if h.dtype not in _DT or o_pre.dtype not in _DT:
+        raise TypeError("h and o_pre must be float32 or bfloat16")
+    _dev(h, "h", h.dtype)
+    _dev(o_pre, "o_pre", o_pre.dtype, (B, NH, S, DV))
+    _dev(gamma, "gamma", torch.float32, (NH, DV))
+    _dev(beta, "beta", torch.float32, (NH, DV))
+    if out is None:
+        out = torch.empty((B, NH, S, DV), dtype=y_dtype or h.dtype, device=h.device)
+    if out.dtype not in _DT:
+        raise TypeError("the output must be float32 or bfloat16")
+    _dev(out, "out", out.dtype, (B, NH, S, DV))
+    code = _lib.mlstm_groupnorm_gate(_ptr(h), _ptr(o_pre), _ptr(gamma), _ptr(beta), float(eps), _ptr(out),
+                                     B, NH, S, DV, _DT[h.dtype], _DT[o_pre.dtype], _DT[out.dtype],
+                                     _stream(stream))
+    _check(code, "mlstm_groupnorm_gate")
+    return out

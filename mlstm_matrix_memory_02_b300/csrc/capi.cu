@@ -373,6 +373,22 @@ mlstm_status mlstm_step_multi(const void *q, const void *k, const void *v, const
                                          B * NH, T, DQK, DV, (cudaStream_t)stream, exp_fg));
 }
 
+mlstm_status mlstm_groupnorm_gate(const void *h, const void *o_pre, const float *gamma, const float *beta,
+                                  float eps, void *y, int B, int NH, int S, int DV, mlstm_dtype h_dt,
+                                  mlstm_dtype o_dt, mlstm_dtype y_dt, void *stream) {
+  for (mlstm_dtype d : {h_dt, o_dt, y_dt})
+    if (d != MLSTM_F32 && d != MLSTM_BF16) return MLSTM_ERR_DTYPE;
+  if (B < 1 || NH < 1 || S < 0 || (long long)B * NH * S > (1LL << 40)) return MLSTM_ERR_SHAPE;
+  if (DV < 32 || DV > 512 || DV % 32 != 0) return MLSTM_ERR_SHAPE;
+  if (!(eps > 0.f) || !(eps < 3.0e38f)) return MLSTM_ERR_SHAPE;  // also rejects NaN
+  if (!gamma || !beta || (S > 0 && (!h || !o_pre || !y))) return MLSTM_ERR_NULL;
+  for (const void *ptr : {h, o_pre, (const void *)gamma, (const void *)beta, (const void *)y})
+    if (!aligned16(ptr)) return MLSTM_ERR_ALIGN;
+  if (mlstm_status st = check_device()) return st;
+  return launch_status(launch_groupnorm_gate(h, h_dt == MLSTM_BF16, o_pre, o_dt == MLSTM_BF16, gamma, beta, eps, y,
+                                             y_dt == MLSTM_BF16, B, NH, S, DV, (cudaStream_t)stream));
+}
+
 // ---------------------------------------------------------------- forward without allocation
 // The scratch of mlstm_fwd_chunkwise_noalloc: a fixed array in device memory, part of the
 // library's image, so that every GPU that loads the library holds it until the process exits.

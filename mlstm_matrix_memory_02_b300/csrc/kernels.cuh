@@ -47,6 +47,12 @@ cudaError_t launch_step_multi(const void *q, const void *k, const void *v, bool 
                               const float *ig, const float *fg, float *C, float *n, float *m, void *h, int P,
                               int NT, int DQK, int DV, cudaStream_t stream, bool exp_fg = false);
 
+// The block step after the cell: per-head group normalisation of h~ and the output gate,
+// y = sigmoid(o~) (gamma (h~ - mu) / sqrt(var + eps) + beta) per (batch, head, token) row.
+cudaError_t launch_groupnorm_gate(const void *h, bool h_bf16, const void *o_pre, bool o_bf16, const float *gamma,
+                                  const float *beta, float eps, void *y, bool y_bf16, int B, int NH, int S, int DV,
+                                  cudaStream_t stream);
+
 // small helpers
 cudaError_t launch_copy_chunk_m(const float *cm, int P, int NC, float *m_last, cudaStream_t stream);
 

@@ -143,3 +143,23 @@ def test_binding_rejects_cpu_tensors(lib):
     g = torch.zeros(1, 1, 64)
     with pytest.raises(TypeError):
         binding.mlstm_fwd_chunkwise(x, x, x, g, g, 16)
+
+
+def test_groupnorm_gate_argument_errors(lib):
+    p = ctypes.c_void_p
+
+    def gn(h=FAKE, gamma=FAKE, DV=64, S=4, eps=1e-5, dts=(0, 0, 0)):
+        return lib.mlstm_groupnorm_gate(p(h), p(FAKE), p(gamma), p(FAKE), ctypes.c_float(eps), p(FAKE),
+                                         2, 2, S, DV, *dts, p(None))
+
+    assert gn(dts=(2, 0, 0)) == ERR_DTYPE
+    assert gn(dts=(0, 0, 0x100)) == ERR_DTYPE  # the forget-gate flag has no meaning here
+    assert gn(DV=48) == ERR_SHAPE
+    assert gn(DV=544) == ERR_SHAPE
+    assert gn(S=-1) == ERR_SHAPE
+    assert gn(eps=0.0) == ERR_SHAPE
+    assert gn(eps=float("nan")) == ERR_SHAPE
+    assert gn(h=None) == ERR_NULL
+    assert gn(gamma=None, S=0) == ERR_NULL
+    assert gn(h=FAKE + 8) == ERR_ALIGN
+

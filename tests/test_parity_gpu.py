@@ -538,6 +538,74 @@ def test_exp_forget_gate_flag_in_sizing_queries(B):
     assert lib.mlstm_fwd_path(1, 2, 256, 256, 256, 64, 2 | B.FORGET_EXP) == -1
 
 
+# ----------------------------------------------------------------------------- group norm and gate
+_TD = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def _gn_case(seed, b, nh, s, dv):
+    rng = np.random.default_rng(seed)
+    h = (1.7 * rng.standard_normal((b, nh, s, dv)) + 0.3).astype(np.float32)
+    o = (1.5 * rng.standard_normal((b, nh, s, dv))).astype(np.float32)
+    g = (1.0 + 0.3 * rng.standard_normal((nh, dv))).astype(np.float32)
+    be = (0.2 * rng.standard_normal((nh, dv))).astype(np.float32)
+    return h, o, g, be
+
+
+@pytest.mark.parametrize("hdt,odt,ydt,b,nh,s,dv", [("f32", "f32", "f32", 2, 3, 17, 64),
+                                                   ("bf16", "bf16", "bf16", 1, 4, 33, 512),
+                                                   ("f32", "bf16", "bf16", 2, 2, 9, 96),
+                                                   ("bf16", "f32", "f32", 1, 1, 5, 32)])
+def test_groupnorm_gate(B, hdt, odt, ydt, b, nh, s, dv):
+    """Per-head group normalisation and output gate against the oracle (inputs in the kernel's
+    dtypes, the oracle fed the same rounded values)."""
+    h, o, g, be = _gn_case(41, b, nh, s, dv)
+    hd = torch.from_numpy(h).cuda().to(_TD[hdt])
+    od = torch.from_numpy(o).cuda().to(_TD[odt])
+    y = B.mlstm_groupnorm_gate(hd, od, torch.from_numpy(g).cuda(), torch.from_numpy(be).cuda(), 1e-5,
+                               y_dtype=_TD[ydt])
+    torch.cuda.synchronize()
+    ref = oracle.groupnorm_gate(npy(hd), npy(od), g, be, 1e-5)
+    assert rel_err(npy(y), ref) <= (TOL_F32 if ydt == "f32" else TOL_BF16)
+
+
+def test_groupnorm_gate_in_place_and_constant_rows(B):
+    """y written over h; rows with zero variance normalise to 0 and leave sigmoid(o) beta."""
+    h, o, g, be = _gn_case(42, 2, 2, 8, 128)
+    h[:, :, 3] = 2.5  # constant rows
+    ref = oracle.groupnorm_gate(h, o, g, be, 1e-5)
+    hd = torch.from_numpy(h).cuda()
+    y = B.mlstm_groupnorm_gate(hd, torch.from_numpy(o).cuda(), torch.from_numpy(g).cuda(),
+                               torch.from_numpy(be).cuda(), 1e-5, out=hd)
+    torch.cuda.synchronize()
+    assert y.data_ptr() == hd.data_ptr()
+    assert rel_err(npy(y), ref) <= TOL_F32
+    const = npy(y)[:, :, 3]
+    assert np.allclose(const, (be[None, :, :] / (1.0 + np.exp(-o[:, :, 3]))), rtol=1e-5, atol=1e-6)
+
+
+def test_groupnorm_gate_after_forward_full_size(B):
+    """The block step on the 1.3B-style layer's forward output (fp32 h, bf16 o~, bf16 y):
+    256 sampled rows against the oracle applied to the same h."""
+    w = W.LAYER_1P3B
+    inp = W.make_inputs(w)
+    d = dev(inp, torch.bfloat16)
+    h, _, _, _ = B.mlstm_fwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], w.chunk, h_dtype=torch.float32)
+    rng = np.random.default_rng(43)
+    o = torch.from_numpy((1.5 * rng.standard_normal(h.shape)).astype(np.float32)).cuda().to(torch.bfloat16)
+    g = torch.from_numpy((1.0 + 0.3 * rng.standard_normal((w.NH, w.DV))).astype(np.float32)).cuda()
+    be = torch.from_numpy((0.2 * rng.standard_normal((w.NH, w.DV))).astype(np.float32)).cuda()
+    y = B.mlstm_groupnorm_gate(h, o, g, be, 1e-5, y_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    rows = rng.choice(w.B * w.NH * w.S, 256, replace=False)
+    hh = npy(h).reshape(-1, w.DV)[rows]
+    oo = npy(o).reshape(-1, w.DV)[rows]
+    head = (rows // w.S) % w.NH
+    ref = np.stack([oracle.groupnorm_gate(hh[i][None, None, None], oo[i][None, None, None],
+                                          npy(g)[head[i]][None], npy(be)[head[i]][None], 1e-5).ravel()
+                    for i in range(len(rows))])
+    assert rel_err(npy(y).reshape(-1, w.DV)[rows], ref) <= TOL_BF16
+
+
 # ----------------------------------------------------------------------------- tensor-core path
 TC_CASES = [
     # (DQK, DV, B, NH, S, gates, init)
