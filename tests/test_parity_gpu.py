@@ -565,7 +565,11 @@ def test_groupnorm_gate(B, hdt, odt, ydt, b, nh, s, dv):
                                y_dtype=_TD[ydt])
     torch.cuda.synchronize()
     ref = oracle.groupnorm_gate(npy(hd), npy(od), g, be, 1e-5)
-    assert rel_err(npy(y), ref) <= (TOL_F32 if ydt == "f32" else TOL_BF16)
+    if ydt == "f32":
+        assert rel_err(npy(y), ref) <= TOL_F32
+    else:  # rounding y to bf16 alone can exceed 2e-2 of the RMS at the largest outputs
+        ok, worst = bf16_out_ok(npy(y), ref)
+        assert ok, worst
 
 
 def test_groupnorm_gate_in_place_and_constant_rows(B):
@@ -603,7 +607,8 @@ def test_groupnorm_gate_after_forward_full_size(B):
     ref = np.stack([oracle.groupnorm_gate(hh[i][None, None, None], oo[i][None, None, None],
                                           npy(g)[head[i]][None], npy(be)[head[i]][None], 1e-5).ravel()
                     for i in range(len(rows))])
-    assert rel_err(npy(y).reshape(-1, w.DV)[rows], ref) <= TOL_BF16
+    ok, worst = bf16_out_ok(npy(y).reshape(-1, w.DV)[rows], ref)
+    assert ok, worst
 
 
 # ----------------------------------------------------------------------------- tensor-core path
