@@ -337,7 +337,8 @@ def run_ours(args, rank, local, world):
     achieved_tf = flops / (ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved_tf, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": achieved_tf / peaks["bf16_tflops"],
-                "traffic": captured_traffic("fwd_tc_kernel") if path >= 1 else None,
+                # the committed capture is of the 1.3B-style layer: other workloads report none
+                "traffic": captured_traffic("fwd_tc_kernel") if path >= 1 and w is W.LAYER_1P3B else None,
                 "kernel": ("fwd_tc_kernel (the whole forward: one launch)" if path >= 1
                            else "gates + states + output kernels"),
                 "algorithmic_flops_per_launch": flops, "ms_per_launch": ms,

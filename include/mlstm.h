@@ -76,13 +76,17 @@ int mlstm_last_cuda_error(void);
  * the difference across a region counts the library's launches inside it. */
 unsigned long long mlstm_kernel_launches(void);
 
-/* Which kernels mlstm_fwd_chunkwise / mlstm_fwd_from_gates run for these sizes:
+/* Which kernels mlstm_fwd_chunkwise runs for these sizes:
  * 1 = the fused tensor-core kernel, one CTA per (head, 128 rows of d_v);
  * 2 = the same kernel with each head's d_qk split over a pair of CTAs (a thread-block
  *     cluster exchanging partial sums through distributed shared memory) -- always for
  *     d_qk = 512, and for smaller heads when the single-CTA grid would leave SMs idle;
- *     (both: bf16 inputs, chunk 64, d_qk in {64, 128, 256, 512}, d_v a multiple of 128)
- * 0 = the CUDA-core kernels (every other supported size), -1 = unsupported sizes or dtype. */
+ *     (both: bf16 inputs, S a multiple of 64, d_qk in {64, 128, 256, 512}, d_v a multiple
+ *     of 128; the kernel walks the sequence in its own chunks of 64 tokens whatever `chunk`
+ *     asks for -- the result is the same function up to rounding)
+ * 0 = the CUDA-core kernels (every other supported size), -1 = unsupported sizes or dtype.
+ * mlstm_fwd_from_gates runs the fused kernel only for chunk 64 (its workspace holds the gate
+ * preprocessing of the asked-for chunk) and the CUDA-core kernels otherwise. */
 int mlstm_fwd_path(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt);
 
 /* Bytes of device workspace mlstm_fwd_chunkwise / mlstm_fwd_chunk_states need for these

@@ -22,6 +22,7 @@ cudaError_t launch_copy_chunk_m(const float *cm, int P, int NC, float *m_last, c
 namespace {
 
 constexpr size_t kAlign = 256;
+constexpr int kTcChunk = 64;  // the fused tensor-core kernel's chunk
 constexpr int kMaxPairs = 65535;  // grid.z limit of the output kernel
 
 inline size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -132,7 +133,7 @@ int mlstm_fwd_path(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype
   dt = split_forget(dt, exp_fg);
   if (dt != MLSTM_F32 && dt != MLSTM_BF16) return -1;
   if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return -1;
-  if (!use_tc(B, NH, S, DQK, DV, chunk, dt)) return 0;
+  if (!use_tc(B, NH, S, DQK, DV, kTcChunk, dt)) return 0;
   return fwd_tc_pair(B * NH, DQK, DV) ? 2 : 1;
 }
 
@@ -239,12 +240,15 @@ mlstm_status mlstm_fwd_chunkwise(const void *q, const void *k, const void *v, co
   if (mlstm_status st = check_device()) return st;
 
   cudaStream_t s = (cudaStream_t)stream;
-  const Layout Lw = layout(B, NH, S, DQK, DV, chunk, dt);
   char *ws = (char *)workspace;
   const int P = B * NH;
-  if (Lw.tc)  // the fused kernel preprocesses the gates itself
-    return run_from_gates(q, k, v, B, NH, S, DQK, DV, chunk, dt, C_init, n_init, h, h_dt, C_last, n_last,
+  // The fused kernel preprocesses the gates itself and walks the sequence in its own chunks of
+  // 64 tokens, whatever chunk was asked for (the result is the same function up to rounding);
+  // its workspace needs are below those of the asked-for chunk's layout, which was checked.
+  if (use_tc(B, NH, S, DQK, DV, kTcChunk, dt))
+    return run_from_gates(q, k, v, B, NH, S, DQK, DV, kTcChunk, dt, C_init, n_init, h, h_dt, C_last, n_last,
                           m_last, workspace, s, igate_pre, fgate_pre, m_init, exp_fg);
+  const Layout Lw = layout(B, NH, S, DQK, DV, chunk, dt);
   if (mlstm_status st = launch_status(launch_gates(igate_pre, fgate_pre, P, S, chunk, m_init, (float *)(ws + Lw.gb),
                                                    (float *)(ws + Lw.gx), (float *)(ws + Lw.gu),
                                                    (float *)(ws + Lw.cm), nullptr, s, exp_fg)))

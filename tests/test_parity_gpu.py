@@ -130,9 +130,13 @@ def test_stress_forward_full_size(B):
     ora = oracle.recurrent(**inp, want_m_tok=True, want_den=True)
     h, C, n, m = run_fwd(B, w, inp)
     assert np.all(np.isfinite(h)), "NaN/Inf in h"
-    # fp32 CUDA-core arithmetic: relative error per summed term <= (terms) * 2^-24
-    u = (w.DQK + w.chunk) * 2.0 ** -24
-    ok, worst, stats = conditioned_ok(h, ora, inp["v"], TOL_BF16, u, u)
+    if B.mlstm_fwd_path(w.B, w.NH, w.S, w.DQK, w.DV, w.chunk) >= 1:
+        # fused tensor-core kernel: fp16 operands (2^-11 per term), fp32 denominators
+        u_num, u_den = 4 * 2.0 ** -11, (w.DQK + 64) * 2.0 ** -24
+    else:
+        # fp32 CUDA-core arithmetic: relative error per summed term <= (terms) * 2^-24
+        u_num = u_den = (w.DQK + w.chunk) * 2.0 ** -24
+    ok, worst, stats = conditioned_ok(h, ora, inp["v"], TOL_BF16, u_num, u_den)
     assert ok, (worst, stats)
     assert stats["rel_err_kappa_le_100"] <= TOL_BF16, stats
     eC, en, em = state_errs(C, n, m, ora["C"], ora["n"], ora["m"])
