@@ -12,7 +12,8 @@ Scale Recurrent Neural Networks" (llms.blog): section 2 "The Normalizer State an
 Stabilization" for the log-space max stabiliser, section 3 "Associative Matrix Cell State"
 for the key scale, the C_t / n_t updates and the retrieval, and section 3 "The Parallel
 Dual Form" for the quadratic form.  ``groupnorm_gate`` (numpy) is the block step after the
-cell: per-head group normalisation and the output gate.  Pins against closed forms, exact
+cell: per-head group normalisation and the output gate.  ``recurrent_backward`` (numpy) gives
+the gradients of the forward, walked backwards in time.  Pins against closed forms, exact
 rational arithmetic and library routines are in ``tests/test_oracle_pins.py``.
 
 Parity pinning: every routine here is pinned (no routine is "parity unpinned").
@@ -196,3 +197,87 @@ def groupnorm_gate(h, o_pre, gamma, beta, eps=1e-5):
     norm = (h - mu) / np.sqrt(var + eps)
     gate = 1.0 / (1.0 + np.exp(-o))
     return gate * (g * norm + b)
+
+
+def _log_forget_np(fg, forget):
+    return fg if forget == "exp" else -np.logaddexp(0.0, -fg)
+
+
+def recurrent_backward(q, k, v, ig, fg, dh, C0=None, n0=None, m0=None, forget="sigmoid"):
+    """Gradients of L = sum_t dh_t . h_t through the stabilised recurrent cell, fp64, numpy.
+
+    The cell's h_t = C_t q_t / max(|n_t^T q_t|, exp(-m_t)) equals the unstabilised
+    C~_t q_t / max(|n~_t^T q_t|, 1) (page section 2: the stabiliser rescales C and n by
+    exp(-m_t)), so its gradients are those of the unstabilised recurrence of section 3
+    (C~_t = f_t C~_{t-1} + i_t v_t k^_t^T, n~_t = f_t n~_{t-1} + i_t k^_t), walked backwards
+    in time.  They are carried here in the stabilised frame: G_t = dL/dC~_t * exp(m_t) and
+    N_t = dL/dn~_t * exp(m_t), so that every factor is the forward's alpha_t or w_t:
+        G_t += dh_t q_t^T / D_t,  N_t += -(dh_t . h_t) / D_t * s_t q_t,
+        (D_t = max(|n_t^T q_t|, exp(-m_t)), s_t = sign(n_t^T q_t) where |n_t^T q_t| > exp(-m_t),
+         else 0: the floor does not depend on q or n)
+        dq_t = C_t^T dh_t / D_t - (dh_t . h_t) / D_t * s_t n_t
+        dv_t = w_t G_t k^_t,   dk_t = w_t (G_t^T v_t + N_t) / sqrt(d),
+        di~_t = w_t (v_t^T G_t k^_t + N_t . k^_t),
+        df~_t = alpha_t (<G_t, C_{t-1}> + N_t . n_{t-1}) * (1 - f_t)   (sigmoid gate; f = exp: * 1)
+        G_{t-1} += alpha_t G_t,  N_{t-1} += alpha_t N_t.
+    With an initial state (C0, n0, m0) (stabilised), also dC0 = G_0, dn0 = N_0 and
+    dm0 = <G_0, C0> + N_0 . n0.  Returns a dict of those arrays.  Where |n_t^T q_t| equals
+    exp(-m_t) exactly the function has a kink and this is one of its one-sided derivatives."""
+    q, k, v, ig, fg, dh = (np.asarray(x, np.float64) for x in (q, k, v, ig, fg, dh))
+    B, NH, S, DQK, DV = _shapes(q, k, v, ig, fg)
+    scale = 1.0 / np.sqrt(DQK)
+    out = {x: np.zeros_like(y) for x, y in (("dq", q), ("dk", k), ("dv", v), ("dig", ig), ("dfg", fg))}
+    init = C0 is not None
+    if init:
+        C0 = np.asarray(C0, np.float64).reshape(B, NH, DV, DQK)
+        n0 = np.asarray(n0, np.float64).reshape(B, NH, DQK)
+        m0 = np.asarray(m0, np.float64).reshape(B, NH)
+        out["dC0"] = np.zeros_like(C0)
+        out["dn0"] = np.zeros_like(n0)
+        out["dm0"] = np.zeros_like(m0)
+    for b in range(B):
+        for hh in range(NH):
+            # forward, keeping every state and the per-token factors
+            C = C0[b, hh].copy() if init else np.zeros((DV, DQK))
+            n = n0[b, hh].copy() if init else np.zeros(DQK)
+            m = float(m0[b, hh]) if init else 0.0
+            Cs, ns, al, ws, fs, ms = [C.copy()], [n.copy()], [], [], [], []
+            for t in range(S):
+                lf = _log_forget_np(fg[b, hh, t], forget)
+                m_new = max(lf + m, ig[b, hh, t])
+                a_t = np.exp(lf + m - m_new)
+                w_t = np.exp(ig[b, hh, t] - m_new)
+                kh = k[b, hh, t] * scale
+                C = a_t * C + w_t * np.outer(v[b, hh, t], kh)
+                n = a_t * n + w_t * kh
+                m = m_new
+                Cs.append(C.copy()); ns.append(n.copy())
+                al.append(a_t); ws.append(w_t); fs.append(np.exp(lf)); ms.append(m)
+            G = np.zeros((DV, DQK))
+            N = np.zeros(DQK)
+            for t in range(S - 1, -1, -1):
+                Ct, nt, qt = Cs[t + 1], ns[t + 1], q[b, hh, t]
+                a = float(nt @ qt)
+                floor_ = np.exp(-ms[t])
+                D = max(abs(a), floor_)
+                h = Ct @ qt / D
+                g_h = dh[b, hh, t]
+                s_t = np.sign(a) if abs(a) > floor_ else 0.0
+                dD_scaled = -float(g_h @ h) / D
+                out["dq"][b, hh, t] = Ct.T @ g_h / D + dD_scaled * s_t * nt
+                G += np.outer(g_h, qt) / D
+                N += dD_scaled * s_t * qt
+                kh = k[b, hh, t] * scale
+                vt = v[b, hh, t]
+                out["dv"][b, hh, t] = ws[t] * (G @ kh)
+                out["dk"][b, hh, t] = ws[t] * (G.T @ vt + N) * scale
+                out["dig"][b, hh, t] = ws[t] * (float(vt @ G @ kh) + float(N @ kh))
+                gate = (1.0 - fs[t]) if forget != "exp" else 1.0
+                out["dfg"][b, hh, t] = al[t] * (float(np.sum(G * Cs[t])) + float(N @ ns[t])) * gate
+                G = al[t] * G
+                N = al[t] * N
+            if init:
+                out["dC0"][b, hh] = G
+                out["dn0"][b, hh] = N
+                out["dm0"][b, hh] = float(np.sum(G * C0[b, hh])) + float(N @ n0[b, hh])
+    return out

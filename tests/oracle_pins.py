@@ -350,6 +350,67 @@ def pin_groupnorm_gate_invariants(lib):
     return err <= 1e-13, f"group norm / gate invariants err {err:.3e}"
 
 
+# ---------------------------------------------------------------- backward
+def _fd_grads(fwd_loss, arrays, eps=1e-6):
+    """Central differences of a scalar function of several arrays, element by element."""
+    out = []
+    for i, arr in enumerate(arrays):
+        g = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            plus = [a.copy() for a in arrays]
+            minus = [a.copy() for a in arrays]
+            plus[i][idx] += eps
+            minus[i][idx] -= eps
+            g[idx] = (fwd_loss(*plus) - fwd_loss(*minus)) / (2 * eps)
+        out.append(g)
+    return out
+
+
+def _backward_case(lib, forget, seed, init, qscale=1.0):
+    rng = np.random.default_rng(seed)
+    B, NH, S, DQK, DV = 1, 2, 6, 4, 3
+    q = qscale * rng.standard_normal((B, NH, S, DQK))
+    k = rng.standard_normal((B, NH, S, DQK))
+    v = rng.standard_normal((B, NH, S, DV))
+    ig = 1.2 * rng.standard_normal((B, NH, S))
+    fg = (rng.normal(1.0, 1.5, (B, NH, S)) if forget == "sigmoid" else rng.normal(-0.1, 0.3, (B, NH, S)))
+    dh = rng.standard_normal((B, NH, S, DV))
+    arrays = [q, k, v, ig, fg]
+    if init:
+        arrays += [0.4 * rng.standard_normal((B, NH, DV, DQK)), 0.4 * rng.standard_normal((B, NH, DQK)),
+                   rng.uniform(-1.0, 1.5, (B, NH))]
+
+    def loss(*a):
+        kw = dict(C0=a[5], n0=a[6], m0=a[7]) if init else {}
+        return float(np.sum(oracle.recurrent(*a[:5], lib=lib, forget=forget, **kw)["h"] * dh))
+
+    fd = _fd_grads(loss, arrays)
+    kw = dict(C0=arrays[5], n0=arrays[6], m0=arrays[7]) if init else {}
+    g = oracle.recurrent_backward(*arrays[:5], dh, forget=forget, **kw)
+    names = ["dq", "dk", "dv", "dig", "dfg"] + (["dC0", "dn0", "dm0"] if init else [])
+    return max(rel(g[nm], f) for nm, f in zip(names, fd))
+
+
+def pin_backward_finite_differences(lib):
+    """Gradients of sum_t dh_t . h_t w.r.t. q, k, v, i~, f~ and the initial state (C0, n0, m0),
+    against central differences of the C oracle's forward (a separate implementation)."""
+    err = max(_backward_case(lib, "sigmoid", 51, False), _backward_case(lib, "sigmoid", 52, True))
+    return err <= 1e-7, f"backward vs finite differences rel err {err:.3e}"
+
+
+def pin_backward_exp_forget_finite_differences(lib):
+    """The same for the exponential forget gate (df~ = alpha (<G, C_{t-1}> + N . n_{t-1}))."""
+    err = max(_backward_case(lib, "exp", 53, False), _backward_case(lib, "exp", 54, True))
+    return err <= 1e-7, f"exp-gate backward vs finite differences rel err {err:.3e}"
+
+
+def pin_backward_floor_branch(lib):
+    """Small q: the floor exp(-m_t) decides the denominator on most rows, where it carries no
+    gradient to q or n; the analytic gradients still match central differences."""
+    err = _backward_case(lib, "sigmoid", 55, False, qscale=0.05)
+    return err <= 1e-7, f"floor-branch backward vs finite differences rel err {err:.3e}"
+
+
 ALL_PINS = [
     pin_recurrent_equals_parallel,
     pin_stabiliser_is_a_rescaling,
@@ -368,6 +429,9 @@ ALL_PINS = [
     pin_exp_forget_two_token_scalar,
     pin_groupnorm_matches_torch,
     pin_groupnorm_gate_invariants,
+    pin_backward_finite_differences,
+    pin_backward_exp_forget_finite_differences,
+    pin_backward_floor_branch,
 ]
 
 
