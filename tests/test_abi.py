@@ -163,3 +163,32 @@ def test_groupnorm_gate_argument_errors(lib):
     assert gn(gamma=None, S=0) == ERR_NULL
     assert gn(h=FAKE + 8) == ERR_ALIGN
 
+
+def test_header_is_plain_c(lib, tmp_path):
+    """include/mlstm.h compiles as C99 (no C++ in the boundary) and every declaration links
+    against the library."""
+    import shutil
+    import subprocess
+    if not shutil.which("gcc"):
+        pytest.skip("gcc not found")
+    src = tmp_path / "abi.c"
+    names = declared_functions()
+    src.write_text('#include "mlstm.h"\n#include <stdio.h>\n'
+                   "int main(void) {\n"
+                   + "".join(f'  printf("%p\\n", (void *){n});\n' for n in names)
+                   + "  return mlstm_status_str(MLSTM_OK)[0] == 'M' ? 0 : 1;\n}\n")
+    lib_dir = os.path.join(ROOT, "mlstm_matrix_memory_02_b300")
+    exe = tmp_path / "abi"
+    res = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                          "-L", lib_dir, "-lmlstm_b300", f"-Wl,-rpath,{lib_dir}", "-o", str(exe)],
+                         capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
+
+
+def test_forget_gate_codes():
+    from mlstm_matrix_memory_02_b300 import binding as B
+    assert B._dt_code(torch.float32) == 0 and B._dt_code(torch.bfloat16) == 1
+    assert B._dt_code(torch.bfloat16, "exp") == 1 | B.FORGET_EXP
+    with pytest.raises(ValueError):
+        B._dt_code(torch.float32, "tanh")
+
