@@ -154,6 +154,17 @@ mlstm_status mlstm_fwd_gates(const float *igate_pre, const float *fgate_pre, int
 mlstm_status mlstm_fwd_check(const void *workspace, size_t ws_bytes, int B, int NH, int S, int DQK,
                              int DV, int chunk, mlstm_dtype dt, void *stream);
 
+/* Exercises the failure path of the bounded device-side waits (no counterpart on the pages; a
+ * test hook for the fault handling): launches one CTA that runs the fused forward's wait on a
+ * barrier nothing ever completes.  After about a second the wait gives up and records
+ * MLSTM_SELFTEST_WAIT_CODE in the error word of `workspace` (a forward workspace for these
+ * sizes), exactly as a forward's wait would; mlstm_fwd_check on the same workspace then returns
+ * MLSTM_ERR_TIMEOUT and mlstm_last_cuda_error() the code.  Nothing faults, traps or hangs, and
+ * the device stays usable.  Do not run it while a forward uses the same workspace. */
+#define MLSTM_SELFTEST_WAIT_CODE 90
+mlstm_status mlstm_wait_selftest(void *workspace, size_t ws_bytes, int B, int NH, int S, int DQK, int DV,
+                                 int chunk, mlstm_dtype dt, void *stream);
+
 /* One recurrent decode step for every (batch, head), in place (section 5 "Inference
  * Memory and Throughput Trade-Offs"; section 2 stabiliser; section 3 updates):
  *   q, k [B, NH, DQK] (dt), v [B, NH, DV] (dt), ig, fg [B, NH] float32 pre-activations

@@ -31,6 +31,8 @@ _lib.mlstm_status_str.restype = ctypes.c_char_p
 _lib.mlstm_status_str.argtypes = [_i]
 _lib.mlstm_last_cuda_error.restype = _i
 _lib.mlstm_last_cuda_error.argtypes = []
+_lib.mlstm_wait_selftest.restype = _i
+_lib.mlstm_wait_selftest.argtypes = [_vp, _sz, _i, _i, _i, _i, _i, _i, _i, _vp]
 _lib.mlstm_groupnorm_gate.restype = _i
 _lib.mlstm_groupnorm_gate.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _i, _i, _i, _i, _i, _i, _i, _vp]
 _lib.mlstm_kernel_launches.restype = ctypes.c_ulonglong
@@ -66,7 +68,9 @@ _lib.mlstm_fwd_chunkwise_noalloc.argtypes = [_vp, _vp, _vp, _fp, _fp, _i, _i, _i
 EXPORTED = ["mlstm_status_str", "mlstm_last_cuda_error", "mlstm_kernel_launches",
             "mlstm_fwd_workspace_bytes", "mlstm_fwd_chunkwise", "mlstm_fwd_from_gates",
             "mlstm_fwd_chunk_states", "mlstm_fwd_gates", "mlstm_fwd_check", "mlstm_fwd_path",
-            "mlstm_step", "mlstm_step_multi", "mlstm_fwd_chunkwise_noalloc", "mlstm_groupnorm_gate"]
+            "mlstm_step", "mlstm_step_multi", "mlstm_fwd_chunkwise_noalloc", "mlstm_groupnorm_gate",
+            "mlstm_wait_selftest"]
+SELFTEST_WAIT_CODE = 90
 
 # Bytes of the fixed scratch array behind mlstm_fwd_chunkwise_noalloc (include/mlstm.h).
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -371,3 +375,13 @@ def mlstm_groupnorm_gate(h, o_pre, gamma, beta, eps=1e-5, out=None, y_dtype=None
                                      _stream(stream))
     _check(code, "mlstm_groupnorm_gate")
     return out
+
+
+def mlstm_wait_selftest(workspace, B, NH, S, DQK, DV, chunk, dtype=torch.bfloat16, stream=None):
+    """Run one bounded device-side wait that nothing completes (about a second); it records
+    SELFTEST_WAIT_CODE in ``workspace``'s error word, so that mlstm_fwd_check on the same
+    workspace raises MlstmError with code 7 (MLSTM_ERR_TIMEOUT)."""
+    code = _lib.mlstm_wait_selftest(_ptr(workspace), workspace.numel(), B, NH, S, DQK, DV, chunk, _DT[dtype],
+                                    _stream(stream))
+    _check(code, "mlstm_wait_selftest")
+

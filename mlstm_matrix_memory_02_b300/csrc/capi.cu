@@ -343,6 +343,21 @@ mlstm_status mlstm_fwd_check(const void *workspace, size_t ws_bytes, int B, int 
   return MLSTM_OK;
 }
 
+mlstm_status mlstm_wait_selftest(void *workspace, size_t ws_bytes, int B, int NH, int S, int DQK, int DV,
+                                 int chunk, mlstm_dtype dt, void *stream) {
+  bool exp_fg;
+  dt = split_forget(dt, exp_fg);
+  if (dt != MLSTM_F32 && dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
+  if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return MLSTM_ERR_SHAPE;
+  if (!workspace) return MLSTM_ERR_NULL;
+  if (!aligned16(workspace)) return MLSTM_ERR_ALIGN;
+  const Layout Lw = layout(B, NH, S, DQK, DV, chunk, dt);
+  if (ws_bytes < Lw.gates_end) return MLSTM_ERR_WORKSPACE;
+  if (mlstm_status st = check_device()) return st;
+  return launch_status(launch_wait_selftest((int *)((char *)workspace + Lw.err), MLSTM_SELFTEST_WAIT_CODE,
+                                            (cudaStream_t)stream));
+}
+
 mlstm_status mlstm_step(const void *q, const void *k, const void *v, const float *ig, const float *fg,
                         float *C, float *n, float *m, void *h, int B, int NH, int DQK, int DV,
                         mlstm_dtype dt, mlstm_dtype h_dt, void *stream) {

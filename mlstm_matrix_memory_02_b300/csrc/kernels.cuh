@@ -53,6 +53,10 @@ cudaError_t launch_groupnorm_gate(const void *h, bool h_bf16, const void *o_pre,
                                   const float *beta, float eps, void *y, bool y_bf16, int B, int NH, int S, int DV,
                                   cudaStream_t stream);
 
+// One bounded device-side wait on a barrier nothing completes: gives up after about a second and
+// records `code` in *err (the failure path of every wait of the fused forward).
+cudaError_t launch_wait_selftest(int *err, int code, cudaStream_t stream);
+
 // small helpers
 cudaError_t launch_copy_chunk_m(const float *cm, int P, int NC, float *m_last, cudaStream_t stream);
 

@@ -192,3 +192,13 @@ def test_forget_gate_codes():
     with pytest.raises(ValueError):
         B._dt_code(torch.float32, "tanh")
 
+
+def test_wait_selftest_argument_errors(lib):
+    p = ctypes.c_void_p
+    st = lib.mlstm_wait_selftest
+    assert st(p(None), ctypes.c_size_t(1 << 20), 1, 2, 128, 128, 128, 64, 1, p(None)) == ERR_NULL
+    assert st(p(FAKE), ctypes.c_size_t(1 << 20), 1, 2, 128, 128, 128, 64, 5, p(None)) == ERR_DTYPE
+    assert st(p(FAKE), ctypes.c_size_t(1 << 20), 1, 2, 100, 128, 128, 64, 1, p(None)) == ERR_SHAPE
+    assert st(p(FAKE + 4), ctypes.c_size_t(1 << 20), 1, 2, 128, 128, 128, 64, 1, p(None)) == ERR_ALIGN
+    assert st(p(FAKE), ctypes.c_size_t(8), 1, 2, 128, 128, 128, 64, 1, p(None)) == ERR_WS
+

@@ -456,6 +456,28 @@ def test_error_codes_do_not_launch(B):
     assert bool((h == 7).all() and (C == 7).all() and (n == 7).all() and (m == 7).all())
 
 
+# ----------------------------------------------------------------------------- failure detection
+def test_bounded_wait_reports_timeout(B):
+    """The failure path of the forward's device-side waits, made without a fault: a wait on a
+    barrier nothing completes gives up after about a second, the host reads MLSTM_ERR_TIMEOUT
+    with that wait's code, and the device stays usable (a forward on the same workspace clears
+    the word, checks clean and matches the oracle)."""
+    b, nh, s, dqk, dv = 1, 2, 128, 128, 128
+    ws = B.alloc_workspace(b, nh, s, dqk, dv, 64)
+    B.mlstm_wait_selftest(ws, b, nh, s, dqk, dv, 64)
+    with pytest.raises(B.MlstmError) as e:
+        B.mlstm_fwd_check(ws, b, nh, s, dqk, dv, 64)
+    assert e.value.code == 7
+    assert B.library().mlstm_last_cuda_error() == B.SELFTEST_WAIT_CODE
+    w = W.LAYER_350M.with_(B=b, NH=nh, S=s, DQK=dqk, DV=dv)
+    inp = W.make_inputs(w)
+    d = dev(inp, torch.bfloat16)
+    h, _, _, _ = B.mlstm_fwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], 64, h_dtype=torch.float32,
+                                       workspace=ws)
+    B.mlstm_fwd_check(ws, b, nh, s, dqk, dv, 64)
+    assert rel_err(npy(h), oracle.recurrent(**inp)["h"]) <= TOL_BF16
+
+
 # ----------------------------------------------------------------------------- exponential forget gate
 def exp_forget_inputs(inp, seed=7):
     """Pre-activations for the exponential gate f = exp(f~): log sigmoid of the workload's
