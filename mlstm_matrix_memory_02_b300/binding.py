@@ -133,7 +133,9 @@ def mlstm_fwd_workspace_bytes(B, NH, S, DQK, DV, chunk, dtype=torch.bfloat16) ->
 
 
 def mlstm_fwd_path(B, NH, S, DQK, DV, chunk, dtype=torch.bfloat16) -> int:
-    """1: fused tensor-core kernel, 0: CUDA-core kernels, -1: unsupported."""
+    """Kernels mlstm_fwd_chunkwise runs for these sizes: 1 = the fused tensor-core kernel,
+    2 = the same with each head's d_qk split over a CTA pair, 0 = the CUDA-core kernels,
+    -1 = unsupported sizes or dtype."""
     return int(_lib.mlstm_fwd_path(B, NH, S, DQK, DV, chunk, _DT[dtype]))
 
 
