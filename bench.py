@@ -191,7 +191,12 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(sel), "sampled": where}
 
 
-def dist_setup():
+def dist_setup(timeout_s: float | None = None):
+    """Process group from the torchrun environment.  Collectives (the barriers and the timing
+    reduction) give up after `timeout_s` (default 600 s, or MLSTM_PG_TIMEOUT_S), so that a rank
+    that died or never joined ends the others with an error instead of holding their GPUs."""
+    import datetime
+
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -199,7 +204,9 @@ def dist_setup():
     if world > 1:
         import torch.distributed as dist
         backend = "nccl" if torch.cuda.is_available() else "gloo"
-        dist.init_process_group(backend=backend)
+        if timeout_s is None:
+            timeout_s = float(os.environ.get("MLSTM_PG_TIMEOUT_S", "600"))
+        dist.init_process_group(backend=backend, timeout=datetime.timedelta(seconds=timeout_s))
     return rank, local, world
 
 

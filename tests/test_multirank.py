@@ -7,6 +7,7 @@ import os
 import socket
 import subprocess
 import sys
+import time
 
 import torch.multiprocessing as mp
 
@@ -54,3 +55,33 @@ def test_reference_arm_under_torchrun_prints_once():
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
+
+
+def _worker_dead_peer(rank, world, port, out):
+    os.environ.update({"RANK": str(rank), "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank),
+                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    sys.path.insert(0, ROOT)
+    import bench
+    bench.dist_setup(timeout_s=15)
+    if rank == 1:
+        return  # this rank leaves before the barrier: it never joins the collective
+    t0 = time.time()
+    try:
+        bench.barrier(world)
+        bench.max_over_ranks(1.0, world)
+        out[rank] = ("no error", time.time() - t0)
+    except Exception as e:  # the surviving rank must learn of the missing peer
+        out[rank] = (type(e).__name__, time.time() - t0)
+
+
+def test_dead_rank_is_detected_not_waited_for():
+    """A rank that exits between steps: the other rank's next collective fails within the
+    process-group timeout (15 s here) instead of waiting for it."""
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_worker_dead_peer, args=(2, port, out), nprocs=2, join=True)
+        kind, waited = out[0]
+        assert kind != "no error"
+        assert waited < 60, waited
+
