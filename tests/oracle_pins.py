@@ -411,6 +411,21 @@ def pin_backward_floor_branch(lib):
     return err <= 1e-7, f"floor-branch backward vs finite differences rel err {err:.3e}"
 
 
+def pin_exp_forget_golden_fixture(lib):
+    """The stored exact case (f = sigmoid(0) = 1/2, i = 1) through the exponential gate with
+    f~ = log(1/2): the same exact values, to rounding."""
+    with open(os.path.join(GOLDEN, "exact_rational_case.json")) as f:
+        g = json.load(f)
+    q, k, v = (np.array(g[x], np.float64) for x in ("q", "k", "v"))
+    ig = np.array(g["ig"], np.float64)
+    fg = np.full_like(ig, np.log(0.5))
+    out = oracle.recurrent(q, k, v, ig, fg, lib=lib, forget="exp")
+    hx = np.array([[float(Fraction(x)) for x in row] for row in g["h"]])
+    Cx = np.array([[float(Fraction(x)) for x in row] for row in g["C_last"]])
+    err = max(rel(out["h"][0, 0], hx), rel(out["C"][0, 0], Cx))
+    return err <= 1e-14, f"exp-gate golden fixture err {err:.3e}"
+
+
 ALL_PINS = [
     pin_recurrent_equals_parallel,
     pin_stabiliser_is_a_rescaling,
@@ -427,6 +442,7 @@ ALL_PINS = [
     pin_exp_forget_dual_form,
     pin_exp_forget_equals_sigmoid_in_log_space,
     pin_exp_forget_two_token_scalar,
+    pin_exp_forget_golden_fixture,
     pin_groupnorm_matches_torch,
     pin_groupnorm_gate_invariants,
     pin_backward_finite_differences,
