@@ -202,3 +202,22 @@ def test_wait_selftest_argument_errors(lib):
     assert st(p(FAKE + 4), ctypes.c_size_t(1 << 20), 1, 2, 128, 128, 128, 64, 1, p(None)) == ERR_ALIGN
     assert st(p(FAKE), ctypes.c_size_t(8), 1, 2, 128, 128, 128, 64, 1, p(None)) == ERR_WS
 
+
+def test_forward_path_selection(lib):
+    """Which kernels mlstm_fwd_chunkwise runs, decided on the host: the fused tensor-core kernel
+    for bf16 inputs with S a multiple of 64, d_qk in {64..512} (powers of two) and d_v a
+    multiple of 128, whatever chunk is asked for; the CTA pair for d_qk = 512 or when one CTA
+    per d_v tile would leave SMs idle; the CUDA-core kernels otherwise."""
+    path = lib.mlstm_fwd_path
+    assert path(4, 4, 2048, 512, 512, 64, 1) == 2          # 1.3B-style layer
+    assert path(8, 4, 1024, 256, 256, 64, 1) == 2          # 350M-style layer: 64 tiles < 148 SMs
+    assert path(1, 8, 16384, 256, 256, 128, 1) == 2        # stress layer asks for chunk 128
+    assert path(2, 80, 64, 128, 128, 64, 1) == 1           # 160 tiles: one CTA each
+    assert path(1, 2, 64, 64, 128, 64, 1) == 1             # d_qk = 64: never split
+    assert path(1, 2, 96, 128, 128, 32, 1) == 0            # S not a multiple of 64
+    assert path(1, 2, 128, 96, 128, 64, 1) == 0            # d_qk not a power of two
+    assert path(1, 2, 128, 128, 96, 64, 1) == 0            # d_v not a multiple of 128
+    assert path(4, 4, 2048, 512, 512, 64, 0) == 0          # fp32 inputs
+    assert path(4, 4, 2048, 512, 512, 64, 1 | 0x100) == 2  # the forget-gate flag changes nothing
+    assert path(1, 2, 100, 64, 64, 64, 1) == -1            # S % chunk != 0
+
