@@ -89,10 +89,17 @@ unsigned long long mlstm_kernel_launches(void);
  * preprocessing of the asked-for chunk) and the CUDA-core kernels otherwise. */
 int mlstm_fwd_path(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt);
 
-/* Bytes of device workspace mlstm_fwd_chunkwise / mlstm_fwd_chunk_states need for these
- * sizes (0 if the sizes are unsupported).  The workspace holds the per-token gate
- * prefix sums, the per-chunk stabiliser and, on paths that materialise them, the
- * chunk-boundary states.  Its contents are scratch: nothing is read back by the caller. */
+/* Bytes of device workspace mlstm_fwd_chunkwise, mlstm_fwd_chunk_states and mlstm_fwd_gates
+ * need for these sizes (0 if the sizes are unsupported), on the path mlstm_fwd_chunkwise takes
+ * (mlstm_fwd_path): the fused tensor-core kernel materialises no boundary states, so its
+ * workspace is small whatever chunk is asked for; the CUDA-core kernels keep every
+ * chunk-boundary state.  The workspace holds the wait-error word at offset 0, the per-token
+ * gate prefix sums, the per-chunk stabiliser and, on the CUDA-core path, the boundary states.
+ * Its contents are scratch: nothing is read back by the caller except through mlstm_fwd_check.
+ * mlstm_fwd_from_gates takes the fused kernel only for chunk 64; for another chunk on sizes
+ * the fused kernel would take, it runs the CUDA-core kernels and needs their larger workspace,
+ * which mlstm_fwd_workspace_bytes(..., MLSTM_F32) returns (the layout does not depend on the
+ * element type). */
 size_t mlstm_fwd_workspace_bytes(int B, int NH, int S, int DQK, int DV, int chunk,
                                  mlstm_dtype dt);
 
@@ -148,19 +155,22 @@ mlstm_status mlstm_fwd_gates(const float *igate_pre, const float *fgate_pre, int
                              int S, int chunk, const float *m_init, float *m_tok,
                              float *m_states, void *workspace, size_t ws_bytes, void *stream);
 
-/* Synchronises `stream` and reports whether the last forward that used `workspace` (with
- * these sizes) completed every bounded device-side wait: MLSTM_OK, or MLSTM_ERR_TIMEOUT when a
- * kernel gave up waiting (mlstm_last_cuda_error() then returns the kernel's wait code). */
+/* Synchronises `stream` and reports whether the last forward that used `workspace` completed
+ * every bounded device-side wait: MLSTM_OK, or MLSTM_ERR_TIMEOUT when a kernel gave up waiting
+ * (mlstm_last_cuda_error() then returns the kernel's wait code).  The word it reads sits at
+ * offset 0 of every forward workspace and every forward clears it before its kernels run, so
+ * the answer concerns the last forward whatever its path or chunk; the size arguments are only
+ * validated, and ws_bytes must be at least 256. */
 mlstm_status mlstm_fwd_check(const void *workspace, size_t ws_bytes, int B, int NH, int S, int DQK,
                              int DV, int chunk, mlstm_dtype dt, void *stream);
 
 /* Exercises the failure path of the bounded device-side waits (no counterpart on the pages; a
  * test hook for the fault handling): launches one CTA that runs the fused forward's wait on a
  * barrier nothing ever completes.  After about a second the wait gives up and records
- * MLSTM_SELFTEST_WAIT_CODE in the error word of `workspace` (a forward workspace for these
- * sizes), exactly as a forward's wait would; mlstm_fwd_check on the same workspace then returns
- * MLSTM_ERR_TIMEOUT and mlstm_last_cuda_error() the code.  Nothing faults, traps or hangs, and
- * the device stays usable.  Do not run it while a forward uses the same workspace. */
+ * MLSTM_SELFTEST_WAIT_CODE in the error word (offset 0) of `workspace`, exactly as a forward's
+ * wait would; mlstm_fwd_check on the same workspace then returns MLSTM_ERR_TIMEOUT and
+ * mlstm_last_cuda_error() the code.  Nothing faults, traps or hangs, and the device stays
+ * usable.  Do not run it while a forward uses the same workspace.  ws_bytes >= 256. */
 #define MLSTM_SELFTEST_WAIT_CODE 90
 mlstm_status mlstm_wait_selftest(void *workspace, size_t ws_bytes, int B, int NH, int S, int DQK, int DV,
                                  int chunk, mlstm_dtype dt, void *stream);
@@ -218,9 +228,13 @@ mlstm_status mlstm_groupnorm_gate(const void *h, const void *o_pre, const float 
  * that loads the library holds until the process exits.  Nothing is allocated by the call:
  * no cudaMalloc, no cudaFree, no allocating library routine.
  *   - Sizes whose mlstm_fwd_workspace_bytes(...) exceeds MLSTM_NOALLOC_SCRATCH_BYTES are
- *     rejected with MLSTM_ERR_WORKSPACE before anything is launched (the 1.3B-style layer,
- *     B=4 NH=4 S=2048 d=512 bf16 chunk 64, needs about 0.43 MB; sizes that take the CUDA-core
- *     path and materialise boundary states fit only when small).
+ *     rejected with MLSTM_ERR_WORKSPACE before anything is launched.  That is the workspace of
+ *     the path the forward takes: the 1.3B-style layer (B=4 NH=4 S=2048 d=512 bf16 chunk 64)
+ *     needs about 0.43 MB and the long-context layer (B=1 NH=8 S=16384 d=256 bf16 chunk 128)
+ *     about 1.6 MB; sizes that take the CUDA-core path materialise boundary states and fit
+ *     only when small.
+ *   - A bounded device-side wait that gave up inside this forward is reported, as for the
+ *     workspace forward, by mlstm_fwd_check_noalloc (below).
  *   - The first call on a device resolves the array's device address on that device (with
  *     it current, cudaGetSymbolAddress); make that first call before any stream capture.
  *   - Every call in the process shares the one array: calls whose work may overlap on the
@@ -236,6 +250,20 @@ mlstm_status mlstm_fwd_chunkwise_noalloc(const void *q, const void *k, const voi
                                          const float *n_init, const float *m_init, void *h,
                                          mlstm_dtype h_dt, float *C_last, float *n_last,
                                          float *m_last, void *stream);
+
+/* mlstm_fwd_check for the forward without allocation (no counterpart on the pages): synchronises
+ * `stream` and reports whether the last mlstm_fwd_chunkwise_noalloc on the current device
+ * completed every bounded device-side wait (MLSTM_OK or MLSTM_ERR_TIMEOUT, as mlstm_fwd_check).
+ * It reads the error word of the library's fixed scratch array and allocates nothing. */
+mlstm_status mlstm_fwd_check_noalloc(void *stream);
+
+/* The device address (and, if `bytes` is not NULL, the size, MLSTM_NOALLOC_SCRATCH_BYTES) of
+ * the fixed scratch array behind mlstm_fwd_chunkwise_noalloc on the current device (no
+ * counterpart on the pages).  The first query on a device resolves the address, with that
+ * device current, as the first forward call would.  The array belongs to the library: a caller
+ * may read it (or point mlstm_wait_selftest at it to exercise mlstm_fwd_check_noalloc), but
+ * anything it writes there may be overwritten by the next forward without allocation. */
+mlstm_status mlstm_noalloc_scratch(void **ptr, size_t *bytes);
 
 #ifdef __cplusplus
 }

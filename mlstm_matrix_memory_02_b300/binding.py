@@ -64,12 +64,16 @@ _lib.mlstm_step_multi.argtypes = [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _vp, _
 _lib.mlstm_fwd_chunkwise_noalloc.restype = _i
 _lib.mlstm_fwd_chunkwise_noalloc.argtypes = [_vp, _vp, _vp, _fp, _fp, _i, _i, _i, _i, _i, _i, _i,
                                              _fp, _fp, _fp, _vp, _i, _fp, _fp, _fp, _vp]
+_lib.mlstm_fwd_check_noalloc.restype = _i
+_lib.mlstm_fwd_check_noalloc.argtypes = [_vp]
+_lib.mlstm_noalloc_scratch.restype = _i
+_lib.mlstm_noalloc_scratch.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(_sz)]
 
 EXPORTED = ["mlstm_status_str", "mlstm_last_cuda_error", "mlstm_kernel_launches",
             "mlstm_fwd_workspace_bytes", "mlstm_fwd_chunkwise", "mlstm_fwd_from_gates",
             "mlstm_fwd_chunk_states", "mlstm_fwd_gates", "mlstm_fwd_check", "mlstm_fwd_path",
             "mlstm_step", "mlstm_step_multi", "mlstm_fwd_chunkwise_noalloc", "mlstm_groupnorm_gate",
-            "mlstm_wait_selftest"]
+            "mlstm_wait_selftest", "mlstm_fwd_check_noalloc", "mlstm_noalloc_scratch"]
 SELFTEST_WAIT_CODE = 90
 
 # Bytes of the fixed scratch array behind mlstm_fwd_chunkwise_noalloc (include/mlstm.h).
@@ -248,6 +252,19 @@ def mlstm_fwd_chunkwise_noalloc(q, k, v, igate_pre, fgate_pre, chunk, out, C_ini
         _ptr(C_last), _ptr(n_last), _ptr(m_last), _stream(stream))
     _check(code, "mlstm_fwd_chunkwise_noalloc")
     return h, C_last, n_last, m_last
+
+
+def mlstm_fwd_check_noalloc(stream=None):
+    """Synchronises the stream and raises MlstmError (MLSTM_ERR_TIMEOUT) if a bounded
+    device-side wait of the last forward without allocation on this device gave up."""
+    _check(_lib.mlstm_fwd_check_noalloc(_stream(stream)), "mlstm_fwd_check_noalloc")
+
+
+def mlstm_noalloc_scratch():
+    """(device address, bytes) of the library's fixed scratch array on the current device."""
+    ptr, n = ctypes.c_void_p(), _sz()
+    _check(_lib.mlstm_noalloc_scratch(ctypes.byref(ptr), ctypes.byref(n)), "mlstm_noalloc_scratch")
+    return int(ptr.value), int(n.value)
 
 
 def mlstm_kernel_launches() -> int:

@@ -8,6 +8,7 @@ from __future__ import annotations
 
 import glob
 import os
+import shutil
 import subprocess
 import sys
 from concurrent.futures import ThreadPoolExecutor
@@ -17,7 +18,23 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(ROOT, "_build", "obj")
 LIB = os.path.join(PKG, "libmlstm_b300.so")
-NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
+
+
+def _find_nvcc() -> str:
+    """nvcc from $NVCC, else $CUDA_HOME/bin, else PATH."""
+    if os.environ.get("NVCC"):
+        return os.environ["NVCC"]
+    home = os.environ.get("CUDA_HOME") or os.environ.get("CUDA_PATH")
+    if home and os.path.exists(os.path.join(home, "bin", "nvcc")):
+        return os.path.join(home, "bin", "nvcc")
+    found = shutil.which("nvcc")
+    if not found:
+        raise RuntimeError("nvcc not found: set NVCC or CUDA_HOME, or put nvcc on PATH")
+    return found
+
+
+NVCC = _find_nvcc()
+CUDA_LIB = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(NVCC))), "lib64")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", f"-I{os.path.join(ROOT, 'include')}"]
@@ -55,7 +72,7 @@ def build(verbose_ptxas: bool = False, clean: bool = False) -> str:
     if (not os.path.exists(LIB) or clean
             or max(os.path.getmtime(o) for o in objs) > os.path.getmtime(LIB)):
         cmd = [NVCC, *ARCH, "-shared", "-cudart", "shared", "-Xlinker",
-               "-rpath,/usr/local/cuda/lib64", "-o", LIB, *objs]
+               f"-rpath,{CUDA_LIB}", "-o", LIB, *objs]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{res.stdout}\n{res.stderr}")

@@ -28,7 +28,7 @@ constexpr int kMaxPairs = 65535;  // grid.z limit of the output kernel
 inline size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t gb, gx, gu, cm, err, Cs, ns, ncopy, gates_end, total;
+  size_t err, gb, gx, gu, cm, Cs, ns, ncopy, gates_end, total;
   bool tc;  // the forward runs on the fused tensor-core kernel (no materialised states)
 };
 
@@ -47,16 +47,19 @@ bool sizes_ok(int B, int NH, int S, int DQK, int DV, int chunk) {
   return true;
 }
 
+// Workspace layout for the kernels of one chunk size.  The wait-error word of the kernels with
+// bounded waits sits at offset 0 of every layout, so that mlstm_fwd_check finds it whatever path
+// or chunk a forward took.
 Layout layout(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) {
   const size_t P = (size_t)B * NH, NC = (size_t)S / chunk;
   Layout L{};
   L.tc = use_tc(B, NH, S, DQK, DV, chunk, dt);
   size_t off = 0;
+  L.err = off; off = round_up(off + sizeof(int));
   L.gb = off; off = round_up(off + P * S * sizeof(float));
   L.gx = off; off = round_up(off + P * S * sizeof(float));
   L.gu = off; off = round_up(off + P * S * sizeof(float));
   L.cm = off; off = round_up(off + P * (NC + 1) * sizeof(float));
-  L.err = off; off = round_up(off + sizeof(int));
   L.gates_end = off;
   const size_t states = L.tc ? 0 : P * (NC + 1);
   L.Cs = off; off = round_up(off + states * DV * DQK * sizeof(float));
@@ -66,6 +69,19 @@ Layout layout(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) 
   L.ncopy = off; off = round_up(off + (L.tc ? P * DQK : 0) * sizeof(float));
   L.total = off;
   return L;
+}
+
+// Bytes that mlstm_fwd_chunkwise (and mlstm_fwd_chunk_states, mlstm_fwd_gates) need on the
+// path the forward actually takes: the fused kernel runs in its own chunks of kTcChunk tokens
+// whatever chunk is asked for, and needs no boundary states; the gate stage of the asked-for
+// chunk must still fit (mlstm_fwd_chunk_states and mlstm_fwd_gates use it).
+size_t fwd_need(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) {
+  if (use_tc(B, NH, S, DQK, DV, kTcChunk, dt)) {
+    const size_t tc = layout(B, NH, S, DQK, DV, kTcChunk, dt).total;
+    const size_t gates = layout(B, NH, S, DQK, DV, chunk, dt).gates_end;
+    return tc > gates ? tc : gates;
+  }
+  return layout(B, NH, S, DQK, DV, chunk, dt).total;
 }
 
 inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
@@ -87,6 +103,21 @@ mlstm_status launch_status(cudaError_t e, int kernels = 1) {
   }
   g_last_cuda_error = (int)e;
   return MLSTM_ERR_LAUNCH;
+}
+
+// Synchronises `s`, then reads the wait-error word at offset 0 of a forward workspace.
+mlstm_status read_error_word(const void *workspace, cudaStream_t s) {
+  int word = 0;
+  if (cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    g_last_cuda_error = (int)cudaGetLastError();
+    return MLSTM_ERR_LAUNCH;
+  }
+  if (word != 0) {
+    g_last_cuda_error = word;  // the code of the wait that gave up
+    return MLSTM_ERR_TIMEOUT;
+  }
+  return MLSTM_OK;
 }
 
 mlstm_status check_device() {
@@ -142,7 +173,7 @@ size_t mlstm_fwd_workspace_bytes(int B, int NH, int S, int DQK, int DV, int chun
   dt = split_forget(dt, exp_fg);
   if (dt != MLSTM_F32 && dt != MLSTM_BF16) return 0;
   if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return 0;
-  return layout(B, NH, S, DQK, DV, chunk, dt).total;
+  return fwd_need(B, NH, S, DQK, DV, chunk, dt);
 }
 
 static mlstm_status check_init(const float *C_init, const float *n_init, const float *m_init) {
@@ -156,7 +187,7 @@ static mlstm_status check_fwd_args(const void *q, const void *k, const void *v, 
                                    int DQK, int DV, int chunk, mlstm_dtype dt, const float *C_init,
                                    const float *n_init, const void *h, mlstm_dtype h_dt,
                                    const float *C_last, const float *n_last, const float *m_last,
-                                   const void *workspace, size_t ws_bytes) {
+                                   const void *workspace, size_t ws_bytes, size_t ws_need) {
   if (dt != MLSTM_F32 && dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
   if (h_dt != MLSTM_F32 && h_dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
   if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return MLSTM_ERR_SHAPE;
@@ -167,7 +198,7 @@ static mlstm_status check_fwd_args(const void *q, const void *k, const void *v, 
   for (const void *ptr : {q, k, v, h, (const void *)C_last, (const void *)n_last, (const void *)m_last, workspace})
     if (!aligned16(ptr)) return MLSTM_ERR_ALIGN;
   if ((C_init && !aligned16(C_init)) || (n_init && !aligned16(n_init))) return MLSTM_ERR_ALIGN;
-  if (ws_bytes < layout(B, NH, S, DQK, DV, chunk, dt).total) return MLSTM_ERR_WORKSPACE;
+  if (ws_bytes < ws_need) return MLSTM_ERR_WORKSPACE;
   return MLSTM_OK;
 }
 
@@ -181,6 +212,9 @@ static mlstm_status run_from_gates(const void *q, const void *k, const void *v, 
                                    const float *ig = nullptr, const float *fg = nullptr,
                                    const float *m_init = nullptr, bool exp_fg = false) {
   const Layout Lw = layout(B, NH, S, DQK, DV, chunk, dt);
+  // The wait-error word reports on this forward only.  The fused kernel clears it itself (its
+  // first CTA, long before any bounded wait could give up); the CUDA-core kernels have no
+  // bounded waits, so it is cleared here.
   char *ws = (char *)workspace;
   float *gb = (float *)(ws + Lw.gb), *gx = (float *)(ws + Lw.gx), *gu = (float *)(ws + Lw.gu);
   float *cm = (float *)(ws + Lw.cm), *Cs = (float *)(ws + Lw.Cs), *ns = (float *)(ws + Lw.ns);
@@ -197,6 +231,7 @@ static mlstm_status run_from_gates(const void *q, const void *k, const void *v, 
     return launch_status(launch_fwd_tc(q, k, v, h_dt == MLSTM_BF16, gb, gx, gu, cm, ig, fg, m_init, P, S, DQK,
                                        DV, C_init, n_init, h, C_last, n_last, m_last, err, s, exp_fg));
   }
+  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return launch_status(cudaGetLastError());
   if (mlstm_status st = launch_status(launch_states_simt(k, v, bf16, gb, gx, cm, P, S, chunk, DQK, DV, C_init,
                                                          n_init, Cs, ns, C_last, n_last, s)))
     return st;
@@ -216,7 +251,10 @@ mlstm_status mlstm_fwd_from_gates(const void *q, const void *k, const void *v, i
   bool exp_fg;  // the variant is that of the gates already in the workspace
   dt = split_forget(dt, exp_fg);
   if (mlstm_status st = check_fwd_args(q, k, v, B, NH, S, DQK, DV, chunk, dt, C_init, n_init, h, h_dt,
-                                       C_last, n_last, m_last, workspace, ws_bytes))
+                                       C_last, n_last, m_last, workspace, ws_bytes,
+                                       sizes_ok(B, NH, S, DQK, DV, chunk) && (dt == MLSTM_F32 || dt == MLSTM_BF16)
+                                           ? layout(B, NH, S, DQK, DV, chunk, dt).total
+                                           : 0))
     return st;
   if (mlstm_status st = check_device()) return st;
   return run_from_gates(q, k, v, B, NH, S, DQK, DV, chunk, dt, C_init, n_init, h, h_dt, C_last, n_last,
@@ -232,7 +270,10 @@ mlstm_status mlstm_fwd_chunkwise(const void *q, const void *k, const void *v, co
   bool exp_fg;
   dt = split_forget(dt, exp_fg);
   if (mlstm_status st = check_fwd_args(q, k, v, B, NH, S, DQK, DV, chunk, dt, C_init, n_init, h, h_dt,
-                                       C_last, n_last, m_last, workspace, ws_bytes))
+                                       C_last, n_last, m_last, workspace, ws_bytes,
+                                       sizes_ok(B, NH, S, DQK, DV, chunk) && (dt == MLSTM_F32 || dt == MLSTM_BF16)
+                                           ? fwd_need(B, NH, S, DQK, DV, chunk, dt)
+                                           : 0))
     return st;
   if (S > 0 && (!igate_pre || !fgate_pre)) return MLSTM_ERR_NULL;
   if (mlstm_status st = check_init(C_init, n_init, m_init)) return st;
@@ -326,21 +367,9 @@ mlstm_status mlstm_fwd_check(const void *workspace, size_t ws_bytes, int B, int 
   if (dt != MLSTM_F32 && dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
   if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return MLSTM_ERR_SHAPE;
   if (!workspace) return MLSTM_ERR_NULL;
-  const Layout Lw = layout(B, NH, S, DQK, DV, chunk, dt);
-  if (ws_bytes < Lw.gates_end) return MLSTM_ERR_WORKSPACE;
+  if (ws_bytes < kAlign) return MLSTM_ERR_WORKSPACE;  // the error word's header
   if (mlstm_status st = check_device()) return st;
-  int word = 0;
-  cudaStream_t s = (cudaStream_t)stream;
-  if (cudaMemcpyAsync(&word, (const char *)workspace + Lw.err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      cudaStreamSynchronize(s) != cudaSuccess) {
-    g_last_cuda_error = (int)cudaGetLastError();
-    return MLSTM_ERR_LAUNCH;
-  }
-  if (word != 0) {
-    g_last_cuda_error = word;  // the code of the wait that gave up
-    return MLSTM_ERR_TIMEOUT;
-  }
-  return MLSTM_OK;
+  return read_error_word(workspace, (cudaStream_t)stream);
 }
 
 mlstm_status mlstm_wait_selftest(void *workspace, size_t ws_bytes, int B, int NH, int S, int DQK, int DV,
@@ -351,11 +380,9 @@ mlstm_status mlstm_wait_selftest(void *workspace, size_t ws_bytes, int B, int NH
   if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return MLSTM_ERR_SHAPE;
   if (!workspace) return MLSTM_ERR_NULL;
   if (!aligned16(workspace)) return MLSTM_ERR_ALIGN;
-  const Layout Lw = layout(B, NH, S, DQK, DV, chunk, dt);
-  if (ws_bytes < Lw.gates_end) return MLSTM_ERR_WORKSPACE;
+  if (ws_bytes < kAlign) return MLSTM_ERR_WORKSPACE;  // the error word's header
   if (mlstm_status st = check_device()) return st;
-  return launch_status(launch_wait_selftest((int *)((char *)workspace + Lw.err), MLSTM_SELFTEST_WAIT_CODE,
-                                            (cudaStream_t)stream));
+  return launch_status(launch_wait_selftest((int *)workspace, MLSTM_SELFTEST_WAIT_CODE, (cudaStream_t)stream));
 }
 
 mlstm_status mlstm_step(const void *q, const void *k, const void *v, const float *ig, const float *fg,
@@ -417,6 +444,29 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[MLSTM_NOALLOC_S
 
 static void *g_noalloc_ptr[64];  // device address of g_noalloc_scratch, per device ordinal
 
+// The array's device address on the current device, resolved on first use (set-up, once per
+// device, with that device current).
+static mlstm_status noalloc_scratch_ptr(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    g_last_cuda_error = (int)cudaGetLastError();
+    return MLSTM_ERR_DEVICE;
+  }
+  if (dev < 0 || dev >= 64) return MLSTM_ERR_DEVICE;
+  void *scratch = __atomic_load_n(&g_noalloc_ptr[dev], __ATOMIC_ACQUIRE);
+  if (scratch == nullptr) {
+    const cudaError_t e = cudaGetSymbolAddress(&scratch, g_noalloc_scratch);
+    if (e != cudaSuccess || scratch == nullptr) {
+      g_last_cuda_error = (int)e;
+      cudaGetLastError();
+      return MLSTM_ERR_LAUNCH;
+    }
+    __atomic_store_n(&g_noalloc_ptr[dev], scratch, __ATOMIC_RELEASE);
+  }
+  *out = scratch;
+  return MLSTM_OK;
+}
+
 mlstm_status mlstm_fwd_chunkwise_noalloc(const void *q, const void *k, const void *v,
                                          const float *igate_pre, const float *fgate_pre, int B,
                                          int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt,
@@ -428,27 +478,12 @@ mlstm_status mlstm_fwd_chunkwise_noalloc(const void *q, const void *k, const voi
   const mlstm_dtype bare = split_forget(dt, exp_fg);  // dt itself (variant included) is passed on
   if (bare != MLSTM_F32 && bare != MLSTM_BF16) return MLSTM_ERR_DTYPE;
   if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return MLSTM_ERR_SHAPE;
-  // sizes whose scratch would not fit in the fixed array are refused before anything runs
-  if (layout(B, NH, S, DQK, DV, chunk, bare).total > (size_t)MLSTM_NOALLOC_SCRATCH_BYTES)
-    return MLSTM_ERR_WORKSPACE;
+  // sizes whose scratch (on the path the forward takes) would not fit in the fixed array are
+  // refused before anything runs
+  if (fwd_need(B, NH, S, DQK, DV, chunk, bare) > (size_t)MLSTM_NOALLOC_SCRATCH_BYTES) return MLSTM_ERR_WORKSPACE;
   if (mlstm_status st = check_device()) return st;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    g_last_cuda_error = (int)cudaGetLastError();
-    return MLSTM_ERR_DEVICE;
-  }
-  if (dev < 0 || dev >= 64) return MLSTM_ERR_DEVICE;
-  // set-up, once per device, with that device current: the array's device address
-  void *scratch = __atomic_load_n(&g_noalloc_ptr[dev], __ATOMIC_ACQUIRE);
-  if (scratch == nullptr) {
-    const cudaError_t e = cudaGetSymbolAddress(&scratch, g_noalloc_scratch);
-    if (e != cudaSuccess || scratch == nullptr) {
-      g_last_cuda_error = (int)e;
-      cudaGetLastError();
-      return MLSTM_ERR_LAUNCH;
-    }
-    __atomic_store_n(&g_noalloc_ptr[dev], scratch, __ATOMIC_RELEASE);
-  }
+  void *scratch = nullptr;
+  if (mlstm_status st = noalloc_scratch_ptr(&scratch)) return st;
   // Everything the forward reads from its workspace is written by the same call first (the
   // gate arrays, the chunk stabiliser, the copy of n_init) and the one word that must start
   // at zero (the kernels' wait-error word) is cleared by the forward itself, so the stale
@@ -456,6 +491,21 @@ mlstm_status mlstm_fwd_chunkwise_noalloc(const void *q, const void *k, const voi
   return mlstm_fwd_chunkwise(q, k, v, igate_pre, fgate_pre, B, NH, S, DQK, DV, chunk, dt, C_init,
                              n_init, m_init, h, h_dt, C_last, n_last, m_last, scratch,
                              (size_t)MLSTM_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+mlstm_status mlstm_fwd_check_noalloc(void *stream) {
+  if (mlstm_status st = check_device()) return st;
+  void *scratch = nullptr;
+  if (mlstm_status st = noalloc_scratch_ptr(&scratch)) return st;
+  return read_error_word(scratch, (cudaStream_t)stream);
+}
+
+mlstm_status mlstm_noalloc_scratch(void **ptr, size_t *bytes) {
+  if (!ptr) return MLSTM_ERR_NULL;
+  if (mlstm_status st = check_device()) return st;
+  if (mlstm_status st = noalloc_scratch_ptr(ptr)) return st;
+  if (bytes) *bytes = (size_t)MLSTM_NOALLOC_SCRATCH_BYTES;
+  return MLSTM_OK;
 }
 
 }  // extern "C"

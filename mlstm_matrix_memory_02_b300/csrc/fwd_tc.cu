@@ -46,64 +46,11 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#ifdef MLSTM_TRACE
-// poll iterations of the bounded waits, per warp of CTA (0, 0)
-__device__ unsigned long long g_polls[32];
-#define MLSTM_POLL_HOOK()                                                                               \
-  do {                                                                                                  \
-    if (blockIdx.x == 0 && blockIdx.y == 0 && (threadIdx.x & 31) == 0) atomicAdd(&g_polls[threadIdx.x >> 5], 1ull); \
-  } while (0)
-#endif
 #include "common.cuh"
 #include "kernels.cuh"
 #include "sm100.cuh"
 #include "tmap.cuh"
 
-// Optional timeline trace for performance analysis (build with -DMLSTM_TRACE): the SM clock at
-// fixed points of every role of CTA (0, 0), per chunk; read back with mlstm_trace_read.
-#ifdef MLSTM_TRACE
-__device__ long long g_trace[2][8][512][8];
-#define TRACE(role, k, ev)                                                                            \
-  do {                                                                                                \
-    if (blockIdx.x < 2 && blockIdx.y == 0 && (k) < 512) g_trace[blockIdx.x][role][k][ev] = clock64(); \
-  } while (0)
-// per CTA: global timer at entry and exit, SM id
-__device__ unsigned long long g_span[2048][3];
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ unsigned smid() {
-  unsigned r;
-  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
-  return r;
-}
-#define SPAN(ev)                                                          \
-  do {                                                                    \
-    const unsigned b_ = blockIdx.y * gridDim.x + blockIdx.x;              \
-    if (b_ < 2048) {                                                      \
-      g_span[b_][ev] = global_ns();                                       \
-      if ((ev) == 0) g_span[b_][2] = smid();                              \
-    }                                                                     \
-  } while (0)
-extern "C" int mlstm_trace_read(long long *dst, size_t bytes) {
-  return (int)cudaMemcpyFromSymbol(dst, g_trace, bytes < sizeof(g_trace) ? bytes : sizeof(g_trace));
-}
-extern "C" int mlstm_polls_read(unsigned long long *dst) {
-  return (int)cudaMemcpyFromSymbol(dst, g_polls, sizeof(g_polls));
-}
-extern "C" int mlstm_span_read(unsigned long long *dst, size_t bytes) {
-  return (int)cudaMemcpyFromSymbol(dst, g_span, bytes < sizeof(g_span) ? bytes : sizeof(g_span));
-}
-#else
-#define TRACE(role, k, ev) \
-  do {                     \
-  } while (0)
-#define SPAN(ev) \
-  do {           \
-  } while (0)
-#endif
 
 namespace mlstm {
 namespace {
@@ -244,7 +191,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
   // second, long after the first CTA has started).
   if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) *(volatile int *)err = 0;
   if (threadIdx.x == 0) {
-    SPAN(0);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.qk_full[i], 1);
       mbar_init(&sm.qk_empty[i], 1);  // committed after the state update that last reads the stage
@@ -290,7 +236,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
   tc_fence_after();
   if (PAIR) cluster_sync();  // the partner's barriers are initialised before any remote access
   const uint32_t tm = sm.tmem_base;
-  if (threadIdx.x == 0) TRACE(0, 511, 0);
 
   if (warp == 0) {
     // ------------------------------------------------------------------ MMA issuer: S and P V
@@ -307,7 +252,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
           if (!mbar_wait(&sm.qk_full[s], (k >> 1) & 1, err, 12, abort_ptr)) break;
           if (k >= 1 && !mbar_wait(&sm.sfree, (k - 1) & 1, err, 13, abort_ptr)) break;
           tc_fence_after();
-          TRACE(1, k, 0);
           const uint64_t dq_raw = smem_desc(smem_u32(STQ(s)), 16, 1024, kSwizzle128B);
           const uint64_t dk_raw = smem_desc(smem_u32(STK(s)), 16, 1024, kSwizzle128B);
 #pragma unroll 1
@@ -322,7 +266,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
           if (!mbar_wait(&sm.pready, kp & 1, err, 17, abort_ptr)) break;
           if (!mbar_wait(&sm.bar_X, kp & 1, err, 9, abort_ptr)) break;
           tc_fence_after();
-          TRACE(1, kp, 4);
           const uint64_t dv = smem_desc(smem_u32(STV(kp & 1)), 8192, 1024, kSwizzle128B);
 #pragma unroll 1
           for (int kk = 0; kk < kL / 16; ++kk)
@@ -370,7 +313,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       prefetch_tensormap(&mapK);
       auto load_qk = [&](int kk) {
         const int s = kk & 1, row = p * S + kk * kL;
-        TRACE(0, kk, 0);
         mbar_arrive_expect_tx(&sm.qk_full[s], (uint32_t)(2 * QB));
 #pragma unroll 1
         for (int kb = 0; kb < DH / 64; ++kb) {
@@ -390,7 +332,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
         if (!mbar_wait(&sm.xready[s], (k >> 1) & 1, err, 15, abort_ptr)) break;
         if (k >= 1 && !mbar_wait(&sm.hfree, (k - 1) & 1, err, 16, abort_ptr)) break;
         tc_fence_after();
-        TRACE(1, k, 1);
         const uint64_t dq_b = smem_desc(smem_u32(STQ(s)), 16, 1024, kSwizzle128B);
 #pragma unroll 1
         for (int kk = 0; kk < DH / 16; ++kk)
@@ -399,7 +340,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
         mma_commit(&sm.bar_X);
         if (!mbar_wait(&sm.kready[s], (k >> 1) & 1, err, 10, abort_ptr)) break;
         tc_fence_after();
-        TRACE(1, k, 2);
         const uint64_t dv = smem_desc(smem_u32(STV(s)), 8192, 1024, kSwizzle128B);
         const uint64_t dk_w = smem_desc(smem_u32(STK(s)), 8192, 1024, kSwizzle128B);
 #pragma unroll 1
@@ -511,7 +451,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       sigma = sig_next;
       __syncwarp();
       if (lane == 0) {
-        TRACE(2, k, 0);
         mbar_arrive(&sm.g_full[s]);
       }
     }
@@ -539,7 +478,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       const int s = kk & 1, par = kk & 1;
       if (!mbar_wait(&sm.g_full[s], (kk >> 1) & 1, err, 21, abort_ptr)) return false;
       if (!mbar_wait(&sm.bar_S[kk & 1], (kk >> 1) & 1, err, 22, abort_ptr)) return false;
-      if (t == 0) TRACE(3, kk, 0);
       tc_fence_after();
       uint32_t u[2][32];
       tmem_ld32(tm + lane_base + kColS, u[0]);
@@ -573,7 +511,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
                         __uint_as_float(u[c >> 3][(4 * c + 3) & 31]), rbar);
         }
       }
-      if (t == 0) TRACE(6, kk, 1);
       return true;
     };
 
@@ -583,7 +520,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       const int s = kk & 1;
       if (!mbar_wait(&sm.qk_full[s], (kk >> 1) & 1, err, 36, abort_ptr)) return false;
       if (kk >= 1 && !mbar_wait(&sm.npart_free, (kk - 1) & 1, err, 37, abort_ptr)) return false;
-      if (t == 0) TRACE(7, kk, 0);
       const Gate &g = sm.g[s];
       uint8_t *const kb = STK(s);
       // rows in batches of four: every load of a batch is issued before its stores
@@ -622,7 +558,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
 #pragma unroll
       for (int e = 0; e < 4; ++e) *reinterpret_cast<uint64_t *>(&sm.npart[krg * DH + kcc * 8 + 2 * e]) = acc[e];
       fence_proxy_async_smem();
-      if (t == 0) TRACE(7, kk, 1);
       mbar_arrive(&sm.kready[kk & 1]);
       return true;
     };
@@ -637,7 +572,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
         }
         if (!mbar_wait_cluster(&sm.sx_full[par], (kk >> 1) & 1, err, 25, abort_ptr)) return false;
         if (!mbar_wait_cluster(&sm.nqx_full[par], (kk >> 1) & 1, err, 30, abort_ptr)) return false;
-        if (t == 0) TRACE(3, kk, 1);
       }
       if (!mbar_wait(&sm.bar_nq[par], (kk >> 1) & 1, err, 23, abort_ptr)) return false;
       // P of the previous chunk has been read by its P V product (which may run after S of this chunk)
@@ -712,7 +646,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
         }
       }
       fence_proxy_async_smem();
-      if (t == 0) TRACE(3, kk, 2);
       mbar_arrive(&sm.pready);
       mbar_arrive(&sm.inv_ready[par]);
       return true;
@@ -733,7 +666,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       const size_t tok0 = (size_t)p * S + (size_t)k * kL;
       // H^T of chunk k: send the partner's columns, keep this CTA's rows, free the accumulator
       if (!mbar_wait(&sm.bar_H, k & 1, err, 26, abort_ptr)) { ok = false; break; }
-      if (t == 0) TRACE(3, k, 3);
       tc_fence_after();
       float own[NR];
       if (PAIR) {
@@ -769,11 +701,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       }
       tc_fence_before();
       mbar_arrive(&sm.hfree);
-      if (t == 0) TRACE(6, k, 6);
       if (PAIR) {
         if (t == 0) mbar_arrive_expect_tx(&sm.hx_full, 128 * 32 * 4);
         if (!mbar_wait_cluster(&sm.hx_full, k & 1, err, 28, abort_ptr)) { ok = false; break; }
-        if (t == 0) TRACE(3, k, 4);
         const float *src = HX + t * 32;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -788,12 +718,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       }
       // 1/den of every row of chunk k (warpgroup 1)
       if (!mbar_wait(&sm.inv_ready[par], (k >> 1) & 1, err, 29, abort_ptr)) { ok = false; break; }
-      if (t == 0) TRACE(6, k, 7);
       TO *hp = h + (tok0 + r_lo) * DV + a0 + t;
 #pragma unroll
       for (int i = 0; i < NR; ++i) hp[(size_t)i * DV] = from_f32<TO>(own[i] * sm.inv[par][r_lo + i]);
       mbar_arrive(&sm.inv_free[par]);
-      if (t == 0) TRACE(3, k, 5);
     }
     if (!ok) set_abort(sm);
   } else if (warp >= 8 && warp < 12) {
@@ -809,14 +737,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       tmem_st16(tm + lane_base + c, r);
     }
     tmem_wait_st();
-    if (t == 0) TRACE(4, 511, 0);
     float sig_last = 0.f;
     bool ok = true;
     for (int k = 0; k < NC; ++k) {
       const int s = k & 1;
       if (!mbar_wait(&sm.g_full[s], (k >> 1) & 1, err, 40, abort_ptr)) { ok = false; break; }
       if (k >= 1 && !mbar_wait(&sm.bar_U, (k - 1) & 1, err, 32, abort_ptr)) { ok = false; break; }
-      if (t == 0) TRACE(4, k, 0);
       tc_fence_after();
       const Gate &g = sm.g[s];
       const float fr_c = g.fr_c, fr_w = g.fr_w;
@@ -872,14 +798,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       }
       tmem_wait_st();
       tc_fence_before();
-      if (t == 0) TRACE(4, k, 1);
       mbar_arrive(&sm.cready);
     }
     if (ok && atile == 0 && rank == 0 && t == 0) m_last[p] = sm.m_fin;
     if (!ok) set_abort(sm);
     // final state C_last = exp(sigma) T, transposed through shared memory for coalesced stores
     if (ok && !mbar_wait(&sm.bar_U, (NC - 1) & 1, err, 33, abort_ptr)) ok = false;
-    if (t == 0) TRACE(4, 511, 1);
     if (ok) {
       // C_last = exp(sigma) T, 32 columns at a time through two swizzled staging tiles
       // [128 rows x 128 bytes] in the (now unused) q/k stages, stored by TMA
@@ -908,7 +832,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
         }
       }
       if (t == 0) bulk_wait_all();
-      if (t == 0) TRACE(4, 511, 2);
     } else {
       set_abort(sm);
     }
@@ -935,7 +858,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
         dst[c] = alpha_prev * src[c] + a;
       }
       mbar_arrive(&sm.npart_free);
-      if (t == 0) TRACE(7, kk, 2);
       return true;
     };
     bool ok = group_sync(&sm.grp[2], gph, err, 50, abort_ptr);
@@ -967,7 +889,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
       // raw q of the stage has landed and the S product has read it
       if (!mbar_wait(&sm.qk_full[s], (k >> 1) & 1, err, 52, abort_ptr)) { ok = false; break; }
       if (!mbar_wait(&sm.bar_S[k & 1], (k >> 1) & 1, err, 56, abort_ptr)) { ok = false; break; }
-      if (t == 0) TRACE(5, k, 0);
       const Gate &g = sm.g[s];
       alpha_prev = g.alpha;
       uint8_t *const qb = STQ(s);
@@ -1022,10 +943,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
           sm.nq[par][qr] = part;
         }
       }
-      if (t == 0) TRACE(5, k, 1);
       mbar_arrive(&sm.bar_nq[par]);
       fence_proxy_async_smem();
-      if (t == 0) TRACE(5, k, 2);
       mbar_arrive(&sm.xready[k & 1]);
     }
     // n after the last chunk
@@ -1037,13 +956,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
 
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0) TRACE(0, 511, 1);
   if (PAIR) cluster_sync();  // no CTA leaves while its partner may still access its shared memory
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tm, 512);
   }
-  if (threadIdx.x == 0) SPAN(1);
 #undef STV
 }
 

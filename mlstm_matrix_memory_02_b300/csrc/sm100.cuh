@@ -48,23 +48,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // may suspend the thread for a short, hardware-chosen time); it gives up after about
 // kWaitCycles SM clocks (about one second), or as soon as *abort (when given) becomes non-zero,
 // records `code` in *err and returns false.
-#ifndef MLSTM_WAIT_MODE
-#define MLSTM_WAIT_MODE 1  // 0: try_wait with a suspend-time hint, 1: try_wait, 2: test_wait spin
-#endif
-constexpr uint32_t kSuspendNs = 20000;
 constexpr long long kWaitCycles = 1LL << 31;
 
+// One poll of a phase: try_wait may suspend the thread for a short, hardware-chosen time
+// before it answers.
 __device__ __forceinline__ bool mbar_poll(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
-#if MLSTM_WAIT_MODE == 0
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
-      : "memory");
-#elif MLSTM_WAIT_MODE == 1
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -72,15 +61,6 @@ __device__ __forceinline__ bool mbar_poll(uint64_t *bar, uint32_t parity) {
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
-#else
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-#endif
   return ok != 0;
 }
 // Non-blocking test of a phase (for loops that watch several barriers at once).
@@ -95,13 +75,9 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-#ifndef MLSTM_POLL_HOOK
-#define MLSTM_POLL_HOOK()
-#endif
 static __device__ __forceinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, int *err, int code, const int *abort) {
   const long long t0 = clock64();
   for (;;) {
-    MLSTM_POLL_HOOK();
     if (mbar_poll(bar, parity)) return true;
     if ((abort && *(const volatile int *)abort) || clock64() - t0 > kWaitCycles) {
       if (err) atomicCAS(err, 0, code);

@@ -72,6 +72,29 @@ def test_workspace_bytes(lib):
     assert ws(1, 1, 0, 64, 64, 64, 0) > 0         # empty sequence is allowed
 
 
+def test_workspace_bytes_follow_the_path_that_runs(lib):
+    """The fused kernel walks any asked-for chunk in its own chunks of 64 and keeps no boundary
+    state, so a bf16 forward asked for chunk 128 needs only the gate arrays of its chunk (for
+    mlstm_fwd_chunk_states and mlstm_fwd_gates) and the fused kernel's own small layout; fp32
+    inputs take the CUDA-core path and need every boundary state."""
+    ws = lib.mlstm_fwd_workspace_bytes
+    P, S = 8, 16384
+    assert lib.mlstm_fwd_path(1, 8, S, 256, 256, 128, 1) >= 1
+    gates128 = 3 * P * S * 4 + P * (S // 128 + 1) * 4
+    assert gates128 <= ws(1, 8, S, 256, 256, 128, 1) < 4 << 20
+    assert ws(1, 8, S, 256, 256, 128, 0) > P * (S // 128) * 256 * 256 * 4
+
+
+def test_noalloc_helpers_argument_errors(lib):
+    """mlstm_noalloc_scratch rejects a NULL output before touching the device; without a usable
+    device both no-allocation helpers report MLSTM_ERR_DEVICE instead of launching."""
+    assert lib.mlstm_noalloc_scratch(None, None) == ERR_NULL
+    if not torch.cuda.is_available():
+        ptr = ctypes.c_void_p()
+        assert lib.mlstm_noalloc_scratch(ctypes.byref(ptr), None) == ERR_DEVICE
+        assert lib.mlstm_fwd_check_noalloc(None) == ERR_DEVICE
+
+
 FAKE = 0x100000  # 16-byte aligned, never dereferenced: every call below fails validation
 
 

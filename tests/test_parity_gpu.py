@@ -478,6 +478,44 @@ def test_bounded_wait_reports_timeout(B):
     assert rel_err(npy(h), oracle.recurrent(**inp)["h"]) <= TOL_BF16
 
 
+def test_check_after_chunk128_tensor_core_forward(B):
+    """mlstm_fwd_check finds the wait-error word whatever chunk the forward was asked for: a bf16
+    forward asked for chunk 128 runs the fused kernel in its own 64-token chunks, and its check
+    is clean on a workspace whose every byte was 0xFF beforehand (sized by
+    mlstm_fwd_workspace_bytes for the path that runs, not for materialised chunk-128 states)."""
+    w = W.LAYER_350M.with_(B=1, NH=2, S=256, DQK=256, DV=256, chunk=128)
+    assert B.mlstm_fwd_path(w.B, w.NH, w.S, w.DQK, w.DV, w.chunk) >= 1
+    ws = B.alloc_workspace(w.B, w.NH, w.S, w.DQK, w.DV, w.chunk)
+    assert ws.numel() < 4 << 20
+    ws.fill_(255)
+    inp = W.make_inputs(w)
+    d = dev(inp, torch.bfloat16)
+    h, _, _, _ = B.mlstm_fwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], w.chunk,
+                                       h_dtype=torch.float32, workspace=ws)
+    B.mlstm_fwd_check(ws, w.B, w.NH, w.S, w.DQK, w.DV, w.chunk)
+    assert rel_err(npy(h), oracle.recurrent(**inp)["h"]) <= TOL_BF16
+
+
+def test_check_after_cuda_core_forward(B):
+    """The CUDA-core path clears the error word too: on a workspace filled with 0xFF, and on one
+    where a selftest left MLSTM_ERR_TIMEOUT, an fp32 forward checks clean afterwards."""
+    w = W.TINY_F32.with_(B=1, NH=2, S=64, DQK=32, DV=32, chunk=16)
+    inp = W.make_inputs(w)
+    d = dev(inp, torch.float32)
+    ws = B.alloc_workspace(w.B, w.NH, w.S, w.DQK, w.DV, w.chunk, torch.float32)
+    ws.fill_(255)
+    h, _, _, _ = B.mlstm_fwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], w.chunk, workspace=ws)
+    B.mlstm_fwd_check(ws, w.B, w.NH, w.S, w.DQK, w.DV, w.chunk, torch.float32)
+    B.mlstm_wait_selftest(ws, w.B, w.NH, w.S, w.DQK, w.DV, w.chunk, torch.float32)
+    with pytest.raises(B.MlstmError) as e:
+        B.mlstm_fwd_check(ws, w.B, w.NH, w.S, w.DQK, w.DV, w.chunk, torch.float32)
+    assert e.value.code == 7
+    h2, _, _, _ = B.mlstm_fwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], w.chunk, workspace=ws)
+    B.mlstm_fwd_check(ws, w.B, w.NH, w.S, w.DQK, w.DV, w.chunk, torch.float32)
+    assert torch.equal(h, h2)
+    assert rel_err(npy(h), oracle.recurrent(**inp)["h"]) <= TOL_F32
+
+
 # ----------------------------------------------------------------------------- exponential forget gate
 def exp_forget_inputs(inp, seed=7):
     """Pre-activations for the exponential gate f = exp(f~): log sigmoid of the workload's
