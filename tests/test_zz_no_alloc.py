@@ -54,7 +54,7 @@ def _case(case):
         return w, torch.bfloat16, TOL_BF16, 64, None
     if case == "tensor_core_chunk128":
         # asked for chunk 128, the fused kernel runs (in its own chunks of 64) on a small workspace
-        w = W.STRESS_16K.with_(B=1, NH=2, S=512)
+        w = W.LAYER_350M.with_(B=1, NH=2, S=512, chunk=128)
         return w, torch.bfloat16, TOL_BF16, 128, None
     w = W.TINY_F32.with_(B=2, NH=3, S=96, DQK=64, DV=32)
     g = torch.Generator(device="cuda").manual_seed(3)
