@@ -99,9 +99,34 @@ int mlstm_fwd_path(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype
  * mlstm_fwd_from_gates takes the fused kernel only for chunk 64; for another chunk on sizes
  * the fused kernel would take, it runs the CUDA-core kernels and needs their larger workspace,
  * which mlstm_fwd_workspace_bytes(..., MLSTM_F32) returns (the layout does not depend on the
- * element type). */
+ * element type).  On the fused path, sizes whose grid would leave most SMs idle (long
+ * sequences over few heads, see mlstm_fwd_segments) also get the sequence-parallel buffers:
+ * per head and segment one float32 state C, n, m for the segment's own map and one for its
+ * entering state (the long-context layer, B=1 NH=8 S=16384 d=256, about 18 MB in all). */
 size_t mlstm_fwd_workspace_bytes(int B, int NH, int S, int DQK, int DV, int chunk,
                                  mlstm_dtype dt);
+
+/* The least workspace mlstm_fwd_chunkwise accepts for these sizes (0 if unsupported): that of
+ * mlstm_fwd_workspace_bytes without the sequence-parallel buffers.  A workspace between the
+ * two runs the forward over whole sequences, one head at a time per CTA (or CTA pair). */
+size_t mlstm_fwd_workspace_min_bytes(int B, int NH, int S, int DQK, int DV, int chunk,
+                                     mlstm_dtype dt);
+
+/* How many segments of each head's sequence mlstm_fwd_chunkwise runs in parallel for these
+ * sizes with a workspace of `ws_bytes` (an addition of this library for long sequences over
+ * few heads; the pages' chunkwise form walks each sequence in one pass).  The segments'
+ * maps compose exactly -- section 3 "The Parallel Dual Form" (the state after a stretch of
+ * tokens is the sum of its tokens' decayed contributions, so stretches compose by an
+ * associative scan) and section 2 (the stabiliser recurrence is max-plus linear in m): a first
+ * pass runs every segment from the zero state with m = -inf (segment 0 from the caller's
+ * initial state), a scan forms the entering state of every segment and the final state, and
+ * a second pass reruns segments 1..G-1 from their entering states.  The result is the same
+ * function up to rounding.  Returns G = 1 (no split: the CUDA-core path, raw-gate-free
+ * mlstm_fwd_from_gates, grids that already fill the GPU, or a workspace without the buffers),
+ * a power of two G > 1 with S divisible by 64 G and at least 256 tokens per segment, or -1 for
+ * unsupported sizes or dtype.  The choice depends on the device's SM count. */
+int mlstm_fwd_segments(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt,
+                       size_t ws_bytes);
 
 /* Chunkwise forward of the mLSTM cell over a whole sequence (section 3 "The Parallel Dual
  * Form", chunked; section 2 stabiliser).
@@ -113,7 +138,9 @@ size_t mlstm_fwd_workspace_bytes(int B, int NH, int S, int DQK, int DV, int chun
  *   h      [B, NH, S, DV]  (h_dt) output: h~_t for every token
  *   C_last [B,NH,DV,DQK], n_last [B,NH,DQK], m_last [B,NH] float32 outputs: the state
  *       after the last token (may alias C_init/n_init/m_init for an in-place update).
- *   workspace: at least mlstm_fwd_workspace_bytes(...) bytes of device memory.
+ *   workspace: at least mlstm_fwd_workspace_min_bytes(...) bytes of device memory;
+ *       mlstm_fwd_workspace_bytes(...) bytes enable the sequence-parallel forward where it
+ *       applies (mlstm_fwd_segments).
  * S == 0 copies the initial state to the outputs. */
 mlstm_status mlstm_fwd_chunkwise(const void *q, const void *k, const void *v,
                                  const float *igate_pre, const float *fgate_pre, int B, int NH,
@@ -227,12 +254,15 @@ mlstm_status mlstm_groupnorm_gate(const void *h, const void *o_pre, const float 
  * of MLSTM_NOALLOC_SCRATCH_BYTES bytes inside the library's device image, which every GPU
  * that loads the library holds until the process exits.  Nothing is allocated by the call:
  * no cudaMalloc, no cudaFree, no allocating library routine.
- *   - Sizes whose mlstm_fwd_workspace_bytes(...) exceeds MLSTM_NOALLOC_SCRATCH_BYTES are
+ *   - Sizes whose mlstm_fwd_workspace_min_bytes(...) exceeds MLSTM_NOALLOC_SCRATCH_BYTES are
  *     rejected with MLSTM_ERR_WORKSPACE before anything is launched.  That is the workspace of
  *     the path the forward takes: the 1.3B-style layer (B=4 NH=4 S=2048 d=512 bf16 chunk 64)
  *     needs about 0.43 MB and the long-context layer (B=1 NH=8 S=16384 d=256 bf16 chunk 128)
  *     about 1.6 MB; sizes that take the CUDA-core path materialise boundary states and fit
- *     only when small.
+ *     only when small.  The array is passed on as a workspace of MLSTM_NOALLOC_SCRATCH_BYTES
+ *     bytes, so the sequence-parallel forward runs where its buffers fit in it
+ *     (mlstm_fwd_segments with that size says which) and the outputs are those of
+ *     mlstm_fwd_chunkwise with a workspace of that size.
  *   - A bounded device-side wait that gave up inside this forward is reported, as for the
  *     workspace forward, by mlstm_fwd_check_noalloc (below).
  *   - The first call on a device resolves the array's device address on that device (with

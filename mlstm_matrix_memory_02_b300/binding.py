@@ -52,6 +52,10 @@ _lib.mlstm_fwd_gates.restype = _i
 _lib.mlstm_fwd_gates.argtypes = [_fp, _fp, _i, _i, _i, _i, _fp, _fp, _fp, _vp, _sz, _vp]
 _lib.mlstm_fwd_path.restype = _i
 _lib.mlstm_fwd_path.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+_lib.mlstm_fwd_workspace_min_bytes.restype = _sz
+_lib.mlstm_fwd_workspace_min_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+_lib.mlstm_fwd_segments.restype = _i
+_lib.mlstm_fwd_segments.argtypes = [_i, _i, _i, _i, _i, _i, _i, _sz]
 _lib.mlstm_fwd_check.restype = _i
 _lib.mlstm_fwd_check.argtypes = [_vp, _sz, _i, _i, _i, _i, _i, _i, _i, _vp]
 _lib.mlstm_step.restype = _i
@@ -73,7 +77,8 @@ EXPORTED = ["mlstm_status_str", "mlstm_last_cuda_error", "mlstm_kernel_launches"
             "mlstm_fwd_workspace_bytes", "mlstm_fwd_chunkwise", "mlstm_fwd_from_gates",
             "mlstm_fwd_chunk_states", "mlstm_fwd_gates", "mlstm_fwd_check", "mlstm_fwd_path",
             "mlstm_step", "mlstm_step_multi", "mlstm_fwd_chunkwise_noalloc", "mlstm_groupnorm_gate",
-            "mlstm_wait_selftest", "mlstm_fwd_check_noalloc", "mlstm_noalloc_scratch"]
+            "mlstm_wait_selftest", "mlstm_fwd_check_noalloc", "mlstm_noalloc_scratch",
+            "mlstm_fwd_workspace_min_bytes", "mlstm_fwd_segments"]
 SELFTEST_WAIT_CODE = 90
 
 # Bytes of the fixed scratch array behind mlstm_fwd_chunkwise_noalloc (include/mlstm.h).
@@ -134,6 +139,18 @@ def _dev(t, name, dtype=None, shape=None):
 
 def mlstm_fwd_workspace_bytes(B, NH, S, DQK, DV, chunk, dtype=torch.bfloat16) -> int:
     return int(_lib.mlstm_fwd_workspace_bytes(B, NH, S, DQK, DV, chunk, _DT[dtype]))
+
+
+def mlstm_fwd_workspace_min_bytes(B, NH, S, DQK, DV, chunk, dtype=torch.bfloat16) -> int:
+    return int(_lib.mlstm_fwd_workspace_min_bytes(B, NH, S, DQK, DV, chunk, _DT[dtype]))
+
+
+def mlstm_fwd_segments(B, NH, S, DQK, DV, chunk, dtype=torch.bfloat16, ws_bytes=None) -> int:
+    """Segments of each head's sequence the forward runs in parallel with a workspace of
+    `ws_bytes` (default: mlstm_fwd_workspace_bytes for these sizes); 1 = none, -1 = unsupported."""
+    if ws_bytes is None:
+        ws_bytes = mlstm_fwd_workspace_bytes(B, NH, S, DQK, DV, chunk, dtype)
+    return int(_lib.mlstm_fwd_segments(B, NH, S, DQK, DV, chunk, _DT[dtype], ws_bytes))
 
 
 def mlstm_fwd_path(B, NH, S, DQK, DV, chunk, dtype=torch.bfloat16) -> int:

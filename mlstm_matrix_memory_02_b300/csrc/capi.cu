@@ -29,6 +29,11 @@ inline size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
   size_t err, gb, gx, gu, cm, Cs, ns, ncopy, gates_end, total;
+  // the sequence-parallel forward's buffers (G segments per head, the fused path only), after
+  // `total`: per (head, segment) the sum of log f, the segment's own state and stabiliser, and
+  // its entering state
+  size_t Bg, Cseg, nseg, mseg, Cin, nin, min, split_total;
+  int G;
   bool tc;  // the forward runs on the fused tensor-core kernel (no materialised states)
 };
 
@@ -68,16 +73,29 @@ Layout layout(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) 
   // which may alias n_init)
   L.ncopy = off; off = round_up(off + (L.tc ? P * DQK : 0) * sizeof(float));
   L.total = off;
+  L.G = L.tc && S > 0 ? fwd_tc_segments((int)P, S, DQK, DV) : 1;
+  const size_t PG = L.G > 1 ? P * L.G : 0;
+  L.Bg = off; off = round_up(off + PG * sizeof(float));
+  L.Cseg = off; off = round_up(off + PG * DV * DQK * sizeof(float));
+  L.nseg = off; off = round_up(off + PG * DQK * sizeof(float));
+  L.mseg = off; off = round_up(off + PG * sizeof(float));
+  L.Cin = off; off = round_up(off + PG * DV * DQK * sizeof(float));
+  L.nin = off; off = round_up(off + PG * DQK * sizeof(float));
+  L.min = off; off = round_up(off + PG * sizeof(float));
+  L.split_total = off;
   return L;
 }
 
 // Bytes that mlstm_fwd_chunkwise (and mlstm_fwd_chunk_states, mlstm_fwd_gates) need on the
 // path the forward actually takes: the fused kernel runs in its own chunks of kTcChunk tokens
 // whatever chunk is asked for, and needs no boundary states; the gate stage of the asked-for
-// chunk must still fit (mlstm_fwd_chunk_states and mlstm_fwd_gates use it).
-size_t fwd_need(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) {
+// chunk must still fit (mlstm_fwd_chunk_states and mlstm_fwd_gates use it).  With `split` the
+// fused path's size includes the sequence-parallel buffers (the size mlstm_fwd_workspace_bytes
+// reports); without, it is the least workspace the forward accepts.
+size_t fwd_need(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt, bool split = true) {
   if (use_tc(B, NH, S, DQK, DV, kTcChunk, dt)) {
-    const size_t tc = layout(B, NH, S, DQK, DV, kTcChunk, dt).total;
+    const Layout L = layout(B, NH, S, DQK, DV, kTcChunk, dt);
+    const size_t tc = split ? L.split_total : L.total;
     const size_t gates = layout(B, NH, S, DQK, DV, chunk, dt).gates_end;
     return tc > gates ? tc : gates;
   }
@@ -168,6 +186,24 @@ int mlstm_fwd_path(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype
   return fwd_tc_pair(B * NH, DQK, DV) ? 2 : 1;
 }
 
+size_t mlstm_fwd_workspace_min_bytes(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) {
+  bool exp_fg;
+  dt = split_forget(dt, exp_fg);
+  if (dt != MLSTM_F32 && dt != MLSTM_BF16) return 0;
+  if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return 0;
+  return fwd_need(B, NH, S, DQK, DV, chunk, dt, false);
+}
+
+int mlstm_fwd_segments(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt, size_t ws_bytes) {
+  bool exp_fg;
+  dt = split_forget(dt, exp_fg);
+  if (dt != MLSTM_F32 && dt != MLSTM_BF16) return -1;
+  if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return -1;
+  if (!use_tc(B, NH, S, DQK, DV, kTcChunk, dt)) return 1;
+  const Layout L = layout(B, NH, S, DQK, DV, kTcChunk, dt);
+  return L.G > 1 && ws_bytes >= L.split_total ? L.G : 1;
+}
+
 size_t mlstm_fwd_workspace_bytes(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) {
   bool exp_fg;
   dt = split_forget(dt, exp_fg);
@@ -202,25 +238,59 @@ static mlstm_status check_fwd_args(const void *q, const void *k, const void *v, 
   return MLSTM_OK;
 }
 
+// The fused forward over G segments of each head's sequence at once, for long sequences over
+// few heads: a first pass runs every segment (segment 0 from the caller's initial state, the
+// others from the zero state with m = -inf), a scan composes the segments' maps into the true
+// entering state of every segment and the final state, and a second pass reruns segments
+// 1..G-1 from their entering states, overwriting their h.  Each (head, segment) is a head of
+// S / G tokens to the fused kernel: the token-major arrays need no copies.
+static mlstm_status run_segments(const void *q, const void *k, const void *v, const Layout &Lw, int P, int S,
+                                 int DQK, int DV, const float *C_init, const float *n_init, const float *m_init,
+                                 const float *ig, const float *fg, bool exp_fg, void *h, mlstm_dtype h_dt,
+                                 float *C_last, float *n_last, float *m_last, char *ws, cudaStream_t s) {
+  const int G = Lw.G, PG = P * G, Sg = S / G;
+  float *Bg = (float *)(ws + Lw.Bg), *Cseg = (float *)(ws + Lw.Cseg), *nseg = (float *)(ws + Lw.nseg);
+  float *mseg = (float *)(ws + Lw.mseg), *Cin = (float *)(ws + Lw.Cin), *nin = (float *)(ws + Lw.nin);
+  float *min = (float *)(ws + Lw.min);
+  float *gb = (float *)(ws + Lw.gb), *gx = (float *)(ws + Lw.gx), *gu = (float *)(ws + Lw.gu);
+  float *cm = (float *)(ws + Lw.cm);
+  int *err = (int *)(ws + Lw.err);
+  const bool hb = h_dt == MLSTM_BF16;
+  if (mlstm_status st = launch_status(launch_seg_init(C_init, n_init, m_init, fg, exp_fg, P, G, Sg, DQK, DV, Cin,
+                                                      nin, min, Bg, s)))
+    return st;
+  if (mlstm_status st = launch_status(launch_fwd_tc(q, k, v, hb, gb, gx, gu, cm, ig, fg, min, PG, Sg, DQK, DV, Cin,
+                                                    nin, h, Cseg, nseg, mseg, err, s, exp_fg, P, 0)))
+    return st;
+  if (mlstm_status st = launch_status(launch_seg_scan(P, G, DQK, DV, Bg, Cseg, nseg, mseg, Cin, nin, min, C_last,
+                                                      n_last, m_last, s)))
+    return st;
+  return launch_status(launch_fwd_tc(q, k, v, hb, gb, gx, gu, cm, ig, fg, min, PG, Sg, DQK, DV, Cin, nin, h, Cseg,
+                                     nseg, mseg, err, s, exp_fg, P, G));
+}
+
 // Everything after kernel (a), on a workspace that kernel (a) has filled for these sizes -- or,
 // on the tensor-core path when ig is given, from the raw gate pre-activations (ig, fg, m_init),
 // whose preprocessing the fused kernel then does itself.
 static mlstm_status run_from_gates(const void *q, const void *k, const void *v, int B, int NH, int S,
                                    int DQK, int DV, int chunk, mlstm_dtype dt, const float *C_init,
                                    const float *n_init, void *h, mlstm_dtype h_dt, float *C_last,
-                                   float *n_last, float *m_last, void *workspace, cudaStream_t s,
-                                   const float *ig = nullptr, const float *fg = nullptr,
+                                   float *n_last, float *m_last, void *workspace, size_t ws_bytes,
+                                   cudaStream_t s, const float *ig = nullptr, const float *fg = nullptr,
                                    const float *m_init = nullptr, bool exp_fg = false) {
   const Layout Lw = layout(B, NH, S, DQK, DV, chunk, dt);
-  // The wait-error word reports on this forward only.  The fused kernel clears it itself (its
-  // first CTA, long before any bounded wait could give up); the CUDA-core kernels have no
-  // bounded waits, so it is cleared here.
+  // The wait-error word reports on this forward only: it is cleared in stream order before the
+  // first kernel, on every path (the CUDA-core kernels have no bounded waits and leave it 0).
   char *ws = (char *)workspace;
   float *gb = (float *)(ws + Lw.gb), *gx = (float *)(ws + Lw.gx), *gu = (float *)(ws + Lw.gu);
   float *cm = (float *)(ws + Lw.cm), *Cs = (float *)(ws + Lw.Cs), *ns = (float *)(ws + Lw.ns);
   int *err = (int *)(ws + Lw.err);
   const int P = B * NH, NC = S / chunk;
   const bool bf16 = dt == MLSTM_BF16;
+  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return launch_status(cudaGetLastError());
+  if (Lw.tc && ig != nullptr && Lw.G > 1 && ws_bytes >= Lw.split_total)
+    return run_segments(q, k, v, Lw, P, S, DQK, DV, C_init, n_init, m_init, ig, fg, exp_fg, h, h_dt, C_last,
+                        n_last, m_last, ws, s);
   if (Lw.tc) {
     if (n_init) {
       float *ncopy = (float *)(ws + Lw.ncopy);
@@ -231,7 +301,6 @@ static mlstm_status run_from_gates(const void *q, const void *k, const void *v, 
     return launch_status(launch_fwd_tc(q, k, v, h_dt == MLSTM_BF16, gb, gx, gu, cm, ig, fg, m_init, P, S, DQK,
                                        DV, C_init, n_init, h, C_last, n_last, m_last, err, s, exp_fg));
   }
-  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return launch_status(cudaGetLastError());
   if (mlstm_status st = launch_status(launch_states_simt(k, v, bf16, gb, gx, cm, P, S, chunk, DQK, DV, C_init,
                                                          n_init, Cs, ns, C_last, n_last, s)))
     return st;
@@ -258,7 +327,7 @@ mlstm_status mlstm_fwd_from_gates(const void *q, const void *k, const void *v, i
     return st;
   if (mlstm_status st = check_device()) return st;
   return run_from_gates(q, k, v, B, NH, S, DQK, DV, chunk, dt, C_init, n_init, h, h_dt, C_last, n_last,
-                        m_last, workspace, (cudaStream_t)stream);
+                        m_last, workspace, ws_bytes, (cudaStream_t)stream);
 }
 
 mlstm_status mlstm_fwd_chunkwise(const void *q, const void *k, const void *v, const float *igate_pre,
@@ -272,7 +341,7 @@ mlstm_status mlstm_fwd_chunkwise(const void *q, const void *k, const void *v, co
   if (mlstm_status st = check_fwd_args(q, k, v, B, NH, S, DQK, DV, chunk, dt, C_init, n_init, h, h_dt,
                                        C_last, n_last, m_last, workspace, ws_bytes,
                                        sizes_ok(B, NH, S, DQK, DV, chunk) && (dt == MLSTM_F32 || dt == MLSTM_BF16)
-                                           ? fwd_need(B, NH, S, DQK, DV, chunk, dt)
+                                           ? fwd_need(B, NH, S, DQK, DV, chunk, dt, false)
                                            : 0))
     return st;
   if (S > 0 && (!igate_pre || !fgate_pre)) return MLSTM_ERR_NULL;
@@ -288,14 +357,14 @@ mlstm_status mlstm_fwd_chunkwise(const void *q, const void *k, const void *v, co
   // its workspace needs are below those of the asked-for chunk's layout, which was checked.
   if (use_tc(B, NH, S, DQK, DV, kTcChunk, dt))
     return run_from_gates(q, k, v, B, NH, S, DQK, DV, kTcChunk, dt, C_init, n_init, h, h_dt, C_last, n_last,
-                          m_last, workspace, s, igate_pre, fgate_pre, m_init, exp_fg);
+                          m_last, workspace, ws_bytes, s, igate_pre, fgate_pre, m_init, exp_fg);
   const Layout Lw = layout(B, NH, S, DQK, DV, chunk, dt);
   if (mlstm_status st = launch_status(launch_gates(igate_pre, fgate_pre, P, S, chunk, m_init, (float *)(ws + Lw.gb),
                                                    (float *)(ws + Lw.gx), (float *)(ws + Lw.gu),
                                                    (float *)(ws + Lw.cm), nullptr, s, exp_fg)))
     return st;
   return run_from_gates(q, k, v, B, NH, S, DQK, DV, chunk, dt, C_init, n_init, h, h_dt, C_last, n_last,
-                        m_last, workspace, s);
+                        m_last, workspace, ws_bytes, s);
 }
 
 mlstm_status mlstm_fwd_chunk_states(const void *k, const void *v, const float *igate_pre,
@@ -480,14 +549,15 @@ mlstm_status mlstm_fwd_chunkwise_noalloc(const void *q, const void *k, const voi
   if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return MLSTM_ERR_SHAPE;
   // sizes whose scratch (on the path the forward takes) would not fit in the fixed array are
   // refused before anything runs
-  if (fwd_need(B, NH, S, DQK, DV, chunk, bare) > (size_t)MLSTM_NOALLOC_SCRATCH_BYTES) return MLSTM_ERR_WORKSPACE;
+  if (fwd_need(B, NH, S, DQK, DV, chunk, bare, false) > (size_t)MLSTM_NOALLOC_SCRATCH_BYTES)
+    return MLSTM_ERR_WORKSPACE;
   if (mlstm_status st = check_device()) return st;
   void *scratch = nullptr;
   if (mlstm_status st = noalloc_scratch_ptr(&scratch)) return st;
   // Everything the forward reads from its workspace is written by the same call first (the
-  // gate arrays, the chunk stabiliser, the copy of n_init) and the one word that must start
-  // at zero (the kernels' wait-error word) is cleared by the forward itself, so the stale
-  // contents of an earlier call never matter.
+  // gate arrays, the chunk stabiliser, the copy of n_init, the sequence-parallel buffers) and
+  // the one word that must start at zero (the kernels' wait-error word) is cleared by the
+  // forward itself, so the stale contents of an earlier call never matter.
   return mlstm_fwd_chunkwise(q, k, v, igate_pre, fgate_pre, B, NH, S, DQK, DV, chunk, dt, C_init,
                              n_init, m_init, h, h_dt, C_last, n_last, m_last, scratch,
                              (size_t)MLSTM_NOALLOC_SCRATCH_BYTES, stream);

@@ -33,13 +33,26 @@ cudaError_t launch_step(const void *q, const void *k, const void *v, bool bf16, 
 // d_v a multiple of 128.  fwd_tc_pair says whether a head's d_qk is split over a CTA pair.
 bool fwd_tc_supported(int S, int L, int D, int DV, bool bf16);
 bool fwd_tc_pair(int P, int D, int DV);
+// Sequence segments the forward runs in parallel for these sizes (1 = none).
+int fwd_tc_segments(int P, int S, int D, int DV);
 // The gate factors come from the raw pre-activations ig, fg (and m_init) when ig is not NULL,
 // otherwise from the gate kernel's b, x, u and chunk stabiliser in the workspace.
 cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, bool out_bf16, const float *gb,
                           const float *gx, const float *gu, const float *cm, const float *ig, const float *fg,
                           const float *m_init, int P, int S, int D, int DV, const float *C_init,
                           const float *n_init, void *h, float *C_last, float *n_last, float *m_last, int *err,
-                          cudaStream_t stream, bool exp_fg = false);
+                          cudaStream_t stream, bool exp_fg = false, int pair_heads = 0, int seg_skip = 0);
+// The sequence-parallel forward's helpers (seq_split.cu), for G segments of Sg tokens per head:
+// entering states of the first pass (the caller's initial state for segment 0, the zero state with
+// m = -inf for the others) and every segment's sum of log f (Bg, P*G floats) ...
+cudaError_t launch_seg_init(const float *C_init, const float *n_init, const float *m_init, const float *fg,
+                            bool exp_fg, int P, int G, int Sg, int DQK, int DV, float *Cin, float *nin, float *min,
+                            float *Bg, cudaStream_t stream);
+// ... and the scan that composes the segments' maps into every segment's entering state and the
+// final state.
+cudaError_t launch_seg_scan(int P, int G, int DQK, int DV, const float *Bg, const float *Cseg, const float *nseg,
+                            const float *mseg, float *Cin, float *nin, float *min, float *C_last, float *n_last,
+                            float *m_last, cudaStream_t stream);
 
 // (d') T consecutive decode steps in one launch, in place (T <= step_multi_max_tokens()).
 int step_multi_max_tokens();

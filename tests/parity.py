@@ -79,3 +79,36 @@ def conditioned_ok(h, ora, v, tol, u_num, u_den):
         "rel_err_kappa_le_100": rel_err(h[kappa <= 100], oh[kappa <= 100]),
     }
     return bool(np.all(excess <= 1.0)), float(np.max(excess)), stats
+
+
+def u_fp32(dqk, chunk):
+    """Relative error per summed term of an fp32 evaluation of nᵀq or C q: the sums run over
+    d_qk products (the inter-chunk part) and L (the intra-chunk part), each rounding at 2^-24."""
+    return (dqk + chunk) * 2.0 ** -24
+
+
+def u_tc(dqk):
+    """The fused tensor-core kernel's allowance: twice that of fp32 sums at its chunk of 64.
+    Its operands are rounded to fp16 but its sums run in fp32; on the long-context stress
+    workload its worst error per condition-number bin (kappa > 100) is measured to stay within
+    twice the fp32 CUDA-core path's on the same values
+    (test_stress_tensor_core_vs_fp32_path_per_kappa_bin), which is what this factor rests on."""
+    return 2.0 * u_fp32(dqk, 64)
+
+
+KAPPA_BINS = ((0.0, 1e2), (1e2, 1e3), (1e3, 1e4), (1e4, np.inf))
+
+
+def kappa_bin_errors(h, ora, bins=KAPPA_BINS):
+    """max |h - h_oracle| / RMS(h_oracle) over the rows whose condition number kappa_t (module
+    docstring) lies in each (lo, hi] bin; returns [(rows, error or None)] per bin."""
+    h = np.asarray(h, np.float64)
+    oh = ora["h"]
+    kappa = ora["dabs_tok"] / np.maximum(np.abs(ora["den_tok"]), np.exp(-ora["m_tok"]))
+    err = np.max(np.abs(h - oh), axis=-1) / rms(oh)
+    out = []
+    for lo, hi in bins:
+        sel = (kappa > lo) & (kappa <= hi)
+        out.append((int(sel.sum()), float(err[sel].max()) if sel.any() else None))
+    return out
+

@@ -77,12 +77,64 @@ def test_workspace_bytes_follow_the_path_that_runs(lib):
     state, so a bf16 forward asked for chunk 128 needs only the gate arrays of its chunk (for
     mlstm_fwd_chunk_states and mlstm_fwd_gates) and the fused kernel's own small layout; fp32
     inputs take the CUDA-core path and need every boundary state."""
-    ws = lib.mlstm_fwd_workspace_bytes
+    ws, ws_min = lib.mlstm_fwd_workspace_bytes, lib.mlstm_fwd_workspace_min_bytes
     P, S = 8, 16384
     assert lib.mlstm_fwd_path(1, 8, S, 256, 256, 128, 1) >= 1
     gates128 = 3 * P * S * 4 + P * (S // 128 + 1) * 4
-    assert gates128 <= ws(1, 8, S, 256, 256, 128, 1) < 4 << 20
+    assert gates128 <= ws_min(1, 8, S, 256, 256, 128, 1) < 4 << 20
     assert ws(1, 8, S, 256, 256, 128, 0) > P * (S // 128) * 256 * 256 * 4
+    assert ws_min(1, 8, S, 256, 256, 128, 0) == ws(1, 8, S, 256, 256, 128, 0)
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 148
+
+
+def _segments_expected(P, S, D, DV):
+    """The rule mlstm_fwd_segments follows, restated: the largest power of two G with G times
+    the plain grid's CTAs within the SM count, S divisible by 64 G, at least 256 tokens a segment."""
+    pair = D == 512 or (D >= 128 and P * (DV // 128) < _sms())
+    ctas = P * (DV // 128) * (2 if pair else 1)
+    G = 1
+    while ctas * 2 * G <= _sms() and S % (64 * 2 * G) == 0 and S // (2 * G) >= 256:
+        G *= 2
+    return G
+
+
+@pytest.mark.parametrize("b,nh,s,dqk,dv", [(1, 8, 16384, 256, 256), (4, 4, 2048, 512, 512),
+                                           (8, 4, 1024, 256, 256), (1, 2, 1024, 256, 256),
+                                           (1, 1, 2048, 512, 256), (2, 1, 1024, 128, 128),
+                                           (1, 2, 512, 64, 128), (1, 2, 448, 256, 256)])
+def test_sequence_parallel_selection(lib, b, nh, s, dqk, dv):
+    """Long sequences over few heads run in G parallel segments when the workspace holds the
+    segment buffers (per (head, segment) two fp32 states C, n, m and a float); the least
+    workspace runs them whole, and the CUDA-core path never splits."""
+    ws, ws_min, seg = lib.mlstm_fwd_workspace_bytes, lib.mlstm_fwd_workspace_min_bytes, lib.mlstm_fwd_segments
+    G = _segments_expected(b * nh, s, dqk, dv)
+    full, least = ws(b, nh, s, dqk, dv, 64, 1), ws_min(b, nh, s, dqk, dv, 64, 1)
+    assert seg(b, nh, s, dqk, dv, 64, 1, full) == G
+    assert seg(b, nh, s, dqk, dv, 64, 1, least) == 1
+    assert seg(b, nh, s, dqk, dv, 64, 1, full - 1) == (1 if G > 1 else G)
+    assert seg(b, nh, s, dqk, dv, 64, 0, 1 << 40) == 1  # fp32 inputs: CUDA-core kernels
+    if G > 1:
+        per_segment = 2 * (dv * dqk + dqk + 1) * 4 + 4
+        assert full - least >= b * nh * G * per_segment
+        assert full - least <= b * nh * G * per_segment + 7 * 256
+    else:
+        assert full == least
+    assert seg(1, 2, 100, 64, 64, 64, 1, 1 << 30) == -1  # S % chunk != 0
+    assert seg(1, 2, 128, 64, 64, 64, 7, 1 << 30) == -1  # bad dtype code
+
+
+def test_sequence_parallel_layer_sizes(lib):
+    """The long-context layer (B=1 NH=8 S=16384 d=256: 32 CTAs alone) runs in 4 segments on a
+    148-SM device; the 1.3B-style layer (128 CTAs) and the 350M-style layer fill the GPU whole."""
+    if _sms() != 148:
+        pytest.skip("segment counts below are those of a 148-SM device")
+    ws, seg = lib.mlstm_fwd_workspace_bytes, lib.mlstm_fwd_segments
+    assert seg(1, 8, 16384, 256, 256, 128, 1, ws(1, 8, 16384, 256, 256, 128, 1)) == 4
+    assert seg(4, 4, 2048, 512, 512, 64, 1, ws(4, 4, 2048, 512, 512, 64, 1)) == 1
+    assert seg(8, 4, 1024, 256, 256, 64, 1, ws(8, 4, 1024, 256, 256, 64, 1)) == 1
 
 
 def test_noalloc_helpers_argument_errors(lib):
