@@ -62,8 +62,9 @@ def dec_bytes(w, h_bytes=4) -> float:
 
 
 def captured_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary (profiles/traffic.json),
-    or None when the kernel's source has changed since that capture."""
+    """DRAM bytes per launch of `kernel` (an entry of profiles/traffic.json: a kernel name, or
+    kernel@workload) from the committed ncu summary, or None when the kernel's source has
+    changed since that capture."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
@@ -286,6 +287,64 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------------------------ GPU arm
+def time_layer(B, w, dev, args, flush, peaks):
+    """One more forward workload, timed like the headline (L2 flushed between calls, CUDA events
+    around each call), with h in the dtype of v (bf16) as the layer hands it on.  The 350M-style
+    layer is HBM-bound (its roofline is HBM of algorithmic bytes); the long-context layer runs in
+    sequence segments on the tensor-core path (4 launches: segment init, first pass, scan, second
+    pass) and is reported against HBM as well, with its tensor-core fraction beside it."""
+    import torch
+    inp = W.make_inputs(w)
+    q, k, v = (torch.from_numpy(inp[x]).to(dev).to(torch.bfloat16) for x in ("q", "k", "v"))
+    ig, fg = (torch.from_numpy(inp[x]).to(dev) for x in ("ig", "fg"))
+    del inp
+    out = (torch.empty((w.B, w.NH, w.S, w.DV), dtype=torch.bfloat16, device=dev),
+           torch.empty((w.B, w.NH, w.DV, w.DQK), dtype=torch.float32, device=dev),
+           torch.empty((w.B, w.NH, w.DQK), dtype=torch.float32, device=dev),
+           torch.empty((w.B, w.NH), dtype=torch.float32, device=dev))
+    ws = B.alloc_workspace(w.B, w.NH, w.S, w.DQK, w.DV, w.chunk, torch.bfloat16, dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        B.mlstm_fwd_chunkwise(q, k, v, ig, fg, w.chunk, h_dtype=torch.bfloat16, out=out, workspace=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    reps = max(args.steps, 5)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    l0 = B.mlstm_kernel_launches()
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    launches = B.mlstm_kernel_launches() - l0
+    B.mlstm_fwd_check(ws, w.B, w.NH, w.S, w.DQK, w.DV, w.chunk)
+    us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+    nbytes, flops = fwd_bytes(w, h_bytes=2), fwd_flops(w)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    tf = flops / (us * 1e-6) / 1e12
+    G = B.mlstm_fwd_segments(w.B, w.NH, w.S, w.DQK, w.DV, w.chunk)
+    key = {W.LAYER_350M.name: "350m", W.STRESS_16K.name: "stress"}[w.name]
+    return {"metric": f"mLSTM chunkwise forward tokens/s ({w.name})", "value": w.B * w.S / (us * 1e-6),
+            "unit": "tokens/s", "us_per_launch": us,
+            "config": {"workload": w.name, "B": w.B, "NH": w.NH, "S": w.S, "DQK": w.DQK, "DV": w.DV,
+                       "chunk": w.chunk, "qkv": "bf16", "gates": "fp32", "h": "bf16",
+                       "sequence_segments": G,
+                       "l2": "flushed between timed calls (256 MiB write, outside the events)"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"],
+                         "traffic": captured_traffic(f"forward@{key}"),
+                         "kernel": ("fwd_tc_kernel (one launch)" if G == 1 else
+                                    f"whole forward: seg_init, fwd_tc_kernel x2 ({G} segments), seg_scan"),
+                         "algorithmic_bytes_per_launch": nbytes,
+                         "peak_source": peaks["source"] + " HBM copy",
+                         "tensor_tflops": tf, "tensor_frac": tf / peaks["bf16_tflops"]},
+            "gpu_launches": int(launches)}
+
+
 def run_ours(args, rank, local, world):
     import torch
     from mlstm_matrix_memory_02_b300 import binding as B
@@ -457,6 +516,10 @@ def run_ours(args, rank, local, world):
                       "l2": "134 MB per launch, larger than L2 (no flush)"}
     del o_pre, y_gn
 
+    # ---- the other forward workloads: the 350M-style layer and the long-context layer
+    layers = {"layer_350m": time_layer(B, W.LAYER_350M, dev, args, flush, peaks),
+              "stress": time_layer(B, W.STRESS_16K, dev, args, flush, peaks)}
+
     # ---- end to end through the public API: pinned host inputs in, h back to the host
     pin = {key: torch.from_numpy(inp[key]).to(torch.bfloat16 if key in "qkv" else torch.float32).pin_memory()
            for key in ("q", "k", "v", "ig", "fg")}
@@ -497,9 +560,14 @@ def run_ours(args, rank, local, world):
         "roofline": roofline,
         "decode": decode,
         "block_epilogue": block_epilogue,
+        "layer_350m": layers["layer_350m"],
+        "stress": layers["stress"],
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": int(launches_fwd + launches_dec + launches_gn),
+        "gpu_launches": int(launches_fwd),
+        "gpu_launches_other": {"decode": int(launches_dec), "block_epilogue": int(launches_gn),
+                               "layer_350m": layers["layer_350m"]["gpu_launches"],
+                               "stress": layers["stress"]["gpu_launches"]},
         "clocks": clk.summary(),
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -515,7 +583,8 @@ def run_ours(args, rank, local, world):
 def run_profile(kind: str):
     """Small, self-contained launches for ncu captures: one warm-up and one timed-shape call.
 
-    fwd:          the --workload forward (one fused launch on the tensor-core path)
+    fwd:          the --workload forward (one fused launch on the tensor-core path; four for the
+                  long-context layer in sequence segments)
     decode:       one decode step of the B=256, NH=8, d=256 state (state initialised randomly)
     decode_multi: 16 decode steps in one launch on the same state
     gn:           group norm + output gate on a 1.3B-layer-shaped h (fp32 h, bf16 o~ and y)"""
@@ -527,8 +596,10 @@ def run_profile(kind: str):
         inp = W.make_inputs(w)
         q, k, v = (torch.from_numpy(inp[x]).to(dev).to(torch.bfloat16) for x in ("q", "k", "v"))
         ig, fg = (torch.from_numpy(inp[x]).to(dev) for x in ("ig", "fg"))
+        # h as the bench writes it: fp32 for the 1.3B-style layer, bf16 for the others
+        h_dtype = torch.float32 if w is W.LAYER_1P3B else torch.bfloat16
         for _ in range(2):
-            B.mlstm_fwd_chunkwise(q, k, v, ig, fg, w.chunk, h_dtype=torch.float32)
+            B.mlstm_fwd_chunkwise(q, k, v, ig, fg, w.chunk, h_dtype=h_dtype)
     elif kind == "gn":
         w = FWD
         g = torch.Generator(device=dev).manual_seed(3)

@@ -10,7 +10,7 @@
 //   h_t = C_t q_t / max(|n_t . q_t|, exp(-m_t))
 // exactly as T single steps, but the state (2 * DV * DQK * 4 bytes per head) crosses HBM once
 // for the T tokens instead of T times: row a of C_t depends only on row a of C_{t-1}, so each
-// warp carries its rows through all T tokens in registers.  One CTA of 256 threads per
+// warp carries two rows at a time through all T tokens in registers.  One CTA of 256 threads per
 // (batch, head); the scalar gate chain, the n chain and the T denominators are formed first.
 #include "common.cuh"
 #include "kernels.cuh"
@@ -57,13 +57,16 @@ __device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
   return v[0];
 }
 
-// BUTTERFLY: reduce the 2 T dot products of a row pair together (worth it from T = 8 on; below
-// that the per-dot warp sums are cheaper and the kernel needs half the registers).
-template <typename T, typename TO, bool BUTTERFLY>
+// BUTTERFLY: reduce the T dot products of the rows in flight together (worth it from T = 8 on;
+// below that the per-dot warp sums are cheaper and the kernel needs fewer registers).  PL: float4
+// columns of a row per lane (DQK / 128, rounded up); RIF: rows a warp carries at once -- every
+// k_t, q_t read from shared memory feeds RIF rows.
+template <typename T, typename TO, bool BUTTERFLY, int PL, int RIF>
 __global__ void __launch_bounds__(kThreads) step_multi_kernel(
     const T *__restrict__ qin, const T *__restrict__ kin, const T *__restrict__ vin, const float *__restrict__ ig,
     const float *__restrict__ fg, float *__restrict__ C, float *__restrict__ n, float *__restrict__ m,
     TO *__restrict__ h, int NT, int DQK, int DV, int exp_fg) {
+  static_assert(!BUTTERFLY || (RIF * kMaxT) % 32 == 0, "dot slots fill whole butterflies");
   extern __shared__ __align__(16) float dsm[];
   float *sq = dsm;                // [NT][DQK]  q_t
   float *sk = dsm + NT * DQK;     // [NT][DQK]  w_t khat_t
@@ -128,118 +131,140 @@ __global__ void __launch_bounds__(kThreads) step_multi_kernel(
   }
   __syncthreads();
 
-  // C rows: warp w carries rows w, w + 8, ... through the T tokens; lane owns float4 columns
-  // lane + 32 j of the row.
-  const int nv4 = DQK / 4;               // float4 per row (a multiple of 8)
-  const int per_lane = (nv4 + 31) / 32;  // 1..4
+  // C rows: warp w carries rows w RIF .. w RIF + RIF - 1 (then the next 8 RIF rows) through the T
+  // tokens; lane owns float4 columns lane + 32 j of each row.
+  const int nv4 = DQK / 4;  // float4 per row (a multiple of 8)
   float4 *C4 = reinterpret_cast<float4 *>(C + (size_t)p * DV * DQK);
   const float4 *sq4 = reinterpret_cast<const float4 *>(sq);
   const float4 *sk4 = reinterpret_cast<const float4 *>(sk);
-  constexpr int kRowsInFlight = 2;
-  for (int a0 = warp * kRowsInFlight; a0 < DV; a0 += (kThreads / 32) * kRowsInFlight) {
-    float4 x[kRowsInFlight][4];
+  for (int a0 = warp * RIF; a0 < DV; a0 += (kThreads / 32) * RIF) {
+    float4 x[RIF][PL];
 #pragma unroll
-    for (int i = 0; i < kRowsInFlight; ++i) {
+    for (int i = 0; i < RIF; ++i) {
       const int a = a0 + i;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < PL; ++j) {
         const int c4 = lane + 32 * j;
-        if (a < DV && j < per_lane && c4 < nv4) x[i][j] = __ldcs(&C4[(size_t)a * nv4 + c4]);
+        if (a < DV && c4 < nv4) x[i][j] = __ldcs(&C4[(size_t)a * nv4 + c4]);
         else x[i][j] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
     if (BUTTERFLY) {
-      // the 2 NT dot products of this row pair (slot i NT + t) are reduced together at the end
-      float dots[32];
+      // the RIF NT dot products of these rows (slot i kMaxT + t) are reduced together at the end,
+      // 32 slots per butterfly
+      float dots[RIF * kMaxT / 32][32];
 #pragma unroll
-      for (int sl = 0; sl < 32; ++sl) dots[sl] = 0.f;
+      for (int b = 0; b < RIF * kMaxT / 32; ++b)
+#pragma unroll
+        for (int sl = 0; sl < 32; ++sl) dots[b][sl] = 0.f;
 #pragma unroll
       for (int t = 0; t < kMaxT; ++t) {
         if (t < NT) {
           const float al = s_alpha[t];
+          float4 kv[PL], qv[PL];
 #pragma unroll
-          for (int i = 0; i < kRowsInFlight; ++i) {
+          for (int j = 0; j < PL; ++j) {
+            const int c4 = lane + 32 * j;
+            kv[j] = c4 < nv4 ? sk4[t * nv4 + c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+            qv[j] = c4 < nv4 ? sq4[t * nv4 + c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int i = 0; i < RIF; ++i) {
             const int a = a0 + i;
             const float va = a < DV ? sv[t * DV + a] : 0.f;
             float dot = 0.f;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int c4 = lane + 32 * j;
-              if (j < per_lane && c4 < nv4) {
-                const float4 kv = sk4[t * nv4 + c4], qv = sq4[t * nv4 + c4];
-                float4 y = x[i][j];
-                y.x = fmaf(al, y.x, va * kv.x);
-                y.y = fmaf(al, y.y, va * kv.y);
-                y.z = fmaf(al, y.z, va * kv.z);
-                y.w = fmaf(al, y.w, va * kv.w);
-                x[i][j] = y;
-                dot = fmaf(y.x, qv.x, dot);
-                dot = fmaf(y.y, qv.y, dot);
-                dot = fmaf(y.z, qv.z, dot);
-                dot = fmaf(y.w, qv.w, dot);
-              }
+            for (int j = 0; j < PL; ++j) {
+              float4 y = x[i][j];
+              y.x = fmaf(al, y.x, va * kv[j].x);
+              y.y = fmaf(al, y.y, va * kv[j].y);
+              y.z = fmaf(al, y.z, va * kv[j].z);
+              y.w = fmaf(al, y.w, va * kv[j].w);
+              x[i][j] = y;
+              dot = fmaf(y.x, qv[j].x, dot);
+              dot = fmaf(y.y, qv[j].y, dot);
+              dot = fmaf(y.z, qv[j].z, dot);
+              dot = fmaf(y.w, qv[j].w, dot);
             }
-            dots[i * kMaxT + t] = dot;
+            dots[(i * kMaxT + t) / 32][(i * kMaxT + t) % 32] = dot;
           }
         }
       }
-      const float tot = transpose_reduce32(dots, lane);
-      const int i = lane / kMaxT, t = lane % kMaxT, a = a0 + i;
-      if (t < NT && a < DV) h[((size_t)p * NT + t) * DV + a] = from_f32<TO>(tot * s_inv[t]);
+#pragma unroll
+      for (int b = 0; b < RIF * kMaxT / 32; ++b) {
+        const float tot = transpose_reduce32(dots[b], lane);
+        const int slot = 32 * b + lane, i = slot / kMaxT, t = slot % kMaxT, a = a0 + i;
+        if (t < NT && a < DV) h[((size_t)p * NT + t) * DV + a] = from_f32<TO>(tot * s_inv[t]);
+      }
     } else {
       for (int t = 0; t < NT; ++t) {
         const float al = s_alpha[t], inv = s_inv[t];
+        float4 kv[PL], qv[PL];
 #pragma unroll
-        for (int i = 0; i < kRowsInFlight; ++i) {
+        for (int j = 0; j < PL; ++j) {
+          const int c4 = lane + 32 * j;
+          kv[j] = c4 < nv4 ? sk4[t * nv4 + c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+          qv[j] = c4 < nv4 ? sq4[t * nv4 + c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < RIF; ++i) {
           const int a = a0 + i;
-          if (a >= DV) break;
-          const float va = sv[t * DV + a];
+          const float va = a < DV ? sv[t * DV + a] : 0.f;
           float dot = 0.f;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int c4 = lane + 32 * j;
-            if (j < per_lane && c4 < nv4) {
-              const float4 kv = sk4[t * nv4 + c4], qv = sq4[t * nv4 + c4];
-              float4 y = x[i][j];
-              y.x = fmaf(al, y.x, va * kv.x);
-              y.y = fmaf(al, y.y, va * kv.y);
-              y.z = fmaf(al, y.z, va * kv.z);
-              y.w = fmaf(al, y.w, va * kv.w);
-              x[i][j] = y;
-              dot = fmaf(y.x, qv.x, dot);
-              dot = fmaf(y.y, qv.y, dot);
-              dot = fmaf(y.z, qv.z, dot);
-              dot = fmaf(y.w, qv.w, dot);
-            }
+          for (int j = 0; j < PL; ++j) {
+            float4 y = x[i][j];
+            y.x = fmaf(al, y.x, va * kv[j].x);
+            y.y = fmaf(al, y.y, va * kv[j].y);
+            y.z = fmaf(al, y.z, va * kv[j].z);
+            y.w = fmaf(al, y.w, va * kv[j].w);
+            x[i][j] = y;
+            dot = fmaf(y.x, qv[j].x, dot);
+            dot = fmaf(y.y, qv[j].y, dot);
+            dot = fmaf(y.z, qv[j].z, dot);
+            dot = fmaf(y.w, qv[j].w, dot);
           }
           dot = warp_sum(dot);
-          if (lane == 0) h[((size_t)p * NT + t) * DV + a] = from_f32<TO>(dot * inv);
+          if (lane == 0 && a < DV) h[((size_t)p * NT + t) * DV + a] = from_f32<TO>(dot * inv);
         }
       }
     }
 #pragma unroll
-    for (int i = 0; i < kRowsInFlight; ++i) {
+    for (int i = 0; i < RIF; ++i) {
       const int a = a0 + i;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < PL; ++j) {
         const int c4 = lane + 32 * j;
-        if (a < DV && j < per_lane && c4 < nv4) __stcs(&C4[(size_t)a * nv4 + c4], x[i][j]);
+        if (a < DV && c4 < nv4) __stcs(&C4[(size_t)a * nv4 + c4], x[i][j]);
       }
     }
   }
 }
 
-template <typename T, typename TO>
-cudaError_t launch_step_multi_t(const void *q, const void *k, const void *v, const float *ig, const float *fg,
+template <typename T, typename TO, bool BUTTERFLY, int RIF>
+cudaError_t launch_step_multi_k(const void *q, const void *k, const void *v, const float *ig, const float *fg,
                                 float *C, float *n, float *m, void *h, int P, int NT, int DQK, int DV,
                                 cudaStream_t stream, bool exp_fg) {
-  auto kern = NT >= 8 ? step_multi_kernel<T, TO, true> : step_multi_kernel<T, TO, false>;
+  const int pl = (DQK / 4 + 31) / 32;
+  auto kern = pl == 1   ? step_multi_kernel<T, TO, BUTTERFLY, 1, RIF>
+              : pl == 2 ? step_multi_kernel<T, TO, BUTTERFLY, 2, RIF>
+              : pl == 3 ? step_multi_kernel<T, TO, BUTTERFLY, 3, RIF>
+                        : step_multi_kernel<T, TO, BUTTERFLY, 4, RIF>;
   const size_t smem = (size_t)NT * (2 * DQK + DV) * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<P, kThreads, smem, stream>>>((const T *)q, (const T *)k, (const T *)v, ig, fg, C, n, m, (TO *)h, NT, DQK,
                                       DV, exp_fg ? 1 : 0);
   return cudaGetLastError();
+}
+
+template <typename T, typename TO>
+cudaError_t launch_step_multi_t(const void *q, const void *k, const void *v, const float *ig, const float *fg,
+                                float *C, float *n, float *m, void *h, int P, int NT, int DQK, int DV,
+                                cudaStream_t stream, bool exp_fg) {
+  if (NT >= 8)
+    return launch_step_multi_k<T, TO, true, 2>(q, k, v, ig, fg, C, n, m, h, P, NT, DQK, DV, stream, exp_fg);
+  return launch_step_multi_k<T, TO, false, 2>(q, k, v, ig, fg, C, n, m, h, P, NT, DQK, DV, stream, exp_fg);
 }
 
 int step_multi_max_tokens() { return kMaxT; }
