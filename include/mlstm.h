@@ -243,6 +243,32 @@ mlstm_status mlstm_groupnorm_gate(const void *h, const void *o_pre, const float 
                                   float eps, void *y, int B, int NH, int S, int DV, mlstm_dtype h_dt,
                                   mlstm_dtype o_dt, mlstm_dtype y_dt, void *stream);
 
+/* Backward of mlstm_fwd_chunkwise (section 3 "The Parallel Dual Form": the parallel form is the
+ * one trained; "Associative Matrix Cell State" for the updates and the retrieval; section 2 for
+ * the stabiliser, which rescales C and n by exp(-m_t) and changes no value of h, so the
+ * gradients are those of the unstabilised cell).  For L = sum_t dh_t . h_t with h from
+ * mlstm_fwd_chunkwise on the same inputs:
+ *   dq, dk [B,NH,S,DQK], dv [B,NH,S,DV] (dt) outputs: dL/dq, dL/dk (k as passed, unscaled),
+ *       dL/dv;
+ *   dig, dfg [B,NH,S] float32 outputs: dL/di~ and dL/df~ (through log sigmoid(f~), or f~ itself
+ *       with MLSTM_FORGET_EXP OR-ed into dt);
+ *   dC_init [B,NH,DV,DQK], dn_init [B,NH,DQK], dm_init [B,NH] float32 outputs (all three or
+ *       none): dL/d of the initial state as the forward takes it (C_init, n_init relative to
+ *       m_init; dm_init = <dC_init, C_init> + dn_init . n_init, zero without an initial state).
+ *   dh [B,NH,S,DV] (dt): dL/dh.  Other inputs as for mlstm_fwd_chunkwise (same chunk rules).
+ * Where |n_t . q_t| equals exp(-m_t) exactly, h has a kink; the derivative taken there treats
+ * the floor as the active branch.  The forward is recomputed inside (gate preprocessing,
+ * boundary states, per-token denominators), so no forward output is needed.  Runs on CUDA
+ * cores in fp32 whatever dt.  workspace: at least mlstm_bwd_workspace_bytes(...) bytes. */
+size_t mlstm_bwd_workspace_bytes(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt);
+mlstm_status mlstm_bwd_chunkwise(const void *q, const void *k, const void *v,
+                                 const float *igate_pre, const float *fgate_pre, const void *dh,
+                                 int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt,
+                                 const float *C_init, const float *n_init, const float *m_init,
+                                 void *dq, void *dk, void *dv, float *dig, float *dfg,
+                                 float *dC_init, float *dn_init, float *dm_init, void *workspace,
+                                 size_t ws_bytes, void *stream);
+
 /* Forward without any device allocation (no counterpart on the source pages: an interface
  * addition of this library).
  *

@@ -56,6 +56,11 @@ _lib.mlstm_fwd_workspace_min_bytes.restype = _sz
 _lib.mlstm_fwd_workspace_min_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
 _lib.mlstm_fwd_segments.restype = _i
 _lib.mlstm_fwd_segments.argtypes = [_i, _i, _i, _i, _i, _i, _i, _sz]
+_lib.mlstm_bwd_workspace_bytes.restype = _sz
+_lib.mlstm_bwd_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+_lib.mlstm_bwd_chunkwise.restype = _i
+_lib.mlstm_bwd_chunkwise.argtypes = [_vp, _vp, _vp, _fp, _fp, _vp, _i, _i, _i, _i, _i, _i, _i, _fp, _fp, _fp,
+                                     _vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp, _vp, _sz, _vp]
 _lib.mlstm_fwd_check.restype = _i
 _lib.mlstm_fwd_check.argtypes = [_vp, _sz, _i, _i, _i, _i, _i, _i, _i, _vp]
 _lib.mlstm_step.restype = _i
@@ -78,7 +83,8 @@ EXPORTED = ["mlstm_status_str", "mlstm_last_cuda_error", "mlstm_kernel_launches"
             "mlstm_fwd_chunk_states", "mlstm_fwd_gates", "mlstm_fwd_check", "mlstm_fwd_path",
             "mlstm_step", "mlstm_step_multi", "mlstm_fwd_chunkwise_noalloc", "mlstm_groupnorm_gate",
             "mlstm_wait_selftest", "mlstm_fwd_check_noalloc", "mlstm_noalloc_scratch",
-            "mlstm_fwd_workspace_min_bytes", "mlstm_fwd_segments"]
+            "mlstm_fwd_workspace_min_bytes", "mlstm_fwd_segments", "mlstm_bwd_workspace_bytes",
+            "mlstm_bwd_chunkwise"]
 SELFTEST_WAIT_CODE = 90
 
 # Bytes of the fixed scratch array behind mlstm_fwd_chunkwise_noalloc (include/mlstm.h).
@@ -208,6 +214,53 @@ def mlstm_fwd_chunkwise(q, k, v, igate_pre, fgate_pre, chunk, h_dtype=None, C_in
         _ptr(C_last), _ptr(n_last), _ptr(m_last), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(code, "mlstm_fwd_chunkwise")
     return h, C_last, n_last, m_last
+
+
+def mlstm_bwd_workspace_bytes(B, NH, S, DQK, DV, chunk, dtype=torch.bfloat16) -> int:
+    return int(_lib.mlstm_bwd_workspace_bytes(B, NH, S, DQK, DV, chunk, _DT[dtype]))
+
+
+def mlstm_bwd_chunkwise(q, k, v, igate_pre, fgate_pre, dh, chunk, C_init=None, n_init=None, m_init=None,
+                        init_grads=None, workspace=None, stream=None, forget="sigmoid"):
+    """Backward of mlstm_fwd_chunkwise for the loss sum(dh * h).  Returns a dict with dq, dk, dv
+    (dtype of q), dig, dfg (fp32) and, when ``init_grads`` is true (default: when an initial
+    state is given), dC_init, dn_init, dm_init."""
+    B, NH, S, DQK = q.shape
+    DV = v.shape[-1]
+    dt = q.dtype
+    if dt not in _DT:
+        raise TypeError("q, k, v must be float32 or bfloat16")
+    _dev(q, "q", dt)
+    _dev(k, "k", dt, (B, NH, S, DQK))
+    _dev(v, "v", dt, (B, NH, S, DV))
+    _dev(dh, "dh", dt, (B, NH, S, DV))
+    _dev(igate_pre, "igate_pre", torch.float32, (B, NH, S))
+    _dev(fgate_pre, "fgate_pre", torch.float32, (B, NH, S))
+    given = any(x is not None for x in (C_init, n_init, m_init))
+    if given:
+        _dev(C_init, "C_init", torch.float32, (B, NH, DV, DQK))
+        _dev(n_init, "n_init", torch.float32, (B, NH, DQK))
+        _dev(m_init, "m_init", torch.float32, (B, NH))
+    if init_grads is None:
+        init_grads = given
+    out = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
+           "dig": torch.empty_like(igate_pre), "dfg": torch.empty_like(fgate_pre)}
+    if init_grads:
+        out["dC_init"] = torch.empty((B, NH, DV, DQK), dtype=torch.float32, device=q.device)
+        out["dn_init"] = torch.empty((B, NH, DQK), dtype=torch.float32, device=q.device)
+        out["dm_init"] = torch.empty((B, NH), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = mlstm_bwd_workspace_bytes(B, NH, S, DQK, DV, chunk, dt)
+        if n == 0:
+            raise ValueError("unsupported sizes for the mLSTM backward")
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    code = _lib.mlstm_bwd_chunkwise(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(igate_pre), _ptr(fgate_pre), _ptr(dh), B, NH, S, DQK, DV, chunk,
+        _dt_code(dt, forget), _ptr(C_init), _ptr(n_init), _ptr(m_init), _ptr(out["dq"]), _ptr(out["dk"]),
+        _ptr(out["dv"]), _ptr(out["dig"]), _ptr(out["dfg"]), _ptr(out.get("dC_init")), _ptr(out.get("dn_init")),
+        _ptr(out.get("dm_init")), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(code, "mlstm_bwd_chunkwise")
+    return out
 
 
 def mlstm_step_multi(q, k, v, ig, fg, C, n, m, h=None, h_dtype=None, stream=None, forget="sigmoid"):

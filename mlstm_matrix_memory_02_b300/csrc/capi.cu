@@ -454,6 +454,136 @@ mlstm_status mlstm_wait_selftest(void *workspace, size_t ws_bytes, int B, int NH
   return launch_status(launch_wait_selftest((int *)workspace, MLSTM_SELFTEST_WAIT_CODE, (cudaStream_t)stream));
 }
 
+// ---------------------------------------------------------------- backward
+namespace {
+struct BwdLayout {
+  size_t gb, gx, gu, cm, Cs, ns, Gs, Ns, h32, den, invD, cc, pq, pk, total;
+};
+
+BwdLayout bwd_layout(int B, int NH, int S, int DQK, int DV, int chunk) {
+  const size_t P = (size_t)B * NH, NC = (size_t)S / chunk, PS = P * S, nt = (size_t)DQK / 32;
+  BwdLayout L{};
+  size_t off = kAlign;  // offset 0: the error-word header every workspace keeps
+  auto take = [&](size_t &at, size_t floats) {
+    at = off;
+    off = round_up(off + floats * sizeof(float));
+  };
+  take(L.gb, PS);
+  take(L.gx, PS);
+  take(L.gu, PS);
+  take(L.cm, P * (NC + 1));
+  take(L.Cs, P * (NC + 1) * DV * DQK);
+  take(L.ns, P * (NC + 1) * DQK);
+  take(L.Gs, P * (NC + 1) * DV * DQK);
+  take(L.Ns, P * (NC + 1) * DQK);
+  take(L.h32, PS * DV);
+  take(L.den, PS);
+  take(L.invD, PS);
+  take(L.cc, PS);
+  take(L.pq, PS * nt);
+  take(L.pk, PS * nt);
+  L.total = off;
+  return L;
+}
+}  // namespace
+
+size_t mlstm_bwd_workspace_bytes(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) {
+  bool exp_fg;
+  dt = split_forget(dt, exp_fg);
+  if (dt != MLSTM_F32 && dt != MLSTM_BF16) return 0;
+  if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return 0;
+  return bwd_layout(B, NH, S, DQK, DV, chunk).total;
+}
+
+mlstm_status mlstm_bwd_chunkwise(const void *q, const void *k, const void *v, const float *igate_pre,
+                                 const float *fgate_pre, const void *dh, int B, int NH, int S, int DQK, int DV,
+                                 int chunk, mlstm_dtype dt, const float *C_init, const float *n_init,
+                                 const float *m_init, void *dq, void *dk, void *dv, float *dig, float *dfg,
+                                 float *dC_init, float *dn_init, float *dm_init, void *workspace, size_t ws_bytes,
+                                 void *stream) {
+  bool exp_fg;
+  dt = split_forget(dt, exp_fg);
+  if (dt != MLSTM_F32 && dt != MLSTM_BF16) return MLSTM_ERR_DTYPE;
+  if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return MLSTM_ERR_SHAPE;
+  if (S > 0 && (!q || !k || !v || !igate_pre || !fgate_pre || !dh || !dq || !dk || !dv || !dig || !dfg))
+    return MLSTM_ERR_NULL;
+  if (!workspace) return MLSTM_ERR_NULL;
+  if (mlstm_status st = check_init(C_init, n_init, m_init)) return st;
+  const int dgiven = (dC_init != nullptr) + (dn_init != nullptr) + (dm_init != nullptr);
+  if (dgiven != 0 && dgiven != 3) return MLSTM_ERR_NULL;
+  for (const void *ptr : {q, k, v, (const void *)igate_pre, (const void *)fgate_pre, dh, (const void *)dq,
+                          (const void *)dk, (const void *)dv, (const void *)dig, (const void *)dfg,
+                          (const void *)dC_init, (const void *)dn_init, (const void *)dm_init,
+                          (const void *)workspace})
+    if (ptr && !aligned16(ptr)) return MLSTM_ERR_ALIGN;
+  const BwdLayout Lw = bwd_layout(B, NH, S, DQK, DV, chunk);
+  if (ws_bytes < Lw.total) return MLSTM_ERR_WORKSPACE;
+  if (mlstm_status st = check_device()) return st;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  char *ws = (char *)workspace;
+  auto F = [&](size_t off) { return (float *)(ws + off); };
+  const int P = B * NH, NC = S / chunk;
+  const bool bf16 = dt == MLSTM_BF16;
+  if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return launch_status(cudaGetLastError());
+  int kernels = 0;
+  cudaError_t e = cudaSuccess;
+  if (S > 0) {
+    e = launch_gates(igate_pre, fgate_pre, P, S, chunk, m_init, F(Lw.gb), F(Lw.gx), F(Lw.gu), F(Lw.cm), nullptr, s,
+                     exp_fg);
+    ++kernels;
+  } else {
+    // no tokens: the only boundary is the initial one
+    e = m_init ? cudaMemcpyAsync(F(Lw.cm), m_init, sizeof(float) * P, cudaMemcpyDeviceToDevice, s)
+               : cudaMemsetAsync(F(Lw.cm), 0, sizeof(float) * P, s);
+  }
+  if (e == cudaSuccess) {
+    e = launch_states_simt(k, v, bf16, F(Lw.gb), F(Lw.gx), F(Lw.cm), P, S, chunk, DQK, DV, C_init, n_init, F(Lw.Cs),
+                           F(Lw.ns), nullptr, nullptr, s);
+    ++kernels;
+  }
+  if (e == cudaSuccess && S > 0) {
+    e = launch_output_simt(q, k, v, bf16, false, F(Lw.gb), F(Lw.gx), F(Lw.gu), F(Lw.cm), F(Lw.Cs), F(Lw.ns), P, S,
+                           chunk, DQK, DV, F(Lw.h32), s, F(Lw.den));
+    ++kernels;
+  }
+  if (e == cudaSuccess && S > 0) {
+    e = launch_bwd_prep(dh, bf16, F(Lw.h32), F(Lw.den), F(Lw.gb), F(Lw.gu), F(Lw.cm), P, S, chunk, DV, F(Lw.invD),
+                        F(Lw.cc), s);
+    ++kernels;
+  }
+  if (e == cudaSuccess) {
+    e = launch_bwd_states(q, dh, bf16, F(Lw.invD), F(Lw.cc), F(Lw.gb), F(Lw.gu), F(Lw.cm), P, S, chunk, DQK, DV,
+                          F(Lw.Gs), F(Lw.Ns), s);
+    ++kernels;
+  }
+  if (e == cudaSuccess && S > 0) {
+    e = launch_bwd_dqdk(q, k, v, dh, bf16, F(Lw.invD), F(Lw.cc), F(Lw.gb), F(Lw.gx), F(Lw.gu), F(Lw.cm), F(Lw.Cs),
+                        F(Lw.ns), F(Lw.Gs), F(Lw.Ns), P, S, chunk, DQK, DV, dq, dk, F(Lw.pq), F(Lw.pk), s);
+    ++kernels;
+  }
+  if (e == cudaSuccess && S > 0) {
+    e = launch_bwd_dv(q, k, dh, bf16, F(Lw.invD), F(Lw.gb), F(Lw.gx), F(Lw.gu), F(Lw.cm), F(Lw.Gs), P, S, chunk,
+                      DQK, DV, dv, s);
+    ++kernels;
+  }
+  if (e == cudaSuccess) {
+    const size_t gs_stride = (size_t)(NC + 1) * DV * DQK, ns_stride = (size_t)(NC + 1) * DQK;
+    e = launch_bwd_gates(fgate_pre, exp_fg, F(Lw.pq), F(Lw.pk), P, S, DQK / 32, F(Lw.Gs), F(Lw.Ns), gs_stride,
+                         ns_stride, C_init, n_init, DQK, DV, dig, dfg, dm_init, s);
+    ++kernels;
+  }
+  if (e == cudaSuccess && dC_init) {
+    // the adjoint entering boundary 0 is the gradient of the initial state
+    e = cudaMemcpy2DAsync(dC_init, sizeof(float) * DV * DQK, F(Lw.Gs), sizeof(float) * (NC + 1) * DV * DQK,
+                          sizeof(float) * DV * DQK, P, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpy2DAsync(dn_init, sizeof(float) * DQK, F(Lw.Ns), sizeof(float) * (NC + 1) * DQK,
+                            sizeof(float) * DQK, P, cudaMemcpyDeviceToDevice, s);
+  }
+  return launch_status(e, kernels);
+}
+
 mlstm_status mlstm_step(const void *q, const void *k, const void *v, const float *ig, const float *fg,
                         float *C, float *n, float *m, void *h, int B, int NH, int DQK, int DV,
                         mlstm_dtype dt, mlstm_dtype h_dt, void *stream) {

@@ -1076,8 +1076,8 @@ cudaError_t launch_dispatch(int DH, bool pair, const CUtensorMap &mq, const CUte
   return cudaErrorInvalidValue;
 }
 
-// Streaming multiprocessors of the current device (148, a B300's count, when no device can be
-// queried: the path queries also run on hosts without a GPU).
+}  // namespace
+
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
@@ -1086,8 +1086,6 @@ int sm_count() {
   cudaGetLastError();
   return 148;
 }
-
-}  // namespace
 
 bool fwd_tc_supported(int S, int L, int D, int DV, bool bf16) {
   return bf16 && L == kL && (D == 64 || D == 128 || D == 256 || D == 512) && DV % kTile == 0 && S > 0 &&

@@ -5,6 +5,10 @@
 
 namespace mlstm {
 
+// Streaming multiprocessors of the current device (148, a B300's count, when no device can be
+// queried: the path queries also run on hosts without a GPU).
+int sm_count();
+
 // exp_fg selects the exponential forget gate f = exp(f~) (log f = f~) instead of sigmoid(f~).
 //
 // (a) gate preprocessing: per-token b, x, u [P, S] and per-chunk m [P, NC+1].
@@ -18,11 +22,38 @@ cudaError_t launch_states_simt(const void *k, const void *v, bool bf16, const fl
                                int DV, const float *C_init, const float *n_init, float *Cs,
                                float *ns, float *C_last, float *n_last, cudaStream_t stream);
 
-// (c) intra-chunk output on CUDA cores, reading the entering states Cs/ns.
+// (c) intra-chunk output on CUDA cores, reading the entering states Cs/ns; den_out (optional,
+// [P, S]) receives each token's signed denominator n_t . q_t.
 cudaError_t launch_output_simt(const void *q, const void *k, const void *v, bool bf16, bool out_bf16,
                                const float *gb, const float *gx, const float *gu, const float *cm,
                                const float *Cs, const float *ns, int P, int S, int L, int DQK, int DV,
-                               void *h, cudaStream_t stream);
+                               void *h, cudaStream_t stream, float *den_out = nullptr);
+
+// Backward of the chunkwise forward on CUDA cores (bwd_simt.cu), after the gate kernel, the
+// boundary states (Cs, ns) and the output kernel (h in fp32 and den) have run for chunk L:
+//   prep:   per token 1 / D_t and c_t = -(dh_t . h_t) s_t / D_t
+//   states: adjoint states G, N entering every chunk boundary, walking the chunks backwards
+//   dqdk:   dq, dk of every token and the per-tile partial sums of q . dq and k . dk
+//   dv:     dv of every token
+//   gates:  di~, df~ and (with an initial state) dm0
+cudaError_t launch_bwd_prep(const void *dh, bool bf16, const float *h32, const float *den, const float *gb,
+                            const float *gu, const float *cm, int P, int S, int L, int DV, float *invD, float *cc,
+                            cudaStream_t stream);
+cudaError_t launch_bwd_states(const void *q, const void *dh, bool bf16, const float *invD, const float *cc,
+                              const float *gb, const float *gu, const float *cm, int P, int S, int L, int DQK,
+                              int DV, float *Gs, float *Ns, cudaStream_t stream);
+cudaError_t launch_bwd_dqdk(const void *q, const void *k, const void *v, const void *dh, bool bf16,
+                            const float *invD, const float *cc, const float *gb, const float *gx, const float *gu,
+                            const float *cm, const float *Cs, const float *ns, const float *Gs, const float *Ns,
+                            int P, int S, int L, int DQK, int DV, void *dq, void *dk, float *part_q,
+                            float *part_k, cudaStream_t stream);
+cudaError_t launch_bwd_dv(const void *q, const void *k, const void *dh, bool bf16, const float *invD,
+                          const float *gb, const float *gx, const float *gu, const float *cm, const float *Gs,
+                          int P, int S, int L, int DQK, int DV, void *dv, cudaStream_t stream);
+cudaError_t launch_bwd_gates(const float *fg, bool exp_fg, const float *part_q, const float *part_k, int P, int S,
+                             int ntiles, const float *Gs0, const float *Ns0, size_t gs_stride, size_t ns_stride,
+                             const float *C_init, const float *n_init, int DQK, int DV, float *dig, float *dfg,
+                             float *dm_init, cudaStream_t stream);
 
 // (d) single decode step, in place.
 cudaError_t launch_step(const void *q, const void *k, const void *v, bool bf16, bool out_bf16,

@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(256) output_simt_kernel(
     const T *__restrict__ qin, const T *__restrict__ kin, const T *__restrict__ vin,
     const float *__restrict__ gb, const float *__restrict__ gx, const float *__restrict__ gu,
     const float *__restrict__ cm, const float *__restrict__ Cs, const float *__restrict__ ns,
-    int S, int DQK, int DV, TO *__restrict__ h) {
+    int S, int DQK, int DV, TO *__restrict__ h, float *__restrict__ den_out) {
   constexpr int RB = L / 16;  // S-tile rows/cols per thread (16 x 16 thread grid)
   extern __shared__ float smem[];
   float *sP = smem;                        // [L][L+1]   S, then P = S o D
@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(256) output_simt_kernel(
     const float floor_ = expf(-(gb[tbase + r] + mr));
     const float out = (num_in[i] + beta * num_x[i]) / fmaxf(fabsf(den), floor_);
     h[(tbase + r) * DV + a0 + ax] = from_f32<TO>(out);
+    if (den_out != nullptr && blockIdx.y == 0 && ax == 0) den_out[tbase + r] = den;
   }
 }
 
@@ -163,7 +164,7 @@ template <typename T, typename TO, int L>
 static cudaError_t launch_output_simt_t(const void *q, const void *k, const void *v, const float *gb,
                                         const float *gx, const float *gu, const float *cm,
                                         const float *Cs, const float *ns, int P, int S, int DQK,
-                                        int DV, void *h, cudaStream_t stream) {
+                                        int DV, void *h, float *den_out, cudaStream_t stream) {
   constexpr int KR = L > kCols ? L : kCols;
   const size_t smem = sizeof(float) * ((size_t)L * (L + 1) + (size_t)(L + KR) * (kSlab + 1) +
                                        (size_t)L * kCols + 3 * (size_t)L);
@@ -172,7 +173,7 @@ static cudaError_t launch_output_simt_t(const void *q, const void *k, const void
   if (err != cudaSuccess) return err;
   dim3 grid(S / L, DV / kCols, P);
   kern<<<grid, 256, smem, stream>>>((const T *)q, (const T *)k, (const T *)v, gb, gx, gu, cm, Cs,
-                                    ns, S, DQK, DV, (TO *)h);
+                                    ns, S, DQK, DV, (TO *)h, den_out);
   return cudaGetLastError();
 }
 
@@ -180,12 +181,12 @@ template <typename T, typename TO>
 static cudaError_t dispatch_L(int L, const void *q, const void *k, const void *v, const float *gb,
                               const float *gx, const float *gu, const float *cm, const float *Cs,
                               const float *ns, int P, int S, int DQK, int DV, void *h,
-                              cudaStream_t st) {
+                              float *den, cudaStream_t st) {
   switch (L) {
-    case 16: return launch_output_simt_t<T, TO, 16>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, st);
-    case 32: return launch_output_simt_t<T, TO, 32>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, st);
-    case 64: return launch_output_simt_t<T, TO, 64>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, st);
-    case 128: return launch_output_simt_t<T, TO, 128>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, st);
+    case 16: return launch_output_simt_t<T, TO, 16>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den, st);
+    case 32: return launch_output_simt_t<T, TO, 32>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den, st);
+    case 64: return launch_output_simt_t<T, TO, 64>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den, st);
+    case 128: return launch_output_simt_t<T, TO, 128>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -193,16 +194,16 @@ static cudaError_t dispatch_L(int L, const void *q, const void *k, const void *v
 cudaError_t launch_output_simt(const void *q, const void *k, const void *v, bool bf16, bool out_bf16,
                                const float *gb, const float *gx, const float *gu, const float *cm,
                                const float *Cs, const float *ns, int P, int S, int L, int DQK, int DV,
-                               void *h, cudaStream_t stream) {
+                               void *h, cudaStream_t stream, float *den_out) {
   if (P == 0 || S == 0) return cudaSuccess;
   if (bf16) {
     if (out_bf16)
-      return dispatch_L<__nv_bfloat16, __nv_bfloat16>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, stream);
-    return dispatch_L<__nv_bfloat16, float>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, stream);
+      return dispatch_L<__nv_bfloat16, __nv_bfloat16>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den_out, stream);
+    return dispatch_L<__nv_bfloat16, float>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den_out, stream);
   }
   if (out_bf16)
-    return dispatch_L<float, __nv_bfloat16>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, stream);
-  return dispatch_L<float, float>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, stream);
+    return dispatch_L<float, __nv_bfloat16>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den_out, stream);
+  return dispatch_L<float, float>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den_out, stream);
 }
 
 }  // namespace mlstm
