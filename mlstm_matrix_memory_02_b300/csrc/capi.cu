@@ -457,7 +457,7 @@ mlstm_status mlstm_wait_selftest(void *workspace, size_t ws_bytes, int B, int NH
 // ---------------------------------------------------------------- backward
 namespace {
 struct BwdLayout {
-  size_t gb, gx, gu, cm, Cs, ns, Gs, Ns, h32, den, invD, cc, pq, pk, total;
+  size_t gb, gx, gu, cm, Cs, ns, Gs, Ns, h32, den, invD, cc, pq, pk, wx, wn, al, sc, total;
 };
 
 BwdLayout bwd_layout(int B, int NH, int S, int DQK, int DV, int chunk) {
@@ -482,6 +482,10 @@ BwdLayout bwd_layout(int B, int NH, int S, int DQK, int DV, int chunk) {
   take(L.cc, PS);
   take(L.pq, PS * nt);
   take(L.pk, PS * nt);
+  take(L.wx, PS);  // tensor-core state walks: per-token weights and per-chunk factors
+  take(L.wn, PS);
+  take(L.al, P * NC);
+  take(L.sc, P * NC);
   L.total = off;
   return L;
 }
@@ -537,7 +541,18 @@ mlstm_status mlstm_bwd_chunkwise(const void *q, const void *k, const void *v, co
     e = m_init ? cudaMemcpyAsync(F(Lw.cm), m_init, sizeof(float) * P, cudaMemcpyDeviceToDevice, s)
                : cudaMemsetAsync(F(Lw.cm), 0, sizeof(float) * P, s);
   }
-  if (e == cudaSuccess) {
+  // the boundary states walk on tensor cores where the shapes allow (bf16, chunk 64 or 128,
+  // d_qk a power of two from 64, d_v a multiple of 128), on CUDA cores otherwise
+  const bool tc_states = S > 0 && states_tc_supported(chunk, DQK, DV, bf16);
+  int *err = (int *)ws;
+  if (e == cudaSuccess && tc_states) {
+    e = launch_state_weights(0, F(Lw.gb), F(Lw.gx), F(Lw.gu), F(Lw.cm), nullptr, nullptr, P, S, chunk, DQK, F(Lw.wx),
+                             F(Lw.wn), F(Lw.al), F(Lw.sc), s);
+    if (e == cudaSuccess)
+      e = launch_states_tc(v, k, F(Lw.wx), F(Lw.wn), F(Lw.al), F(Lw.sc), P, S, chunk, DQK, DV, false, C_init, n_init,
+                           F(Lw.Cs), F(Lw.ns), nullptr, nullptr, err, s);
+    kernels += 2;
+  } else if (e == cudaSuccess) {
     e = launch_states_simt(k, v, bf16, F(Lw.gb), F(Lw.gx), F(Lw.cm), P, S, chunk, DQK, DV, C_init, n_init, F(Lw.Cs),
                            F(Lw.ns), nullptr, nullptr, s);
     ++kernels;
@@ -552,7 +567,14 @@ mlstm_status mlstm_bwd_chunkwise(const void *q, const void *k, const void *v, co
                         F(Lw.cc), s);
     ++kernels;
   }
-  if (e == cudaSuccess) {
+  if (e == cudaSuccess && tc_states) {
+    e = launch_state_weights(1, F(Lw.gb), F(Lw.gx), F(Lw.gu), F(Lw.cm), F(Lw.invD), F(Lw.cc), P, S, chunk, DQK,
+                             F(Lw.wx), F(Lw.wn), F(Lw.al), F(Lw.sc), s);
+    if (e == cudaSuccess)
+      e = launch_states_tc(dh, q, F(Lw.wx), F(Lw.wn), F(Lw.al), F(Lw.sc), P, S, chunk, DQK, DV, true, nullptr,
+                           nullptr, F(Lw.Gs), F(Lw.Ns), nullptr, nullptr, err, s);
+    kernels += 2;
+  } else if (e == cudaSuccess) {
     e = launch_bwd_states(q, dh, bf16, F(Lw.invD), F(Lw.cc), F(Lw.gb), F(Lw.gu), F(Lw.cm), P, S, chunk, DQK, DV,
                           F(Lw.Gs), F(Lw.Ns), s);
     ++kernels;

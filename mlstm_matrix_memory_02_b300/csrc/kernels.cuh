@@ -50,6 +50,20 @@ cudaError_t launch_bwd_dqdk(const void *q, const void *k, const void *v, const v
 cudaError_t launch_bwd_dv(const void *q, const void *k, const void *dh, bool bf16, const float *invD,
                           const float *gb, const float *gx, const float *gu, const float *cm, const float *Gs,
                           int P, int S, int L, int DQK, int DV, void *dv, cudaStream_t stream);
+// Chunk-boundary states on tensor cores (states_tc.cu): bf16 X [P, S, DV] and Y [P, S, DQK],
+// L a multiple of 64 up to 128, DQK in {64, 128, 256, 512}, DV a multiple of 128, S > 0.  The
+// weights come from launch_state_weights (mode 0: the forward state with X = v, Y = k; mode 1:
+// the adjoint with X = dh, Y = q, needing invD and cc).  Walks the chunks forwards, or
+// backwards with `reverse`, from (C0, n0) (NULL = zero); states/nstates [P, NC+1, ...] and the
+// final C_fin/n_fin are each optional.  Bounded waits record a code in *err.
+bool states_tc_supported(int L, int DQK, int DV, bool bf16);
+cudaError_t launch_state_weights(int mode, const float *gb, const float *gx, const float *gu, const float *cm,
+                                 const float *invD, const float *cc, int P, int S, int L, int DQK, float *wx,
+                                 float *wn, float *alpha, float *sc, cudaStream_t stream);
+cudaError_t launch_states_tc(const void *X, const void *Y, const float *wx, const float *wn, const float *alpha,
+                             const float *sc, int P, int S, int L, int DQK, int DV, bool reverse, const float *C0,
+                             const float *n0, float *states, float *nstates, float *C_fin, float *n_fin, int *err,
+                             cudaStream_t stream);
 cudaError_t launch_bwd_gates(const float *fg, bool exp_fg, const float *part_q, const float *part_k, int P, int S,
                              int ntiles, const float *Gs0, const float *Ns0, size_t gs_stride, size_t ns_stride,
                              const float *C_init, const float *n_init, int DQK, int DV, float *dig, float *dfg,

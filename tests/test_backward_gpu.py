@@ -124,6 +124,34 @@ def test_backward_350m_shape_bf16(B, init):
     run_case(B, W.LAYER_350M.with_(B=1, NH=2, S=256), 64, init=init, conditioned=init)
 
 
+@pytest.mark.parametrize("dqk,dv,s,chunk,init", [(64, 128, 192, 64, False), (128, 256, 256, 128, True),
+                                                 (512, 128, 128, 64, True), (256, 384, 384, 128, False)])
+def test_backward_bf16_tensor_core_states(B, dqk, dv, s, chunk, init):
+    """bf16 shapes whose boundary and adjoint states walk on tensor cores (chunk 64 or 128, d_qk a
+    power of two from 64, d_v a multiple of 128), every d_qk variant of that kernel."""
+    run_case(B, W.LAYER_350M.with_(B=1, NH=2, S=s, DQK=dqk, DV=dv), chunk, init=init, conditioned=init)
+
+
+def test_backward_state_paths_agree(B):
+    """The same bf16 inputs with chunk 32 (states on CUDA cores) and chunk 64 (states on tensor
+    cores): the gradients agree to the bf16 tolerance."""
+    w = W.LAYER_350M.with_(B=1, NH=2, S=256, DQK=128, DV=128)
+    inp = W.make_inputs(w)
+    d = {x: torch.from_numpy(inp[x]).cuda().to(torch.bfloat16).contiguous() for x in ("q", "k", "v")}
+    d.update({x: torch.from_numpy(inp[x]).cuda().contiguous() for x in ("ig", "fg")})
+    dh = torch.from_numpy(upstream(w)).cuda().to(torch.bfloat16)
+    g32, g64 = (B.mlstm_bwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], dh, c) for c in (32, 64))
+    torch.cuda.synchronize()
+    for name in ("dq", "dk", "dv", "dig", "dfg"):
+        a, b = npy(g64[name]), npy(g32[name])
+        if name in ("dq", "dk", "dv"):
+            # both sides are rounded to bf16: twice the one-sided bound
+            bound = 2 * (TOL_BF16 * np.sqrt(np.mean(b * b)) + 2.0 ** -8 * np.abs(b))
+            assert np.all(np.abs(a - b) <= bound), (name, float(np.max(np.abs(a - b) / bound)))
+        else:
+            assert rel_err(a, b) <= TOL_BF16, name
+
+
 def test_backward_stress_gates_fp32(B):
     """Heavy-tailed input gates and weak forget gates (the long-context workload's gate
     distributions) at a small size, fp32."""
