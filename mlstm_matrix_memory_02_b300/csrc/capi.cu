@@ -32,8 +32,8 @@ struct Layout {
   // the sequence-parallel forward's buffers (G segments per head, the fused path only), after
   // `total`: per (head, segment) the sum of log f, the segment's own state and stabiliser, and
   // its entering state
-  size_t Bg, Cseg, nseg, mseg, Cin, nin, min, split_total;
-  int G;
+  size_t Bg, Cseg, nseg, mseg, Cin, nin, min, m1, cmseg, wx, wn, split_total;
+  int G, G1, Ls;  // segments per head (second pass, first pass); the first pass's chunk
   bool tc;  // the forward runs on the fused tensor-core kernel (no materialised states)
 };
 
@@ -73,15 +73,29 @@ Layout layout(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) 
   // which may alias n_init)
   L.ncopy = off; off = round_up(off + (L.tc ? P * DQK : 0) * sizeof(float));
   L.total = off;
-  L.G = L.tc && S > 0 ? fwd_tc_segments((int)P, S, DQK, DV) : 1;
+  L.G = L.tc && S > 0 && states_tc_supported(64, DQK, DV, true) ? fwd_tc_segments((int)P, S, DQK, DV) : 1;
   const size_t PG = L.G > 1 ? P * L.G : 0;
-  L.Bg = off; off = round_up(off + PG * sizeof(float));
-  L.Cseg = off; off = round_up(off + PG * DV * DQK * sizeof(float));
-  L.nseg = off; off = round_up(off + PG * DQK * sizeof(float));
+  // the first pass (states only) fills the GPU with finer segments where that keeps at least
+  // 128 tokens a segment
+  L.G1 = L.G;
+  if (L.G > 1) {
+    const long long ctas = (long long)P * (DV / 128);
+    while (ctas * 2 * L.G1 <= sm_count() && S % (64 * 2 * L.G1) == 0 && S / (2 * L.G1) >= 128) L.G1 *= 2;
+  }
+  const size_t PG1 = L.G > 1 ? P * L.G1 : 0;
+  L.Ls = L.G > 1 && (S / L.G1) % 128 == 0 ? 128 : 64;
+  const size_t PS1 = L.G > 1 ? P * (size_t)S : 0, NC1 = L.G > 1 ? PS1 / L.Ls : 0;
+  L.Bg = off; off = round_up(off + PG1 * sizeof(float));
+  L.Cseg = off; off = round_up(off + PG1 * DV * DQK * sizeof(float));
+  L.nseg = off; off = round_up(off + PG1 * DQK * sizeof(float));
   L.mseg = off; off = round_up(off + PG * sizeof(float));
   L.Cin = off; off = round_up(off + PG * DV * DQK * sizeof(float));
   L.nin = off; off = round_up(off + PG * DQK * sizeof(float));
   L.min = off; off = round_up(off + PG * sizeof(float));
+  L.m1 = off; off = round_up(off + PG1 * sizeof(float));
+  L.cmseg = off; off = round_up(off + (NC1 + PG1) * sizeof(float));  // PG1 chains of S / (G1 Ls) + 1
+  L.wx = off; off = round_up(off + PS1 * sizeof(float));
+  L.wn = off; off = round_up(off + PS1 * sizeof(float));
   L.split_total = off;
   return L;
 }
@@ -239,34 +253,38 @@ static mlstm_status check_fwd_args(const void *q, const void *k, const void *v, 
 }
 
 // The fused forward over G segments of each head's sequence at once, for long sequences over
-// few heads: a first pass runs every segment (segment 0 from the caller's initial state, the
-// others from the zero state with m = -inf), a scan composes the segments' maps into the true
-// entering state of every segment and the final state, and a second pass reruns segments
-// 1..G-1 from their entering states, overwriting their h.  Each (head, segment) is a head of
-// S / G tokens to the fused kernel: the token-major arrays need no copies.
+// few heads: a first pass computes the own map of each of G1 >= G finer segments from the zero
+// state with m = -inf (gate preprocessing and the tensor-core state walk over P G1 heads of
+// S / G1 tokens, final state only), a scan composes the maps from the caller's initial state
+// into the entering state of each of the G segments and the final state, and the fused kernel
+// then runs all P G segments from their entering states.  Each (head, segment) is a head of S / G tokens to the kernels: the
+// token-major arrays need no copies.
 static mlstm_status run_segments(const void *q, const void *k, const void *v, const Layout &Lw, int P, int S,
                                  int DQK, int DV, const float *C_init, const float *n_init, const float *m_init,
                                  const float *ig, const float *fg, bool exp_fg, void *h, mlstm_dtype h_dt,
                                  float *C_last, float *n_last, float *m_last, char *ws, cudaStream_t s) {
-  const int G = Lw.G, PG = P * G, Sg = S / G;
-  float *Bg = (float *)(ws + Lw.Bg), *Cseg = (float *)(ws + Lw.Cseg), *nseg = (float *)(ws + Lw.nseg);
-  float *mseg = (float *)(ws + Lw.mseg), *Cin = (float *)(ws + Lw.Cin), *nin = (float *)(ws + Lw.nin);
-  float *min = (float *)(ws + Lw.min);
-  float *gb = (float *)(ws + Lw.gb), *gx = (float *)(ws + Lw.gx), *gu = (float *)(ws + Lw.gu);
-  float *cm = (float *)(ws + Lw.cm);
+  const int G = Lw.G, PG = P * G, Sg = S / G, G1 = Lw.G1, PG1 = P * G1, Sg1 = S / G1, Ls = Lw.Ls;
+  auto F = [&](size_t off) { return (float *)(ws + off); };
   int *err = (int *)(ws + Lw.err);
   const bool hb = h_dt == MLSTM_BF16;
-  if (mlstm_status st = launch_status(launch_seg_init(C_init, n_init, m_init, fg, exp_fg, P, G, Sg, DQK, DV, Cin,
-                                                      nin, min, Bg, s)))
-    return st;
-  if (mlstm_status st = launch_status(launch_fwd_tc(q, k, v, hb, gb, gx, gu, cm, ig, fg, min, PG, Sg, DQK, DV, Cin,
-                                                    nin, h, Cseg, nseg, mseg, err, s, exp_fg, P, 0)))
-    return st;
-  if (mlstm_status st = launch_status(launch_seg_scan(P, G, DQK, DV, Bg, Cseg, nseg, mseg, Cin, nin, min, C_last,
-                                                      n_last, m_last, s)))
-    return st;
-  return launch_status(launch_fwd_tc(q, k, v, hb, gb, gx, gu, cm, ig, fg, min, PG, Sg, DQK, DV, Cin, nin, h, Cseg,
-                                     nseg, mseg, err, s, exp_fg, P, G));
+  cudaError_t e = launch_seg_init(fg, exp_fg, P, G1, Sg1, F(Lw.m1), F(Lw.Bg), s);
+  if (e == cudaSuccess)
+    e = launch_gates(ig, fg, PG1, Sg1, Ls, F(Lw.m1), F(Lw.gb), F(Lw.gx), F(Lw.gu), F(Lw.cmseg), nullptr, s, exp_fg);
+  if (e == cudaSuccess)
+    e = launch_state_weights(2, F(Lw.gb), F(Lw.gx), F(Lw.gu), F(Lw.cmseg), nullptr, nullptr, PG1, Sg1, Ls, DQK,
+                             F(Lw.wx), F(Lw.wn), nullptr, nullptr, s);
+  if (e == cudaSuccess)
+    e = launch_states_tc(v, k, F(Lw.wx), F(Lw.wn), nullptr, nullptr, PG1, Sg1, Ls, DQK, DV, false, nullptr, nullptr,
+                         nullptr, nullptr, F(Lw.Cseg), F(Lw.nseg), err, s);
+  if (e == cudaSuccess)
+    e = launch_seg_scan(P, G1, G1 / G, DQK, DV, Sg1 / Ls, F(Lw.Bg), F(Lw.Cseg), F(Lw.nseg), F(Lw.cmseg), C_init,
+                        n_init, m_init, F(Lw.Cin), F(Lw.nin), F(Lw.min), C_last, n_last, m_last, s);
+  if (e != cudaSuccess) return launch_status(e);
+  if (mlstm_status st = launch_status(cudaSuccess, 5)) return st;
+  // the segments' own final states land in the first pass's buffers, which are free by now
+  return launch_status(launch_fwd_tc(q, k, v, hb, F(Lw.gb), F(Lw.gx), F(Lw.gu), F(Lw.cm), ig, fg, F(Lw.min), PG,
+                                     Sg, DQK, DV, F(Lw.Cin), F(Lw.nin), h, F(Lw.Cseg), F(Lw.nseg), F(Lw.mseg), err, s,
+                                     exp_fg, P));
 }
 
 // Everything after kernel (a), on a workspace that kernel (a) has filled for these sizes -- or,

@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
     const float *__restrict__ cm, const float *__restrict__ igp, const float *__restrict__ fgp,
     const float *__restrict__ m_init, int S, int DV, float scale, const float *__restrict__ C_init,
     const float *__restrict__ n_init, TO *__restrict__ h, float *__restrict__ n_last, float *__restrict__ m_last,
-    int *__restrict__ err, int exp_fg, int seg_skip) {
+    int *__restrict__ err, int exp_fg) {
   constexpr int D = PAIR ? 2 * DH : DH;  // d_qk
   constexpr int QB = DH * 128;           // bytes of a [64 x DH] 2-byte tile (DH / 64 swizzled blocks)
   constexpr uint32_t kColC16 = DH;
@@ -196,11 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = PAIR ? (int)cluster_ctarank() : 0;
   const int atile = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  // head index; with seg_skip = G > 1 the grid covers segments 1..G-1 of each group of G
-  // consecutive heads (the sequence-parallel forward's second pass)
-  const int p = seg_skip > 1 ? (int)(blockIdx.y / (seg_skip - 1)) * seg_skip + 1 + (int)(blockIdx.y % (seg_skip - 1))
-                             : (int)blockIdx.y;
-  const int a0 = atile * kTile, c0 = rank * DH;
+  const int a0 = atile * kTile, c0 = rank * DH, p = blockIdx.y;
   const int NC = S / kL;
   const int r_lo = PAIR ? 32 * rank : 0;  // first output row finalised here
   const int prt = 1 - rank;
@@ -1035,13 +1031,13 @@ cudaError_t launch_one(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
                        const float *gb, const float *gx, const float *gu, const float *cm, const float *ig,
                        const float *fg, const float *m_init, int P, int S, int DV, float scale,
                        const float *C_init, const float *n_init, void *h, float *n_last, float *m_last, int *err,
-                       int exp_fg, int seg_skip, cudaStream_t stream) {
+                       int exp_fg, cudaStream_t stream) {
   auto kern = fwd_tc_kernel<DH, PAIR, TO>;
   const size_t smem = smem_bytes<DH, PAIR>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((DV / kTile) * (PAIR ? 2 : 1), seg_skip > 1 ? P / seg_skip * (seg_skip - 1) : P, 1);
+  cfg.gridDim = dim3((DV / kTile) * (PAIR ? 2 : 1), P, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -1053,7 +1049,7 @@ cudaError_t launch_one(const CUtensorMap &mq, const CUtensorMap &mk, const CUten
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mc, gb, gx, gu, cm, ig, fg, m_init, S, DV, scale, C_init, n_init,
-                            static_cast<TO *>(h), n_last, m_last, err, exp_fg, seg_skip);
+                            static_cast<TO *>(h), n_last, m_last, err, exp_fg);
 }
 
 template <typename TO>
@@ -1061,11 +1057,11 @@ cudaError_t launch_dispatch(int DH, bool pair, const CUtensorMap &mq, const CUte
                             const CUtensorMap &mc, const float *gb, const float *gx, const float *gu,
                             const float *cm, const float *ig, const float *fg, const float *m_init, int P, int S,
                             int DV, float scale, const float *C_init, const float *n_init, void *h, float *n_last,
-                            float *m_last, int *err, int exp_fg, int seg_skip, cudaStream_t stream) {
+                            float *m_last, int *err, int exp_fg, cudaStream_t stream) {
 #define MLSTM_TC_CASE(dh_, pr_)                                                                                  \
   if (DH == dh_ && pair == pr_)                                                                                  \
     return launch_one<dh_, pr_, TO>(mq, mk, mv, mc, gb, gx, gu, cm, ig, fg, m_init, P, S, DV, scale, C_init,    \
-                                    n_init, h, n_last, m_last, err, exp_fg, seg_skip, stream);
+                                    n_init, h, n_last, m_last, err, exp_fg, stream);
   MLSTM_TC_CASE(64, false)
   MLSTM_TC_CASE(128, false)
   MLSTM_TC_CASE(256, false)
@@ -1112,7 +1108,7 @@ cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, bool out_
                           const float *gx, const float *gu, const float *cm, const float *ig, const float *fg,
                           const float *m_init, int P, int S, int D, int DV, const float *C_init,
                           const float *n_init, void *h, float *C_last, float *n_last, float *m_last, int *err,
-                          cudaStream_t stream, bool exp_fg, int pair_heads, int seg_skip) {
+                          cudaStream_t stream, bool exp_fg, int pair_heads) {
   // the CTA-pair decision is that of the caller's head count (the segmented passes keep it)
   const bool pair = fwd_tc_pair(pair_heads > 0 ? pair_heads : P, D, DV);
   const int DH = pair ? D / 2 : D;
@@ -1124,9 +1120,9 @@ cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, bool out_
   const float scale = (float)(1.0 / __builtin_sqrt((double)D));
   if (out_bf16)
     return launch_dispatch<__nv_bfloat16>(DH, pair, mq, mk, mv, mc, gb, gx, gu, cm, ig, fg, m_init, P, S, DV, scale,
-                                          C_init, n_init, h, n_last, m_last, err, exp_fg ? 1 : 0, seg_skip, stream);
+                                          C_init, n_init, h, n_last, m_last, err, exp_fg ? 1 : 0, stream);
   return launch_dispatch<float>(DH, pair, mq, mk, mv, mc, gb, gx, gu, cm, ig, fg, m_init, P, S, DV, scale, C_init,
-                                n_init, h, n_last, m_last, err, exp_fg ? 1 : 0, seg_skip, stream);
+                                n_init, h, n_last, m_last, err, exp_fg ? 1 : 0, stream);
 }
 
 }  // namespace mlstm

@@ -53,9 +53,11 @@ cudaError_t launch_bwd_dv(const void *q, const void *k, const void *dh, bool bf1
 // Chunk-boundary states on tensor cores (states_tc.cu): bf16 X [P, S, DV] and Y [P, S, DQK],
 // L a multiple of 64 up to 128, DQK in {64, 128, 256, 512}, DV a multiple of 128, S > 0.  The
 // weights come from launch_state_weights (mode 0: the forward state with X = v, Y = k; mode 1:
-// the adjoint with X = dh, Y = q, needing invD and cc).  Walks the chunks forwards, or
-// backwards with `reverse`, from (C0, n0) (NULL = zero); states/nstates [P, NC+1, ...] and the
-// final C_fin/n_fin are each optional.  Bounded waits record a code in *err.
+// the adjoint with X = dh, Y = q, needing invD and cc; mode 2: the final forward state alone,
+// with no per-chunk factors).  Walks the chunks forwards, or backwards with `reverse`, from
+// (C0, n0) (NULL = zero); states/nstates [P, NC+1, ...] and the final C_fin/n_fin are each
+// optional.  With alpha == NULL (mode 2 weights) only C_fin/n_fin are written, from the zero
+// state, forwards.  Bounded waits record a code in *err.
 bool states_tc_supported(int L, int DQK, int DV, bool bf16);
 cudaError_t launch_state_weights(int mode, const float *gb, const float *gx, const float *gu, const float *cm,
                                  const float *invD, const float *cc, int P, int S, int L, int DQK, float *wx,
@@ -86,17 +88,18 @@ cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, bool out_
                           const float *gx, const float *gu, const float *cm, const float *ig, const float *fg,
                           const float *m_init, int P, int S, int D, int DV, const float *C_init,
                           const float *n_init, void *h, float *C_last, float *n_last, float *m_last, int *err,
-                          cudaStream_t stream, bool exp_fg = false, int pair_heads = 0, int seg_skip = 0);
+                          cudaStream_t stream, bool exp_fg = false, int pair_heads = 0);
 // The sequence-parallel forward's helpers (seq_split.cu), for G segments of Sg tokens per head:
-// entering states of the first pass (the caller's initial state for segment 0, the zero state with
-// m = -inf for the others) and every segment's sum of log f (Bg, P*G floats) ...
-cudaError_t launch_seg_init(const float *C_init, const float *n_init, const float *m_init, const float *fg,
-                            bool exp_fg, int P, int G, int Sg, int DQK, int DV, float *Cin, float *nin, float *min,
-                            float *Bg, cudaStream_t stream);
-// ... and the scan that composes the segments' maps into every segment's entering state and the
-// final state.
-cudaError_t launch_seg_scan(int P, int G, int DQK, int DV, const float *Bg, const float *Cseg, const float *nseg,
-                            const float *mseg, float *Cin, float *nin, float *min, float *C_last, float *n_last,
+// every segment's sum of log f (Bg, P*G floats) and m = -inf as its first-pass entering
+// stabiliser (min) ...
+cudaError_t launch_seg_init(const float *fg, bool exp_fg, int P, int G, int Sg, float *min, float *Bg,
+                            cudaStream_t stream);
+// ... and the scan that composes the G segments' maps (their states Cseg, nseg and the last
+// entry of their chunk stabiliser chains cm, NCg + 1 per segment) from the initial state into
+// the entering state of every R-th segment (Cin, nin, min: G / R per head) and the final state.
+cudaError_t launch_seg_scan(int P, int G, int R, int DQK, int DV, int NCg, const float *Bg, const float *Cseg,
+                            const float *nseg, const float *cm, const float *C_init, const float *n_init,
+                            const float *m_init, float *Cin, float *nin, float *min, float *C_last, float *n_last,
                             float *m_last, cudaStream_t stream);
 
 // (d') T consecutive decode steps in one launch, in place (T <= step_multi_max_tokens()).

@@ -32,16 +32,22 @@ using namespace sm100;
 
 constexpr int kSub = 64;      // tokens per slab (one TMA stage)
 constexpr int kTileM = 128;   // rows of DV per CTA (tensor-memory lanes)
-constexpr int kStagesT = 2;   // slabs in flight
-constexpr int kThreadsT = 320;
+// slabs in flight: four (two chunks of 128 tokens) where shared memory allows, else two
+template <int NQ>
+__host__ __device__ constexpr int stages_for() { return NQ <= 4 ? 4 : 2; }
+constexpr int kConvT = 256;  // conversion threads (warps 6-13)
+constexpr int kThreadsT = 192 + kConvT;
 // warp 0: TMA loads; warp 1: tensor-memory allocation and MMA issue; warps 2-5: epilogue
-// (tensor-memory lanes 32 (w % 4) .. + 31); warps 6-9: conversion and the n vector.
+// (tensor-memory lanes 32 (w % 4) .. + 31); warps 6-13: conversion and the n vector.
 
 template <int NQ>  // DQK / 64
 struct alignas(1024) StatesSmem {
-  unsigned char tile[kStagesT][(2 + NQ) * 8192];  // X boxes 0, 1 then NQ Y boxes, 64 x 128 B each
-  uint64_t full[kStagesT], conv[kStagesT], empty[kStagesT];
+  static constexpr int ST = stages_for<NQ>();
+  unsigned char tile[ST][(2 + NQ) * 8192];  // X boxes 0, 1 then NQ Y boxes, 64 x 128 B each
+  uint64_t full[ST], conv[ST], empty[ST];
   uint64_t mma_done, epi_ready, fin;
+  float wx[ST][64];  // the slab's X weights
+  float wn[ST][64];  // the slab's n weights
   uint32_t tmem_base;
   int abort_flag;
   int conv_fail;  // written by the conversion warps only, read by them after a barrier
@@ -60,12 +66,16 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
   constexpr int NN = DQK > 256 ? 2 : 1;  // MMAs per K step (N <= 256 each)
   constexpr int NB = DQK / NN;           // N of each
   constexpr uint32_t kCols = DQK < 32 ? 32 : DQK;
+  constexpr int ST = stages_for<NQ>();
   extern __shared__ unsigned char st_raw[];
   StatesSmem<NQ> &sm = *reinterpret_cast<StatesSmem<NQ> *>(
       (reinterpret_cast<uintptr_t>(st_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int p = blockIdx.y, a0 = blockIdx.x * kTileM;
   const int NC = S / L, SUB = L / kSub, NS = S / kSub;
+  // without per-chunk factors the walk keeps only the final state: the weights already carry
+  // each token's decay to the end of the sequence (no rescaling between chunks, no stores)
+  const bool final_only = alpha == nullptr;
   int *abort_ptr = &sm.abort_flag;
   // slab j (in walking order) is slab sub(j) of the sequence; chunk i of the walk is chunk kc(i)
   auto kc_of = [&](int i) { return reverse ? NC - 1 - i : i; };
@@ -75,9 +85,9 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
   };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStagesT; ++s) {
+    for (int s = 0; s < ST; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.conv[s], 128);
+      mbar_init(&sm.conv[s], kConvT);
       mbar_init(&sm.empty[s], 1);
     }
     mbar_init(&sm.mma_done, 1);
@@ -103,8 +113,8 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
       prefetch_tensormap(&mapY);
       int issued = 0;
       for (int j = 0; j < NS; ++j) {
-        const int s = j & 1;
-        if (j >= kStagesT && !mbar_wait(&sm.empty[s], ((j >> 1) - 1) & 1, err, 41, abort_ptr)) break;
+        const int s = j % ST;
+        if (j >= ST && !mbar_wait(&sm.empty[s], ((j / ST) - 1) & 1, err, 41, abort_ptr)) break;
         if (st_aborted(abort_ptr)) break;
         const int row = p * S + sub_of(j) * kSub;
         mbar_arrive_expect_tx(&sm.full[s], (uint32_t)(2 + NQ) * 8192u);
@@ -114,8 +124,8 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
         issued = j + 1;
       }
       // nothing may leave while loads it issued are still landing
-      for (int j = issued > kStagesT ? issued - kStagesT : 0; j < issued; ++j)
-        mbar_wait(&sm.full[j & 1], (j >> 1) & 1, err, 49);
+      for (int j = issued > ST ? issued - ST : 0; j < issued; ++j)
+        mbar_wait(&sm.full[j % ST], (j / ST) & 1, err, 49);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issue
@@ -124,13 +134,13 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
       int j = 0;
       bool ok = true;
       for (int i = 0; i < NC && ok; ++i) {
-        if (!mbar_wait(&sm.epi_ready, i & 1, err, 42, abort_ptr)) {
+        if (!final_only && !mbar_wait(&sm.epi_ready, i & 1, err, 42, abort_ptr)) {
           ok = false;
           break;
         }
         for (int r = 0; r < SUB; ++r, ++j) {
-          const int s = j & 1;
-          if (!mbar_wait(&sm.conv[s], (j >> 1) & 1, err, 43, abort_ptr)) {
+          const int s = j % ST;
+          if (!mbar_wait(&sm.conv[s], (j / ST) & 1, err, 43, abort_ptr)) {
             ok = false;
             break;
           }
@@ -142,11 +152,13 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
 #pragma unroll
             for (int h = 0; h < NN; ++h)
               mma_f16_ss(tm + h * NB, dx + (uint64_t)(ks * 2048 >> 4),
-                         dy + (uint64_t)((ks * 2048 + h * (NB / 64) * 8192) >> 4), id, 1);
+                         dy + (uint64_t)((ks * 2048 + h * (NB / 64) * 8192) >> 4), id,
+                         final_only ? ((j | ks) != 0) : 1);
           mma_commit(&sm.empty[s]);
         }
-        if (ok) mma_commit(&sm.mma_done);
+        if (ok && !final_only) mma_commit(&sm.mma_done);
       }
+      if (ok && final_only) mma_commit(&sm.mma_done);
       if (!ok) st_set_abort(abort_ptr);
       mma_commit(&sm.fin);  // completes once every MMA issued above has finished
       mbar_wait(&sm.fin, 0, err, 48);
@@ -159,10 +171,35 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
     auto boundary_row = [&](int b) { return Crow_states + (size_t)b * DV * DQK; };
     float s_prev = 1.f;
     bool ok = true;
-    for (int i = 0; i <= NC && ok; ++i) {
+    if (final_only) {
+      // one read of T after the last slab: the final state
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&sm.mma_done, 0, err, 44, abort_ptr));
+      if (got) {
+        tc_fence_after();
+        for (int c0 = 0; c0 < DQK; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(trow + c0, r);
+          tmem_wait_ld();
+          float *dst = C_fin + ((size_t)p * DV + a0 + row) * DQK + c0;
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4 *>(dst + e) = make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
+                                                               __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+        }
+      } else {
+        ok = false;
+      }
+    }
+    // the chunk's decay and scale, loaded one chunk ahead (they sit on the serial chain)
+    float a_nxt = !final_only && NC > 0 ? alpha[(size_t)p * NC + kc_of(0)] : 0.f;
+    float s_nxt = !final_only && NC > 0 ? sc[(size_t)p * NC + kc_of(0)] : 1.f;
+    for (int i = 0; i <= NC && ok && !final_only; ++i) {
       const int b_in = reverse ? NC - i : i;  // boundary whose state T holds now
-      const int kc = i < NC ? kc_of(i) : 0;
-      const float s_cur = i < NC ? sc[(size_t)p * NC + kc] : 1.f;
+      const float s_cur = i < NC ? s_nxt : 1.f, a_cur = a_nxt;
+      if (i + 1 < NC) {
+        a_nxt = alpha[(size_t)p * NC + kc_of(i + 1)];
+        s_nxt = sc[(size_t)p * NC + kc_of(i + 1)];
+      }
       if (i > 0) {
         // the whole warp takes the same branch before its collective tensor-memory loads
         const bool got = __all_sync(0xffffffffu, mbar_wait(&sm.mma_done, (i - 1) & 1, err, 44, abort_ptr));
@@ -203,7 +240,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
         if (i < NC) {
           // T for the next chunk: alpha_k times the state, in units of s_k
 #pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(v[e] * (alpha[(size_t)p * NC + kc] / s_cur));
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(v[e] * (a_cur / s_cur));
           tmem_st16(trow + c0, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
           tmem_st16(trow + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
         }
@@ -218,20 +255,20 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
     if (!ok) st_set_abort(abort_ptr);
   } else {
     // ------------------------------------------------------------------ conversion and n
-    const int ct = threadIdx.x - 192;  // 0..127
+    const int ct = threadIdx.x - 192;  // 0 .. kConvT - 1
     const bool do_n = blockIdx.x == 0 && (nstates != nullptr || n_fin != nullptr);
-    constexpr int NPT = (DQK + 127) / 128;  // n columns per thread
+    constexpr int NPT = (DQK + kConvT - 1) / kConvT;  // n columns per thread
     float nacc[NPT];
 #pragma unroll
     for (int u = 0; u < NPT; ++u) {
-      const int c = ct + 128 * u;
+      const int c = ct + kConvT * u;
       nacc[u] = (n0 != nullptr && c < DQK) ? n0[(size_t)p * DQK + c] : 0.f;
     }
     auto store_n = [&](int b) {
       if (!do_n) return;
 #pragma unroll
       for (int u = 0; u < NPT; ++u) {
-        const int c = ct + 128 * u;
+        const int c = ct + kConvT * u;
         if (c < DQK) {
           if (nstates) nstates[((size_t)p * (NC + 1) + b) * DQK + c] = nacc[u];
         }
@@ -242,46 +279,58 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
     for (int i = 0; i < NC && ok; ++i) {
       const int kc = kc_of(i);
       store_n(reverse ? NC - i : i);
-      const float al = alpha[(size_t)p * NC + kc];
+      const float al = final_only ? 1.f : alpha[(size_t)p * NC + kc];
 #pragma unroll
       for (int u = 0; u < NPT; ++u) nacc[u] *= al;
       for (int r = 0; r < SUB; ++r, ++j) {
-        const int s = j & 1;
+        const int s = j % ST;
         // every conversion thread passes each named barrier, so a wait that gives up in one of
         // them is shared through conv_fail before anyone acts on it
-        if (!mbar_wait(&sm.full[s], (j >> 1) & 1, err, 45, abort_ptr)) *(volatile int *)&sm.conv_fail = 1;
-        named_barrier_sync(1, 128);
+        const size_t tok0 = (size_t)p * S + (size_t)(kc * SUB + r) * kSub;
+        // the slab's weights, staged once (both were read by the previous use of this stage
+        // before the barriers of the slabs since)
+        if (ct < kSub) sm.wx[s][ct] = wx[tok0 + ct];
+        else if (do_n && ct < 2 * kSub) sm.wn[s][ct - kSub] = wn[tok0 + ct - kSub];
+        if (!mbar_wait(&sm.full[s], (j / ST) & 1, err, 45, abort_ptr)) *(volatile int *)&sm.conv_fail = 1;
+        named_barrier_sync(1, kConvT);
         if (*(volatile int *)&sm.conv_fail) {
           ok = false;
           break;
         }
-        const size_t tok0 = (size_t)p * S + (size_t)(kc * SUB + r) * kSub;
         unsigned char *tile = sm.tile[s];
         if (do_n) {
-          // n += sum_t omega'_t y_t, read from the bf16 slab before it is converted
+          // n += sum_t omega'_t y_t, read from the bf16 slab before it is converted (eight
+          // independent partial sums per column)
 #pragma unroll
           for (int u = 0; u < NPT; ++u) {
-            const int c = ct + 128 * u;
+            const int c = ct + kConvT * u;
             if (c < DQK) {
               const unsigned char *box = tile + (2 + c / 64) * 8192;
               const int ch = (c & 63) >> 3, el = c & 7;
-              float acc = 0.f;
-              for (int t = 0; t < kSub; ++t) {
-                const __nv_bfloat16 y =
-                    *reinterpret_cast<const __nv_bfloat16 *>(box + t * 128 + ((ch ^ (t & 7)) << 4) + 2 * el);
-                acc = fmaf(wn[tok0 + t], __bfloat162float(y), acc);
-              }
-              nacc[u] += acc;
+              float acc[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+              for (int t0 = 0; t0 < kSub; t0 += 8)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const int t = t0 + e;  // t & 7 == e
+                  const __nv_bfloat16 y =
+                      *reinterpret_cast<const __nv_bfloat16 *>(box + t * 128 + ((ch ^ e) << 4) + 2 * el);
+                  acc[e] = fmaf(sm.wn[s][t], __bfloat162float(y), acc[e]);
+                }
+              nacc[u] += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
             }
           }
         }
-        named_barrier_sync(1, 128);  // every read of the bf16 slab is done
+        named_barrier_sync(1, kConvT);  // every read of the bf16 slab is done
         // X: 2 boxes x 64 rows x 8 pieces of 16 bytes; row = token, scaled by its weight
-        for (int pc = ct; pc < 2 * 64 * 8; pc += 128) {
+#pragma unroll
+        for (int pc = ct; pc < 2 * 64 * 8; pc += kConvT) {
           const int t = (pc & 511) >> 3;
           uint4 *ptr = reinterpret_cast<uint4 *>(tile + pc * 16);
           const uint4 raw = *ptr;
-          const float w = wx[tok0 + t];
+          const float w = sm.wx[s][t];
           const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
           uint32_t out[4];
 #pragma unroll
@@ -293,7 +342,8 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
           *ptr = make_uint4(out[0], out[1], out[2], out[3]);
         }
         // Y: NQ boxes, converted as they are
-        for (int pc = ct; pc < NQ * 64 * 8; pc += 128) {
+#pragma unroll
+        for (int pc = ct; pc < NQ * 64 * 8; pc += kConvT) {
           uint4 *ptr = reinterpret_cast<uint4 *>(tile + 2 * 8192 + pc * 16);
           const uint4 raw = *ptr;
           const uint32_t in[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -314,7 +364,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
       if (n_fin) {
 #pragma unroll
         for (int u = 0; u < NPT; ++u) {
-          const int c = ct + 128 * u;
+          const int c = ct + kConvT * u;
           if (c < DQK) n_fin[(size_t)p * DQK + c] = nacc[u];
         }
       }
@@ -331,7 +381,9 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
 }
 
 // Per-token weights and per-chunk factors of the state recurrences (one CTA per (chunk, head),
-// one thread per token).  mode 0, the forward state C^(k): omega = omega' = w_t / sqrt(d) with
+// one thread per token).  mode 2, the final forward state only: omega = omega' = the weight of
+// token t in the final state, exp(i~_t + sum_{tau > t} log f_tau - m_S) / sqrt(d), and no
+// per-chunk factors.  mode 0, the forward state C^(k): omega = omega' = w_t / sqrt(d) with
 // the state-update weight w_t = exp(b_L + x_t - m^(k+1)); mode 1, the adjoint G^(k):
 // omega = beta_t / D_t, omega' = beta_t c_t with beta_t = exp(m^(k) - max(m^(k), u_t)).  Both:
 // alpha_k = exp(b_L + m^(k) - m^(k+1)); omega is stored divided by s_k, the power of two at or
@@ -348,6 +400,21 @@ __global__ void state_weights_kernel(int mode, const float *__restrict__ gb, con
   const float m_in = cm[(size_t)p * (NC + 1) + kc], m_out = cm[(size_t)p * (NC + 1) + kc + 1];
   const float bl = gb[tb + L - 1];
   float w, w2;
+  if (mode == 2) {
+    // the decay of every later chunk folded in: b from the end of this chunk to the end of the
+    // sequence, against the final stabiliser (every weight <= 1, the largest exactly 1)
+    __shared__ float s_after;
+    if (t == 0) {
+      float acc = 0.f;
+      for (int j = kc + 1; j < NC; ++j) acc += gb[(size_t)p * S + (size_t)j * L + L - 1];
+      s_after = acc;
+    }
+    __syncthreads();
+    w = rsqrtf((float)DQK) * expf(bl + s_after + gx[tb + t] - cm[(size_t)p * (NC + 1) + NC]);
+    wx[tb + t] = w;
+    wn[tb + t] = w;
+    return;
+  }
   if (mode == 0) {
     w = rsqrtf((float)DQK) * expf(bl + gx[tb + t] - m_out);
     w2 = w;

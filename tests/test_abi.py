@@ -107,8 +107,9 @@ def _segments_expected(P, S, D, DV):
                                            (1, 2, 512, 64, 128), (1, 2, 448, 256, 256)])
 def test_sequence_parallel_selection(lib, b, nh, s, dqk, dv):
     """Long sequences over few heads run in G parallel segments when the workspace holds the
-    segment buffers (per (head, segment) two fp32 states C, n, m and a float); the least
-    workspace runs them whole, and the CUDA-core path never splits."""
+    segment buffers (per (head, segment) two fp32 states C, n, m and a float, per token two
+    weights, per first-pass chunk a few floats); the least workspace runs them whole, and the
+    CUDA-core path never splits."""
     ws, ws_min, seg = lib.mlstm_fwd_workspace_bytes, lib.mlstm_fwd_workspace_min_bytes, lib.mlstm_fwd_segments
     G = _segments_expected(b * nh, s, dqk, dv)
     full, least = ws(b, nh, s, dqk, dv, 64, 1), ws_min(b, nh, s, dqk, dv, 64, 1)
@@ -117,9 +118,15 @@ def test_sequence_parallel_selection(lib, b, nh, s, dqk, dv):
     assert seg(b, nh, s, dqk, dv, 64, 1, full - 1) == (1 if G > 1 else G)
     assert seg(b, nh, s, dqk, dv, 64, 0, 1 << 40) == 1  # fp32 inputs: CUDA-core kernels
     if G > 1:
-        per_segment = 2 * (dv * dqk + dqk + 1) * 4 + 4
-        assert full - least >= b * nh * G * per_segment
-        assert full - least <= b * nh * G * per_segment + 7 * 256
+        # first-pass segments: finer where the GPU has room, at least 128 tokens each
+        G1 = G
+        while b * nh * (dv // 128) * 2 * G1 <= _sms() and s % (64 * 2 * G1) == 0 and s // (2 * G1) >= 128:
+            G1 *= 2
+        per_state = (dv * dqk + dqk + 1) * 4  # C, n, m
+        per_token = 2 * 4                     # two weights
+        least_extra = b * nh * ((G + G1) * per_state + s * per_token)
+        slack = b * nh * (3 * 4 * G1 + 4 * G + 4 * (s // 64)) + 14 * 256  # B, m1, chains, round-ups
+        assert least_extra <= full - least <= least_extra + slack
     else:
         assert full == least
     assert seg(1, 2, 100, 64, 64, 64, 1, 1 << 30) == -1  # S % chunk != 0
