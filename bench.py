@@ -291,8 +291,9 @@ def time_layer(B, w, dev, args, flush, peaks):
     """One more forward workload, timed like the headline (L2 flushed between calls, CUDA events
     around each call), with h in the dtype of v (bf16) as the layer hands it on.  The 350M-style
     layer is HBM-bound (its roofline is HBM of algorithmic bytes); the long-context layer runs in
-    sequence segments on the tensor-core path (4 launches: segment init, first pass, scan, second
-    pass) and is reported against HBM as well, with its tensor-core fraction beside it."""
+    sequence segments on the tensor-core path (6 launches: segment init, gate preprocessing,
+    weights and tensor-core state walk of the first pass, scan, fused kernel) and is reported
+    against HBM as well, with its tensor-core fraction beside it."""
     import torch
     inp = W.make_inputs(w)
     q, k, v = (torch.from_numpy(inp[x]).to(dev).to(torch.bfloat16) for x in ("q", "k", "v"))
@@ -338,10 +339,56 @@ def time_layer(B, w, dev, args, flush, peaks):
                          "frac": gbs / peaks["hbm_gbs"],
                          "traffic": captured_traffic(f"forward@{key}"),
                          "kernel": ("fwd_tc_kernel (one launch)" if G == 1 else
-                                    f"whole forward: seg_init, fwd_tc_kernel x2 ({G} segments), seg_scan"),
+                                    f"whole forward in {G} segments: seg_init, gates, state_weights, "
+                                    "states_tc (first pass), seg_scan, fwd_tc_kernel"),
                          "algorithmic_bytes_per_launch": nbytes,
                          "peak_source": peaks["source"] + " HBM copy",
                          "tensor_tflops": tf, "tensor_frac": tf / peaks["bf16_tflops"]},
+            "gpu_launches": int(launches)}
+
+
+def time_backward(B, w, dev, args, flush, peaks):
+    """The chunkwise backward (mlstm_bwd_chunkwise) of a layer for a random upstream gradient,
+    bf16 q/k/v/dh and gradients, L2 flushed between calls.  Reported against the tensor-core
+    peak with twice the forward's algorithmic flops (the usual backward-to-forward ratio of a
+    layer built from products: each forward product has two gradient products)."""
+    import torch
+    inp = W.make_inputs(w)
+    q, k, v = (torch.from_numpy(inp[x]).to(dev).to(torch.bfloat16) for x in ("q", "k", "v"))
+    ig, fg = (torch.from_numpy(inp[x]).to(dev) for x in ("ig", "fg"))
+    del inp
+    g = torch.Generator(device=dev).manual_seed(21)
+    dh = torch.randn((w.B, w.NH, w.S, w.DV), device=dev, generator=g).to(torch.bfloat16)
+    ws = torch.empty(B.mlstm_bwd_workspace_bytes(w.B, w.NH, w.S, w.DQK, w.DV, w.chunk), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(args.warmup, 3)):
+        B.mlstm_bwd_chunkwise(q, k, v, ig, fg, dh, w.chunk, workspace=ws)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
+    l0 = B.mlstm_kernel_launches()
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        B.mlstm_bwd_chunkwise(q, k, v, ig, fg, dh, w.chunk, workspace=ws)
+        b.record(stream)
+    torch.cuda.synchronize()
+    launches = B.mlstm_kernel_launches() - l0
+    B.mlstm_fwd_check(ws, w.B, w.NH, w.S, w.DQK, w.DV, w.chunk)  # the error word sits at offset 0 here too
+    us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+    flops = 2 * fwd_flops(w)
+    tf = flops / (us * 1e-6) / 1e12
+    return {"metric": f"mLSTM chunkwise backward tokens/s ({w.name})", "value": w.B * w.S / (us * 1e-6),
+            "unit": "tokens/s", "us_per_launch": us,
+            "config": {"workload": w.name, "B": w.B, "NH": w.NH, "S": w.S, "DQK": w.DQK, "DV": w.DV,
+                       "chunk": w.chunk, "qkv_dh_grads": "bf16", "gates": "fp32",
+                       "state_walks": "tensor cores (tcgen05)", "chunk_products": "CUDA cores, fp32",
+                       "l2": "flushed between timed calls"},
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": tf / peaks["bf16_tflops"], "traffic": None,
+                         "algorithmic_flops_per_launch": flops,
+                         "kernel": "whole backward (gates, state walks, output recompute, chunk gradients)",
+                         "peak_source": f"{peaks['source']} bf16 dense (burst)"},
             "gpu_launches": int(launches)}
 
 
@@ -518,7 +565,8 @@ def run_ours(args, rank, local, world):
 
     # ---- the other forward workloads: the 350M-style layer and the long-context layer
     layers = {"layer_350m": time_layer(B, W.LAYER_350M, dev, args, flush, peaks),
-              "stress": time_layer(B, W.STRESS_16K, dev, args, flush, peaks)}
+              "stress": time_layer(B, W.STRESS_16K, dev, args, flush, peaks),
+              "backward_350m": time_backward(B, W.LAYER_350M, dev, args, flush, peaks)}
 
     # ---- end to end through the public API: pinned host inputs in, h back to the host
     pin = {key: torch.from_numpy(inp[key]).to(torch.bfloat16 if key in "qkv" else torch.float32).pin_memory()
@@ -562,12 +610,14 @@ def run_ours(args, rank, local, world):
         "block_epilogue": block_epilogue,
         "layer_350m": layers["layer_350m"],
         "stress": layers["stress"],
+        "backward_350m": layers["backward_350m"],
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches_fwd),
         "gpu_launches_other": {"decode": int(launches_dec), "block_epilogue": int(launches_gn),
                                "layer_350m": layers["layer_350m"]["gpu_launches"],
-                               "stress": layers["stress"]["gpu_launches"]},
+                               "stress": layers["stress"]["gpu_launches"],
+                               "backward_350m": layers["backward_350m"]["gpu_launches"]},
         "clocks": clk.summary(),
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -587,7 +637,8 @@ def run_profile(kind: str):
                   long-context layer in sequence segments)
     decode:       one decode step of the B=256, NH=8, d=256 state (state initialised randomly)
     decode_multi: 16 decode steps in one launch on the same state
-    gn:           group norm + output gate on a 1.3B-layer-shaped h (fp32 h, bf16 o~ and y)"""
+    gn:           group norm + output gate on a 1.3B-layer-shaped h (fp32 h, bf16 o~ and y)
+    bwd:          the chunkwise backward of the 350M-style layer (bf16)"""
     import torch
     from mlstm_matrix_memory_02_b300 import binding as B
     dev = torch.device("cuda", 0)
@@ -600,6 +651,15 @@ def run_profile(kind: str):
         h_dtype = torch.float32 if w is W.LAYER_1P3B else torch.bfloat16
         for _ in range(2):
             B.mlstm_fwd_chunkwise(q, k, v, ig, fg, w.chunk, h_dtype=h_dtype)
+    elif kind == "bwd":
+        w = W.LAYER_350M
+        inp = W.make_inputs(w)
+        q, k, v = (torch.from_numpy(inp[x]).to(dev).to(torch.bfloat16) for x in ("q", "k", "v"))
+        ig, fg = (torch.from_numpy(inp[x]).to(dev) for x in ("ig", "fg"))
+        g = torch.Generator(device=dev).manual_seed(21)
+        dh = torch.randn((w.B, w.NH, w.S, w.DV), device=dev, generator=g).to(torch.bfloat16)
+        for _ in range(2):
+            B.mlstm_bwd_chunkwise(q, k, v, ig, fg, dh, w.chunk)
     elif kind == "gn":
         w = FWD
         g = torch.Generator(device=dev).manual_seed(3)
@@ -648,7 +708,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["1p3b", "350m", "stress"], default="1p3b",
                     help="forward workload (default: the 1.3B-style layer)")
-    ap.add_argument("--profile", choices=["fwd", "decode", "decode_multi", "gn"], default=None,
+    ap.add_argument("--profile", choices=["fwd", "decode", "decode_multi", "gn", "bwd"], default=None,
                     help="run one small forward or decode step for ncu captures and exit")
     args = ap.parse_args()
     global FWD
