@@ -63,8 +63,9 @@ def dec_bytes(w, h_bytes=4) -> float:
 
 def captured_traffic(kernel: str):
     """DRAM bytes per launch of `kernel` (an entry of profiles/traffic.json: a kernel name, or
-    kernel@workload) from the committed ncu summary, or None when the kernel's source has
-    changed since that capture."""
+    forward@workload / backward@workload for a call of several kernels) from the committed ncu
+    summary, or None when one of its sources has changed since that capture (the entry holds a
+    hash of the listed source files)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
@@ -73,9 +74,11 @@ def captured_traffic(kernel: str):
         entry = json.load(f).get(kernel)
     if not entry:
         return None
-    with open(os.path.join(ROOT, entry["source"]), "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
-    return float(entry["dram_bytes"]) if sha == entry["sha"] else None
+    h = hashlib.sha256()
+    for src in entry.get("sources", [entry.get("source")]):
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    return float(entry["dram_bytes"]) if h.hexdigest()[:16] == entry["sha"] else None
 
 
 def load_peaks():
@@ -385,7 +388,7 @@ def time_backward(B, w, dev, args, flush, peaks):
                        "state_walks": "tensor cores (tcgen05)", "chunk_products": "CUDA cores, fp32",
                        "l2": "flushed between timed calls"},
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": tf / peaks["bf16_tflops"], "traffic": None,
+                         "frac": tf / peaks["bf16_tflops"], "traffic": captured_traffic("backward@350m"),
                          "algorithmic_flops_per_launch": flops,
                          "kernel": "whole backward (gates, state walks, output recompute, chunk gradients)",
                          "peak_source": f"{peaks['source']} bf16 dense (burst)"},
