@@ -162,7 +162,8 @@ __global__ void __launch_bounds__(256) bwd_dqdk_kernel(
     const float *__restrict__ gx, const float *__restrict__ gu, const float *__restrict__ cm,
     const float *__restrict__ Cs, const float *__restrict__ ns, const float *__restrict__ Gs,
     const float *__restrict__ Ns, int S, int DQK, int DV, T *__restrict__ dq, T *__restrict__ dk,
-    float *__restrict__ part_q, float *__restrict__ part_k) {
+    float *__restrict__ part_q, float *__restrict__ part_k, const float *__restrict__ yq,
+    const float *__restrict__ yk) {
   constexpr int RB = L / 16;  // L x L tile entries per thread (16 x 16 thread grid)
   constexpr int RR = L / 8;   // output rows per thread (8 x 32 thread grid)
   constexpr int KR = L > kSlab ? L : kSlab;
@@ -253,7 +254,7 @@ __global__ void __launch_bounds__(256) bwd_dqdk_kernel(
   // ---- inter-chunk parts: g C^(k) (entering state) and v G^(k+1) (adjoint from the right)
   const float *Ck = Cs + ((size_t)p * (NC + 1) + kc) * (size_t)DV * DQK;
   const float *Gk = Gs + ((size_t)p * (NC + 1) + kc + 1) * (size_t)DV * DQK;
-  for (int pass = 0; pass < 2; ++pass) {
+  for (int pass = 0; pass < 2 && yq == nullptr; ++pass) {
     const float *St = pass == 0 ? Ck : Gk;
     for (int a0 = 0; a0 < DV; a0 += kSlab) {
       __syncthreads();
@@ -285,6 +286,10 @@ __global__ void __launch_bounds__(256) bwd_dqdk_kernel(
   for (int i = 0; i < RR; ++i) {
     const int u = ry + 8 * i;
     const size_t at = (tbase + u) * DQK + c0 + cx;
+    if (yq != nullptr) {
+      dq_x[i] = yq[at];
+      dk_x[i] = yk[at];
+    }
     const float dqv = dq_in[i] + sBeta[u] * (dq_x[i] + sC[u] * nk);
     const float dkv = scale * (dk_in[i] + sW[u] * (dk_x[i] + Nk));
     dq[at] = from_f32<T>(dqv);
@@ -305,7 +310,8 @@ template <typename T, int L>
 __global__ void __launch_bounds__(256) bwd_dv_kernel(
     const T *__restrict__ qin, const T *__restrict__ kin, const T *__restrict__ dh, const float *__restrict__ invD,
     const float *__restrict__ gb, const float *__restrict__ gx, const float *__restrict__ gu,
-    const float *__restrict__ cm, const float *__restrict__ Gs, int S, int DQK, int DV, T *__restrict__ dv) {
+    const float *__restrict__ cm, const float *__restrict__ Gs, int S, int DQK, int DV, T *__restrict__ dv,
+    const float *__restrict__ yv) {
   constexpr int RB = L / 16;
   constexpr int RR = L / 8;
   constexpr int KR = L > kSlab ? L : kSlab;
@@ -382,7 +388,7 @@ __global__ void __launch_bounds__(256) bwd_dv_kernel(
     for (int i = 0; i < RR; ++i) dv_in[i] = fmaf(sM[u * (L + 1) + ry + 8 * i], gu_a, dv_in[i]);
   }
   const float *Gk = Gs + ((size_t)p * (NC + 1) + kc + 1) * (size_t)DV * DQK;
-  for (int c0 = 0; c0 < DQK; c0 += kSlab) {
+  for (int c0 = 0; c0 < DQK && yv == nullptr; c0 += kSlab) {
     __syncthreads();
     for (int e = tid; e < L * kSlab; e += blockDim.x) {
       const int r = e / kSlab, c = e - r * kSlab;
@@ -403,6 +409,7 @@ __global__ void __launch_bounds__(256) bwd_dv_kernel(
 #pragma unroll
   for (int i = 0; i < RR; ++i) {
     const int t = ry + 8 * i;
+    if (yv != nullptr) dv_x[i] = yv[(tbase + t) * DV + a0 + ax];
     dv[(tbase + t) * DV + a0 + ax] = from_f32<T>(dv_in[i] + sW[t] * dv_x[i]);
   }
 }
@@ -476,7 +483,20 @@ __global__ void __launch_bounds__(256) bwd_gates_kernel(
   }
 }
 
+// ---------------------------------------------------------------- bf16 (or fp32) to fp32
+__global__ void to_f32_kernel(const void *__restrict__ src, int bf16, float *__restrict__ dst, size_t n) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = bf16 ? __bfloat162float(static_cast<const __nv_bfloat16 *>(src)[i]) : static_cast<const float *>(src)[i];
+}
+
 // ---------------------------------------------------------------- launchers
+cudaError_t launch_to_f32(const void *src, bool bf16, float *dst, size_t n, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const size_t blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+  to_f32_kernel<<<(unsigned)blocks, 256, 0, stream>>>(src, bf16 ? 1 : 0, dst, n);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_prep(const void *dh, bool bf16, const float *h32, const float *den, const float *gb,
                             const float *gu, const float *cm, int P, int S, int L, int DV, float *invD, float *cc,
                             cudaStream_t stream) {
@@ -517,27 +537,27 @@ template <typename T, int L>
 cudaError_t dqdk_t(const void *q, const void *k, const void *v, const void *dh, const float *invD, const float *cc,
                    const float *gb, const float *gx, const float *gu, const float *cm, const float *Cs,
                    const float *ns, const float *Gs, const float *Ns, int P, int S, int DQK, int DV, void *dq,
-                   void *dk, float *part_q, float *part_k, cudaStream_t stream) {
+                   void *dk, float *part_q, float *part_k, const float *yq, const float *yk, cudaStream_t stream) {
   auto kern = bwd_dqdk_kernel<T, L>;
   const size_t smem = chunk_smem<L>(6);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<dim3(S / L, DQK / kCols, P), 256, smem, stream>>>((const T *)q, (const T *)k, (const T *)v, (const T *)dh,
                                                            invD, cc, gb, gx, gu, cm, Cs, ns, Gs, Ns, S, DQK, DV,
-                                                           (T *)dq, (T *)dk, part_q, part_k);
+                                                           (T *)dq, (T *)dk, part_q, part_k, yq, yk);
   return cudaGetLastError();
 }
 
 template <typename T, int L>
 cudaError_t dv_t(const void *q, const void *k, const void *dh, const float *invD, const float *gb, const float *gx,
                  const float *gu, const float *cm, const float *Gs, int P, int S, int DQK, int DV, void *dv,
-                 cudaStream_t stream) {
+                 const float *yv, cudaStream_t stream) {
   auto kern = bwd_dv_kernel<T, L>;
   const size_t smem = chunk_smem<L>(4);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<dim3(S / L, DV / kCols, P), 256, smem, stream>>>((const T *)q, (const T *)k, (const T *)dh, invD, gb, gx,
-                                                          gu, cm, Gs, S, DQK, DV, (T *)dv);
+                                                          gu, cm, Gs, S, DQK, DV, (T *)dv, yv);
   return cudaGetLastError();
 }
 }  // namespace
@@ -546,11 +566,11 @@ cudaError_t launch_bwd_dqdk(const void *q, const void *k, const void *v, const v
                             const float *invD, const float *cc, const float *gb, const float *gx, const float *gu,
                             const float *cm, const float *Cs, const float *ns, const float *Gs, const float *Ns,
                             int P, int S, int L, int DQK, int DV, void *dq, void *dk, float *part_q,
-                            float *part_k, cudaStream_t stream) {
+                            float *part_k, cudaStream_t stream, const float *yq, const float *yk) {
   if (P == 0 || S == 0) return cudaSuccess;
 #define MLSTM_BWD_DQDK(T_, L_)                                                                                   \
   return dqdk_t<T_, L_>(q, k, v, dh, invD, cc, gb, gx, gu, cm, Cs, ns, Gs, Ns, P, S, DQK, DV, dq, dk, part_q, \
-                        part_k, stream)
+                        part_k, yq, yk, stream)
   if (bf16) {
     switch (L) {
       case 16: MLSTM_BWD_DQDK(__nv_bfloat16, 16);
@@ -572,9 +592,9 @@ cudaError_t launch_bwd_dqdk(const void *q, const void *k, const void *v, const v
 
 cudaError_t launch_bwd_dv(const void *q, const void *k, const void *dh, bool bf16, const float *invD,
                           const float *gb, const float *gx, const float *gu, const float *cm, const float *Gs,
-                          int P, int S, int L, int DQK, int DV, void *dv, cudaStream_t stream) {
+                          int P, int S, int L, int DQK, int DV, void *dv, cudaStream_t stream, const float *yv) {
   if (P == 0 || S == 0) return cudaSuccess;
-#define MLSTM_BWD_DV(T_, L_) return dv_t<T_, L_>(q, k, dh, invD, gb, gx, gu, cm, Gs, P, S, DQK, DV, dv, stream)
+#define MLSTM_BWD_DV(T_, L_) return dv_t<T_, L_>(q, k, dh, invD, gb, gx, gu, cm, Gs, P, S, DQK, DV, dv, yv, stream)
   if (bf16) {
     switch (L) {
       case 16: MLSTM_BWD_DV(__nv_bfloat16, 16);

@@ -475,12 +475,16 @@ mlstm_status mlstm_wait_selftest(void *workspace, size_t ws_bytes, int B, int NH
 // ---------------------------------------------------------------- backward
 namespace {
 struct BwdLayout {
-  size_t gb, gx, gu, cm, Cs, ns, Gs, Ns, h32, den, invD, cc, pq, pk, wx, wn, al, sc, total;
+  size_t gb, gx, gu, cm, Cs, ns, Gs, Ns, h32, den, invD, cc, pq, pk, wx, wn, al, sc;
+  size_t Cst, Gst, q32, k32, v32, dh32, xq, yq, yk, yv, total;
+  bool tc_states, tc_prod;  // state walks / state products on tensor cores
 };
 
-BwdLayout bwd_layout(int B, int NH, int S, int DQK, int DV, int chunk) {
+BwdLayout bwd_layout(int B, int NH, int S, int DQK, int DV, int chunk, bool bf16) {
   const size_t P = (size_t)B * NH, NC = (size_t)S / chunk, PS = P * S, nt = (size_t)DQK / 32;
   BwdLayout L{};
+  L.tc_states = S > 0 && states_tc_supported(chunk, DQK, DV, bf16);
+  L.tc_prod = L.tc_states && state_prod_supported(chunk, DQK, DV);
   size_t off = kAlign;  // offset 0: the error-word header every workspace keeps
   auto take = [&](size_t &at, size_t floats) {
     at = off;
@@ -504,6 +508,18 @@ BwdLayout bwd_layout(int B, int NH, int S, int DQK, int DV, int chunk) {
   take(L.wn, PS);
   take(L.al, P * NC);
   take(L.sc, P * NC);
+  // tensor-core state products: transposed states, fp32 copies of the tokens, the products
+  const size_t SQ = L.tc_prod ? P * (NC + 1) * DV * DQK : 0, TQ = L.tc_prod ? PS * DQK : 0, TV = L.tc_prod ? PS * DV : 0;
+  take(L.Cst, SQ);
+  take(L.Gst, SQ);
+  take(L.q32, TQ);
+  take(L.k32, TQ);
+  take(L.v32, TV);
+  take(L.dh32, TV);
+  take(L.xq, TV);
+  take(L.yq, TQ);
+  take(L.yk, TQ);
+  take(L.yv, TV);
   L.total = off;
   return L;
 }
@@ -514,7 +530,7 @@ size_t mlstm_bwd_workspace_bytes(int B, int NH, int S, int DQK, int DV, int chun
   dt = split_forget(dt, exp_fg);
   if (dt != MLSTM_F32 && dt != MLSTM_BF16) return 0;
   if (!sizes_ok(B, NH, S, DQK, DV, chunk)) return 0;
-  return bwd_layout(B, NH, S, DQK, DV, chunk).total;
+  return bwd_layout(B, NH, S, DQK, DV, chunk, dt == MLSTM_BF16).total;
 }
 
 mlstm_status mlstm_bwd_chunkwise(const void *q, const void *k, const void *v, const float *igate_pre,
@@ -538,7 +554,7 @@ mlstm_status mlstm_bwd_chunkwise(const void *q, const void *k, const void *v, co
                           (const void *)dC_init, (const void *)dn_init, (const void *)dm_init,
                           (const void *)workspace})
     if (ptr && !aligned16(ptr)) return MLSTM_ERR_ALIGN;
-  const BwdLayout Lw = bwd_layout(B, NH, S, DQK, DV, chunk);
+  const BwdLayout Lw = bwd_layout(B, NH, S, DQK, DV, chunk, dt == MLSTM_BF16);
   if (ws_bytes < Lw.total) return MLSTM_ERR_WORKSPACE;
   if (mlstm_status st = check_device()) return st;
 
@@ -560,16 +576,28 @@ mlstm_status mlstm_bwd_chunkwise(const void *q, const void *k, const void *v, co
                : cudaMemsetAsync(F(Lw.cm), 0, sizeof(float) * P, s);
   }
   // the boundary states walk on tensor cores where the shapes allow (bf16, chunk 64 or 128,
-  // d_qk a power of two from 64, d_v a multiple of 128), on CUDA cores otherwise
-  const bool tc_states = S > 0 && states_tc_supported(chunk, DQK, DV, bf16);
+  // d_qk a power of two from 64, d_v a multiple of 128), on CUDA cores otherwise; with d_qk a
+  // multiple of 128 too, the products of the tokens with the states also run on tensor cores
+  const bool tc_states = Lw.tc_states, tc_prod = Lw.tc_prod;
   int *err = (int *)ws;
   if (e == cudaSuccess && tc_states) {
     e = launch_state_weights(0, F(Lw.gb), F(Lw.gx), F(Lw.gu), F(Lw.cm), nullptr, nullptr, P, S, chunk, DQK, F(Lw.wx),
                              F(Lw.wn), F(Lw.al), F(Lw.sc), s);
     if (e == cudaSuccess)
       e = launch_states_tc(v, k, F(Lw.wx), F(Lw.wn), F(Lw.al), F(Lw.sc), P, S, chunk, DQK, DV, false, C_init, n_init,
-                           F(Lw.Cs), F(Lw.ns), nullptr, nullptr, err, s);
+                           F(Lw.Cs), F(Lw.ns), nullptr, nullptr, err, s, tc_prod ? F(Lw.Cst) : nullptr);
     kernels += 2;
+  }
+  if (e == cudaSuccess && tc_prod) {
+    // fp32 copies of the tokens (the tf32 operands), then C^(k) q_t for every token
+    const size_t nq = (size_t)P * S * DQK, nv = (size_t)P * S * DV;
+    e = launch_to_f32(q, bf16, F(Lw.q32), nq, s);
+    if (e == cudaSuccess) e = launch_to_f32(k, bf16, F(Lw.k32), nq, s);
+    if (e == cudaSuccess) e = launch_to_f32(v, bf16, F(Lw.v32), nv, s);
+    if (e == cudaSuccess) e = launch_to_f32(dh, bf16, F(Lw.dh32), nv, s);
+    if (e == cudaSuccess)
+      e = launch_state_prod(F(Lw.Cs), DV, DQK, 0, F(Lw.q32), nullptr, 1.f, P, S, chunk, F(Lw.xq), err, s);
+    kernels += 5;
   } else if (e == cudaSuccess) {
     e = launch_states_simt(k, v, bf16, F(Lw.gb), F(Lw.gx), F(Lw.cm), P, S, chunk, DQK, DV, C_init, n_init, F(Lw.Cs),
                            F(Lw.ns), nullptr, nullptr, s);
@@ -577,7 +605,7 @@ mlstm_status mlstm_bwd_chunkwise(const void *q, const void *k, const void *v, co
   }
   if (e == cudaSuccess && S > 0) {
     e = launch_output_simt(q, k, v, bf16, false, F(Lw.gb), F(Lw.gx), F(Lw.gu), F(Lw.cm), F(Lw.Cs), F(Lw.ns), P, S,
-                           chunk, DQK, DV, F(Lw.h32), s, F(Lw.den));
+                           chunk, DQK, DV, F(Lw.h32), s, F(Lw.den), tc_prod ? F(Lw.xq) : nullptr);
     ++kernels;
   }
   if (e == cudaSuccess && S > 0) {
@@ -590,8 +618,18 @@ mlstm_status mlstm_bwd_chunkwise(const void *q, const void *k, const void *v, co
                              F(Lw.wx), F(Lw.wn), F(Lw.al), F(Lw.sc), s);
     if (e == cudaSuccess)
       e = launch_states_tc(dh, q, F(Lw.wx), F(Lw.wn), F(Lw.al), F(Lw.sc), P, S, chunk, DQK, DV, true, nullptr,
-                           nullptr, F(Lw.Gs), F(Lw.Ns), nullptr, nullptr, err, s);
+                           nullptr, F(Lw.Gs), F(Lw.Ns), nullptr, nullptr, err, s, tc_prod ? F(Lw.Gst) : nullptr);
     kernels += 2;
+  }
+  if (e == cudaSuccess && tc_prod) {
+    // C^(k)^T g_t = C^(k)^T dh_t / D_t, G^(k+1)^T v_t and G^(k+1) khat_t for every token
+    e = launch_state_prod(F(Lw.Cst), DQK, DV, 0, F(Lw.dh32), F(Lw.invD), 1.f, P, S, chunk, F(Lw.yq), err, s);
+    if (e == cudaSuccess)
+      e = launch_state_prod(F(Lw.Gst), DQK, DV, 1, F(Lw.v32), nullptr, 1.f, P, S, chunk, F(Lw.yk), err, s);
+    if (e == cudaSuccess)
+      e = launch_state_prod(F(Lw.Gs), DV, DQK, 1, F(Lw.k32), nullptr, 1.f / sqrtf((float)DQK), P, S, chunk,
+                            F(Lw.yv), err, s);
+    kernels += 3;
   } else if (e == cudaSuccess) {
     e = launch_bwd_states(q, dh, bf16, F(Lw.invD), F(Lw.cc), F(Lw.gb), F(Lw.gu), F(Lw.cm), P, S, chunk, DQK, DV,
                           F(Lw.Gs), F(Lw.Ns), s);
@@ -599,12 +637,13 @@ mlstm_status mlstm_bwd_chunkwise(const void *q, const void *k, const void *v, co
   }
   if (e == cudaSuccess && S > 0) {
     e = launch_bwd_dqdk(q, k, v, dh, bf16, F(Lw.invD), F(Lw.cc), F(Lw.gb), F(Lw.gx), F(Lw.gu), F(Lw.cm), F(Lw.Cs),
-                        F(Lw.ns), F(Lw.Gs), F(Lw.Ns), P, S, chunk, DQK, DV, dq, dk, F(Lw.pq), F(Lw.pk), s);
+                        F(Lw.ns), F(Lw.Gs), F(Lw.Ns), P, S, chunk, DQK, DV, dq, dk, F(Lw.pq), F(Lw.pk), s,
+                        tc_prod ? F(Lw.yq) : nullptr, tc_prod ? F(Lw.yk) : nullptr);
     ++kernels;
   }
   if (e == cudaSuccess && S > 0) {
     e = launch_bwd_dv(q, k, dh, bf16, F(Lw.invD), F(Lw.gb), F(Lw.gx), F(Lw.gu), F(Lw.cm), F(Lw.Gs), P, S, chunk,
-                      DQK, DV, dv, s);
+                      DQK, DV, dv, s, tc_prod ? F(Lw.yv) : nullptr);
     ++kernels;
   }
   if (e == cudaSuccess) {

@@ -23,11 +23,12 @@ cudaError_t launch_states_simt(const void *k, const void *v, bool bf16, const fl
                                float *ns, float *C_last, float *n_last, cudaStream_t stream);
 
 // (c) intra-chunk output on CUDA cores, reading the entering states Cs/ns; den_out (optional,
-// [P, S]) receives each token's signed denominator n_t . q_t.
+// [P, S]) receives each token's signed denominator n_t . q_t; xq (optional, [P, S, DV]) holds
+// C^(k) q_t for every token, computed elsewhere, in place of the kernel's own product.
 cudaError_t launch_output_simt(const void *q, const void *k, const void *v, bool bf16, bool out_bf16,
                                const float *gb, const float *gx, const float *gu, const float *cm,
                                const float *Cs, const float *ns, int P, int S, int L, int DQK, int DV,
-                               void *h, cudaStream_t stream, float *den_out = nullptr);
+                               void *h, cudaStream_t stream, float *den_out = nullptr, const float *xq = nullptr);
 
 // Backward of the chunkwise forward on CUDA cores (bwd_simt.cu), after the gate kernel, the
 // boundary states (Cs, ns) and the output kernel (h in fp32 and den) have run for chunk L:
@@ -42,14 +43,18 @@ cudaError_t launch_bwd_prep(const void *dh, bool bf16, const float *h32, const f
 cudaError_t launch_bwd_states(const void *q, const void *dh, bool bf16, const float *invD, const float *cc,
                               const float *gb, const float *gu, const float *cm, int P, int S, int L, int DQK,
                               int DV, float *Gs, float *Ns, cudaStream_t stream);
+// With yq, yk (dqdk) or yv (dv) given ([P, S, DQK] or [P, S, DV]: C^(k)^T g_t, G^(k+1)^T v_t,
+// G^(k+1) khat_t computed elsewhere), the kernels read them instead of forming those products.
 cudaError_t launch_bwd_dqdk(const void *q, const void *k, const void *v, const void *dh, bool bf16,
                             const float *invD, const float *cc, const float *gb, const float *gx, const float *gu,
                             const float *cm, const float *Cs, const float *ns, const float *Gs, const float *Ns,
                             int P, int S, int L, int DQK, int DV, void *dq, void *dk, float *part_q,
-                            float *part_k, cudaStream_t stream);
+                            float *part_k, cudaStream_t stream, const float *yq = nullptr,
+                            const float *yk = nullptr);
 cudaError_t launch_bwd_dv(const void *q, const void *k, const void *dh, bool bf16, const float *invD,
                           const float *gb, const float *gx, const float *gu, const float *cm, const float *Gs,
-                          int P, int S, int L, int DQK, int DV, void *dv, cudaStream_t stream);
+                          int P, int S, int L, int DQK, int DV, void *dv, cudaStream_t stream,
+                          const float *yv = nullptr);
 // Chunk-boundary states on tensor cores (states_tc.cu): bf16 X [P, S, DV] and Y [P, S, DQK],
 // L a multiple of 64 up to 128, DQK in {64, 128, 256, 512}, DV a multiple of 128, S > 0.  The
 // weights come from launch_state_weights (mode 0: the forward state with X = v, Y = k; mode 1:
@@ -62,10 +67,20 @@ bool states_tc_supported(int L, int DQK, int DV, bool bf16);
 cudaError_t launch_state_weights(int mode, const float *gb, const float *gx, const float *gu, const float *cm,
                                  const float *invD, const float *cc, int P, int S, int L, int DQK, float *wx,
                                  float *wn, float *alpha, float *sc, cudaStream_t stream);
+// states_t (optional) receives every boundary state transposed, [P, NC+1, DQK, DV].
 cudaError_t launch_states_tc(const void *X, const void *Y, const float *wx, const float *wn, const float *alpha,
                              const float *sc, int P, int S, int L, int DQK, int DV, bool reverse, const float *C0,
                              const float *n0, float *states, float *nstates, float *C_fin, float *n_fin, int *err,
-                             cudaStream_t stream);
+                             cudaStream_t stream, float *states_t = nullptr);
+// Products of every 64-token slab with the state at its chunk's boundary (+ bshift) on tensor
+// cores (state_prod_tc.cu, tf32): Out[t][r] = scale (tok_scale[t]) sum_c A[r][c] Y[t][c], with A
+// the states [P, S/L + 1, MA, K] fp32 and Y [P, S, K] fp32; L a multiple of 64, MA and K
+// multiples of 128.
+bool state_prod_supported(int L, int DQK, int DV);
+cudaError_t launch_state_prod(const float *A, int MA, int K, int bshift, const float *Y, const float *tok_scale,
+                              float scale, int P, int S, int L, float *out, int *err, cudaStream_t stream);
+// bf16 or fp32 elements to fp32.
+cudaError_t launch_to_f32(const void *src, bool bf16, float *dst, size_t n, cudaStream_t stream);
 cudaError_t launch_bwd_gates(const float *fg, bool exp_fg, const float *part_q, const float *part_k, int P, int S,
                              int ntiles, const float *Gs0, const float *Ns0, size_t gs_stride, size_t ns_stride,
                              const float *C_init, const float *n_init, int DQK, int DV, float *dig, float *dfg,

@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(256) output_simt_kernel(
     const T *__restrict__ qin, const T *__restrict__ kin, const T *__restrict__ vin,
     const float *__restrict__ gb, const float *__restrict__ gx, const float *__restrict__ gu,
     const float *__restrict__ cm, const float *__restrict__ Cs, const float *__restrict__ ns,
-    int S, int DQK, int DV, TO *__restrict__ h, float *__restrict__ den_out) {
+    int S, int DQK, int DV, TO *__restrict__ h, float *__restrict__ den_out, const float *__restrict__ xq) {
   constexpr int RB = L / 16;  // S-tile rows/cols per thread (16 x 16 thread grid)
   extern __shared__ float smem[];
   float *sP = smem;                        // [L][L+1]   S, then P = S o D
@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(256) output_simt_kernel(
 #pragma unroll
     for (int i = 0; i < RR; ++i) num_in[i] = fmaf(sP[(ry + 8 * i) * (L + 1) + j], vv, num_in[i]);
   }
-  for (int c0 = 0; c0 < DQK; c0 += kSlab) {
+  for (int c0 = 0; c0 < DQK && xq == nullptr; c0 += kSlab) {
     __syncthreads();
     for (int e = tid; e < L * kSlab; e += blockDim.x) {
       const int r = e / kSlab, c = e - r * kSlab;
@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(256) output_simt_kernel(
 #pragma unroll
   for (int i = 0; i < RR; ++i) {
     const int r = ry + 8 * i;
+    if (xq != nullptr) num_x[i] = xq[(tbase + r) * DV + a0 + ax];  // C q_r, from the state product
     const float mr = sMr[r];
     const float beta = expf(m_in - mr);
     const float den = sRow[r] + beta * sDenX[r];
@@ -164,7 +165,7 @@ template <typename T, typename TO, int L>
 static cudaError_t launch_output_simt_t(const void *q, const void *k, const void *v, const float *gb,
                                         const float *gx, const float *gu, const float *cm,
                                         const float *Cs, const float *ns, int P, int S, int DQK,
-                                        int DV, void *h, float *den_out, cudaStream_t stream) {
+                                        int DV, void *h, float *den_out, const float *xq, cudaStream_t stream) {
   constexpr int KR = L > kCols ? L : kCols;
   const size_t smem = sizeof(float) * ((size_t)L * (L + 1) + (size_t)(L + KR) * (kSlab + 1) +
                                        (size_t)L * kCols + 3 * (size_t)L);
@@ -173,7 +174,7 @@ static cudaError_t launch_output_simt_t(const void *q, const void *k, const void
   if (err != cudaSuccess) return err;
   dim3 grid(S / L, DV / kCols, P);
   kern<<<grid, 256, smem, stream>>>((const T *)q, (const T *)k, (const T *)v, gb, gx, gu, cm, Cs,
-                                    ns, S, DQK, DV, (TO *)h, den_out);
+                                    ns, S, DQK, DV, (TO *)h, den_out, xq);
   return cudaGetLastError();
 }
 
@@ -181,12 +182,12 @@ template <typename T, typename TO>
 static cudaError_t dispatch_L(int L, const void *q, const void *k, const void *v, const float *gb,
                               const float *gx, const float *gu, const float *cm, const float *Cs,
                               const float *ns, int P, int S, int DQK, int DV, void *h,
-                              float *den, cudaStream_t st) {
+                              float *den, const float *xq, cudaStream_t st) {
   switch (L) {
-    case 16: return launch_output_simt_t<T, TO, 16>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den, st);
-    case 32: return launch_output_simt_t<T, TO, 32>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den, st);
-    case 64: return launch_output_simt_t<T, TO, 64>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den, st);
-    case 128: return launch_output_simt_t<T, TO, 128>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den, st);
+    case 16: return launch_output_simt_t<T, TO, 16>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den, xq, st);
+    case 32: return launch_output_simt_t<T, TO, 32>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den, xq, st);
+    case 64: return launch_output_simt_t<T, TO, 64>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den, xq, st);
+    case 128: return launch_output_simt_t<T, TO, 128>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den, xq, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -194,16 +195,16 @@ static cudaError_t dispatch_L(int L, const void *q, const void *k, const void *v
 cudaError_t launch_output_simt(const void *q, const void *k, const void *v, bool bf16, bool out_bf16,
                                const float *gb, const float *gx, const float *gu, const float *cm,
                                const float *Cs, const float *ns, int P, int S, int L, int DQK, int DV,
-                               void *h, cudaStream_t stream, float *den_out) {
+                               void *h, cudaStream_t stream, float *den_out, const float *xq) {
   if (P == 0 || S == 0) return cudaSuccess;
   if (bf16) {
     if (out_bf16)
-      return dispatch_L<__nv_bfloat16, __nv_bfloat16>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den_out, stream);
-    return dispatch_L<__nv_bfloat16, float>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den_out, stream);
+      return dispatch_L<__nv_bfloat16, __nv_bfloat16>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den_out, xq, stream);
+    return dispatch_L<__nv_bfloat16, float>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den_out, xq, stream);
   }
   if (out_bf16)
-    return dispatch_L<float, __nv_bfloat16>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den_out, stream);
-  return dispatch_L<float, float>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den_out, stream);
+    return dispatch_L<float, __nv_bfloat16>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den_out, xq, stream);
+  return dispatch_L<float, float>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den_out, xq, stream);
 }
 
 }  // namespace mlstm

@@ -61,7 +61,8 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
     const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapY, const float *__restrict__ wx,
     const float *__restrict__ wn, const float *__restrict__ alpha, const float *__restrict__ sc, int S, int L,
     int DV, int reverse, const float *__restrict__ C0, const float *__restrict__ n0, float *__restrict__ states,
-    float *__restrict__ nstates, float *__restrict__ C_fin, float *__restrict__ n_fin, int *__restrict__ err) {
+    float *__restrict__ nstates, float *__restrict__ C_fin, float *__restrict__ n_fin, int *__restrict__ err,
+    float *__restrict__ states_t) {
   constexpr int DQK = 64 * NQ;
   constexpr int NN = DQK > 256 ? 2 : 1;  // MMAs per K step (N <= 256 each)
   constexpr int NB = DQK / NN;           // N of each
@@ -236,6 +237,12 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
             for (int e = 0; e < 32; e += 4)
               *reinterpret_cast<float4 *>(d2 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
           }
+        }
+        if (states_t) {
+          // the transposed state [DQK][DV]: for each column the warp's 32 rows are contiguous
+          float *dt = states_t + ((size_t)p * (NC + 1) + b_in) * (size_t)DQK * DV + (size_t)c0 * DV + a0 + row;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) dt[(size_t)e * DV] = v[e];
         }
         if (i < NC) {
           // T for the next chunk: alpha_k times the state, in units of s_k
@@ -445,13 +452,13 @@ template <int NQ>
 cudaError_t states_tc_t(const CUtensorMap &mx, const CUtensorMap &my, const float *wx, const float *wn,
                         const float *alpha, const float *sc, int P, int S, int L, int DV, bool reverse,
                         const float *C0, const float *n0, float *states, float *nstates, float *C_fin, float *n_fin,
-                        int *err, cudaStream_t stream) {
+                        int *err, float *states_t, cudaStream_t stream) {
   auto kern = states_tc_kernel<NQ>;
   const size_t smem = sizeof(StatesSmem<NQ>) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<dim3(DV / kTileM, P), kThreadsT, smem, stream>>>(mx, my, wx, wn, alpha, sc, S, L, DV, reverse ? 1 : 0, C0,
-                                                          n0, states, nstates, C_fin, n_fin, err);
+                                                          n0, states, nstates, C_fin, n_fin, err, states_t);
   return cudaGetLastError();
 }
 
@@ -474,17 +481,17 @@ cudaError_t launch_state_weights(int mode, const float *gb, const float *gx, con
 cudaError_t launch_states_tc(const void *X, const void *Y, const float *wx, const float *wn, const float *alpha,
                              const float *sc, int P, int S, int L, int DQK, int DV, bool reverse, const float *C0,
                              const float *n0, float *states, float *nstates, float *C_fin, float *n_fin, int *err,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, float *states_t) {
   if (P == 0 || S == 0) return cudaSuccess;  // no chunk: the caller's initial state is the only boundary
   CUtensorMap mx, my;
   const uint64_t rows = (uint64_t)P * S;
   if (!make_tmap_2d_b16(&mx, X, true, rows, DV, DV, 64, kSub)) return cudaErrorInvalidValue;
   if (!make_tmap_2d_b16(&my, Y, true, rows, DQK, DQK, 64, kSub)) return cudaErrorInvalidValue;
   switch (DQK) {
-    case 64: return states_tc_t<1>(mx, my, wx, wn, alpha, sc, P, S, L, DV, reverse, C0, n0, states, nstates, C_fin, n_fin, err, stream);
-    case 128: return states_tc_t<2>(mx, my, wx, wn, alpha, sc, P, S, L, DV, reverse, C0, n0, states, nstates, C_fin, n_fin, err, stream);
-    case 256: return states_tc_t<4>(mx, my, wx, wn, alpha, sc, P, S, L, DV, reverse, C0, n0, states, nstates, C_fin, n_fin, err, stream);
-    case 512: return states_tc_t<8>(mx, my, wx, wn, alpha, sc, P, S, L, DV, reverse, C0, n0, states, nstates, C_fin, n_fin, err, stream);
+    case 64: return states_tc_t<1>(mx, my, wx, wn, alpha, sc, P, S, L, DV, reverse, C0, n0, states, nstates, C_fin, n_fin, err, states_t, stream);
+    case 128: return states_tc_t<2>(mx, my, wx, wn, alpha, sc, P, S, L, DV, reverse, C0, n0, states, nstates, C_fin, n_fin, err, states_t, stream);
+    case 256: return states_tc_t<4>(mx, my, wx, wn, alpha, sc, P, S, L, DV, reverse, C0, n0, states, nstates, C_fin, n_fin, err, states_t, stream);
+    case 512: return states_tc_t<8>(mx, my, wx, wn, alpha, sc, P, S, L, DV, reverse, C0, n0, states, nstates, C_fin, n_fin, err, states_t, stream);
   }
   return cudaErrorInvalidValue;
 }
