@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(256) bwd_dqdk_kernel(
     const float *__restrict__ Cs, const float *__restrict__ ns, const float *__restrict__ Gs,
     const float *__restrict__ Ns, int S, int DQK, int DV, T *__restrict__ dq, T *__restrict__ dk,
     float *__restrict__ part_q, float *__restrict__ part_k, const float *__restrict__ yq,
-    const float *__restrict__ yk) {
+    const float *__restrict__ yk, const float *__restrict__ m1) {
   constexpr int RB = L / 16;  // L x L tile entries per thread (16 x 16 thread grid)
   constexpr int RR = L / 8;   // output rows per thread (8 x 32 thread grid)
   constexpr int KR = L > kSlab ? L : kSlab;
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(256) bwd_dqdk_kernel(
   for (int i = 0; i < RB; ++i)
 #pragma unroll
     for (int j = 0; j < RB; ++j) s[i][j] = 0.f;
-  for (int a0 = 0; a0 < DV; a0 += kSlab) {
+  for (int a0 = 0; a0 < DV && m1 == nullptr; a0 += kSlab) {
     __syncthreads();
     for (int e = tid; e < L * kSlab; e += blockDim.x) {
       const int r = e / kSlab, a = e - r * kSlab;
@@ -220,13 +220,19 @@ __global__ void __launch_bounds__(256) bwd_dqdk_kernel(
         for (int j = 0; j < RB; ++j) s[i][j] = fmaf(ga[i], vb[j], s[i][j]);
     }
   }
+  if (m1 != nullptr) {  // the chunk's M1, formed once
+    __syncthreads();
+    const float *mc = m1 + ((size_t)p * NC + kc) * L * L;
+    for (int e = tid; e < L * L; e += blockDim.x) sM[(e / L) * (L + 1) + e % L] = mc[e];
+  } else {
 #pragma unroll
-  for (int i = 0; i < RB; ++i) {
-    const int u = ty + 16 * i;
+    for (int i = 0; i < RB; ++i) {
+      const int u = ty + 16 * i;
 #pragma unroll
-    for (int j = 0; j < RB; ++j) {
-      const int t = tx + 16 * j;
-      sM[u * (L + 1) + t] = t <= u ? (s[i][j] + sC[u]) * expf(sGx[t] - sMx[u]) : 0.f;
+      for (int j = 0; j < RB; ++j) {
+        const int t = tx + 16 * j;
+        sM[u * (L + 1) + t] = t <= u ? (s[i][j] + sC[u]) * expf(sGx[t] - sMx[u]) : 0.f;
+      }
     }
   }
 
@@ -311,7 +317,7 @@ __global__ void __launch_bounds__(256) bwd_dv_kernel(
     const T *__restrict__ qin, const T *__restrict__ kin, const T *__restrict__ dh, const float *__restrict__ invD,
     const float *__restrict__ gb, const float *__restrict__ gx, const float *__restrict__ gu,
     const float *__restrict__ cm, const float *__restrict__ Gs, int S, int DQK, int DV, T *__restrict__ dv,
-    const float *__restrict__ yv) {
+    const float *__restrict__ yv, const float *__restrict__ pm) {
   constexpr int RB = L / 16;
   constexpr int RR = L / 8;
   constexpr int KR = L > kSlab ? L : kSlab;
@@ -342,7 +348,7 @@ __global__ void __launch_bounds__(256) bwd_dv_kernel(
   for (int i = 0; i < RB; ++i)
 #pragma unroll
     for (int j = 0; j < RB; ++j) s[i][j] = 0.f;
-  for (int c0 = 0; c0 < DQK; c0 += kSlab) {
+  for (int c0 = 0; c0 < DQK && pm == nullptr; c0 += kSlab) {
     __syncthreads();
     for (int e = tid; e < L * kSlab; e += blockDim.x) {
       const int r = e / kSlab, c = e - r * kSlab;
@@ -363,13 +369,19 @@ __global__ void __launch_bounds__(256) bwd_dv_kernel(
         for (int j = 0; j < RB; ++j) s[i][j] = fmaf(qa[i], kb[j], s[i][j]);
     }
   }
+  if (pm != nullptr) {  // the chunk's P, formed once
+    __syncthreads();
+    const float *pc = pm + ((size_t)p * NC + kc) * L * L;
+    for (int e = tid; e < L * L; e += blockDim.x) sM[(e / L) * (L + 1) + e % L] = pc[e];
+  } else {
 #pragma unroll
-  for (int i = 0; i < RB; ++i) {
-    const int u = ty + 16 * i;
+    for (int i = 0; i < RB; ++i) {
+      const int u = ty + 16 * i;
 #pragma unroll
-    for (int j = 0; j < RB; ++j) {
-      const int t = tx + 16 * j;
-      sM[u * (L + 1) + t] = t <= u ? s[i][j] * scale * expf(sGx[t] - sMx[u]) : 0.f;
+      for (int j = 0; j < RB; ++j) {
+        const int t = tx + 16 * j;
+        sM[u * (L + 1) + t] = t <= u ? s[i][j] * scale * expf(sGx[t] - sMx[u]) : 0.f;
+      }
     }
   }
   const int ry = tid >> 5, ax = tid & 31;
@@ -483,16 +495,140 @@ __global__ void __launch_bounds__(256) bwd_gates_kernel(
   }
 }
 
+// ---------------------------------------------------------------- a chunk's L x L matrices
+// CTA (chunk, head), 256 threads, once per chunk (the column-tile kernels then read them):
+//   mode 0: P_ut = E_ut (q_u . khat_t) -- the forward's decay-weighted scores -- and n^(k) . q_u;
+//   mode 1: M1_ut = E_ut (g_u . v_t + c_u) with g_u = dh_u / D_u;
+// t <= u, zero above the diagonal; out [P, NC, L, L] fp32 (row u, column t).
+template <typename T, int L>
+__global__ void __launch_bounds__(256) bwd_mat_kernel(
+    int mode, const T *__restrict__ xin, const T *__restrict__ yin, int K, const float *__restrict__ invD,
+    const float *__restrict__ cc, const float *__restrict__ gx, const float *__restrict__ gu,
+    const float *__restrict__ cm, const float *__restrict__ ns, int S, int DQK, float *__restrict__ out,
+    float *__restrict__ nq) {
+  constexpr int RB = L / 16;
+  __shared__ float sX[L][kSlab + 1], sY[L][kSlab + 1];
+  __shared__ float sMx[L], sGx[L], sW[L], sC[L];
+  const int kc = blockIdx.x, p = blockIdx.y, tid = threadIdx.x;
+  const int NC = S / L;
+  const size_t tbase = (size_t)p * S + (size_t)kc * L;
+  const float m_in = cm[(size_t)p * (NC + 1) + kc];
+  if (tid < L) {
+    sMx[tid] = fmaxf(m_in, gu[tbase + tid]);
+    sGx[tid] = gx[tbase + tid];
+    sW[tid] = mode == 1 ? invD[tbase + tid] : 1.f;
+    sC[tid] = mode == 1 ? cc[tbase + tid] : 0.f;
+  }
+  const float *nv = ns + ((size_t)p * (NC + 1) + kc) * (size_t)DQK;
+  const int ty = tid >> 4, tx = tid & 15, lane = tid & 31, warp = tid >> 5;
+  float s[RB][RB];
+#pragma unroll
+  for (int i = 0; i < RB; ++i)
+#pragma unroll
+    for (int j = 0; j < RB; ++j) s[i][j] = 0.f;
+  float nqa[L / 8];
+#pragma unroll
+  for (int i = 0; i < L / 8; ++i) nqa[i] = 0.f;
+  for (int c0 = 0; c0 < K; c0 += kSlab) {
+    __syncthreads();
+    for (int e = tid; e < L * kSlab; e += blockDim.x) {
+      const int r = e / kSlab, c = e - r * kSlab;
+      sX[r][c] = to_f32(xin[(tbase + r) * K + c0 + c]) * sW[r];
+      sY[r][c] = to_f32(yin[(tbase + r) * K + c0 + c]);
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int c = 0; c < kSlab; ++c) {
+      float xa[RB], yb[RB];
+#pragma unroll
+      for (int i = 0; i < RB; ++i) xa[i] = sX[ty + 16 * i][c];
+#pragma unroll
+      for (int j = 0; j < RB; ++j) yb[j] = sY[tx + 16 * j][c];
+#pragma unroll
+      for (int i = 0; i < RB; ++i)
+#pragma unroll
+        for (int j = 0; j < RB; ++j) s[i][j] = fmaf(xa[i], yb[j], s[i][j]);
+    }
+    if (mode == 0) {  // n^(k) . q_u for this slab: warp w takes rows w, w + 8, ...
+#pragma unroll
+      for (int i = 0; i < L / 8; ++i) nqa[i] = fmaf(sX[warp + 8 * i][lane], nv[c0 + lane], nqa[i]);
+    }
+  }
+  const float scale = mode == 0 ? rsqrtf((float)DQK) : 1.f;
+  float *o = out + ((size_t)p * NC + kc) * L * L;
+#pragma unroll
+  for (int i = 0; i < RB; ++i) {
+    const int u = ty + 16 * i;
+#pragma unroll
+    for (int j = 0; j < RB; ++j) {
+      const int t = tx + 16 * j;
+      o[u * L + t] = t <= u ? (s[i][j] * scale + sC[u]) * expf(sGx[t] - sMx[u]) : 0.f;
+    }
+  }
+  if (mode == 0) {
+#pragma unroll
+    for (int i = 0; i < L / 8; ++i) {
+      const float x = warp_sum(nqa[i]);
+      if (lane == 0) nq[tbase + warp + 8 * i] = x;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- bf16 (or fp32) to fp32
+// Eight elements per thread and step: a 16-byte load of bf16 (or two of fp32), two 16-byte stores
+// (n a multiple of 8, both pointers 16-byte aligned).
 __global__ void to_f32_kernel(const void *__restrict__ src, int bf16, float *__restrict__ dst, size_t n) {
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
-    dst[i] = bf16 ? __bfloat162float(static_cast<const __nv_bfloat16 *>(src)[i]) : static_cast<const float *>(src)[i];
+  const size_t n8 = n / 8;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    float4 a, b;
+    if (bf16) {
+      const uint4 u = reinterpret_cast<const uint4 *>(src)[i];
+      a = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                      __uint_as_float(u.y & 0xffff0000u));
+      b = make_float4(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xffff0000u), __uint_as_float(u.w << 16),
+                      __uint_as_float(u.w & 0xffff0000u));
+    } else {
+      a = reinterpret_cast<const float4 *>(src)[2 * i];
+      b = reinterpret_cast<const float4 *>(src)[2 * i + 1];
+    }
+    reinterpret_cast<float4 *>(dst)[2 * i] = a;
+    reinterpret_cast<float4 *>(dst)[2 * i + 1] = b;
+  }
 }
 
 // ---------------------------------------------------------------- launchers
+cudaError_t launch_bwd_mat(int mode, const void *x, const void *y, bool bf16, int K, const float *invD,
+                           const float *cc, const float *gx, const float *gu, const float *cm, const float *ns, int P,
+                           int S, int L, int DQK, float *out, float *nq, cudaStream_t stream) {
+  if (P == 0 || S == 0) return cudaSuccess;
+  dim3 grid(S / L, P);
+#define MLSTM_BWD_MAT(T_, L_)                                                                                  \
+  bwd_mat_kernel<T_, L_><<<grid, 256, 0, stream>>>(mode, (const T_ *)x, (const T_ *)y, K, invD, cc, gx, gu, cm, \
+                                                    ns, S, DQK, out, nq);                                       \
+  return cudaGetLastError()
+  if (bf16) {
+    switch (L) {
+      case 16: MLSTM_BWD_MAT(__nv_bfloat16, 16);
+      case 32: MLSTM_BWD_MAT(__nv_bfloat16, 32);
+      case 64: MLSTM_BWD_MAT(__nv_bfloat16, 64);
+      case 128: MLSTM_BWD_MAT(__nv_bfloat16, 128);
+    }
+  } else {
+    switch (L) {
+      case 16: MLSTM_BWD_MAT(float, 16);
+      case 32: MLSTM_BWD_MAT(float, 32);
+      case 64: MLSTM_BWD_MAT(float, 64);
+      case 128: MLSTM_BWD_MAT(float, 128);
+    }
+  }
+#undef MLSTM_BWD_MAT
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_to_f32(const void *src, bool bf16, float *dst, size_t n, cudaStream_t stream) {
   if (n == 0) return cudaSuccess;
-  const size_t blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+  if (n % 8 != 0) return cudaErrorInvalidValue;
+  const size_t n8 = n / 8, blocks = (n8 + 255) / 256 < 4096 ? (n8 + 255) / 256 : 4096;
   to_f32_kernel<<<(unsigned)blocks, 256, 0, stream>>>(src, bf16 ? 1 : 0, dst, n);
   return cudaGetLastError();
 }
@@ -537,27 +673,28 @@ template <typename T, int L>
 cudaError_t dqdk_t(const void *q, const void *k, const void *v, const void *dh, const float *invD, const float *cc,
                    const float *gb, const float *gx, const float *gu, const float *cm, const float *Cs,
                    const float *ns, const float *Gs, const float *Ns, int P, int S, int DQK, int DV, void *dq,
-                   void *dk, float *part_q, float *part_k, const float *yq, const float *yk, cudaStream_t stream) {
+                   void *dk, float *part_q, float *part_k, const float *yq, const float *yk, const float *m1,
+                   cudaStream_t stream) {
   auto kern = bwd_dqdk_kernel<T, L>;
   const size_t smem = chunk_smem<L>(6);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<dim3(S / L, DQK / kCols, P), 256, smem, stream>>>((const T *)q, (const T *)k, (const T *)v, (const T *)dh,
                                                            invD, cc, gb, gx, gu, cm, Cs, ns, Gs, Ns, S, DQK, DV,
-                                                           (T *)dq, (T *)dk, part_q, part_k, yq, yk);
+                                                           (T *)dq, (T *)dk, part_q, part_k, yq, yk, m1);
   return cudaGetLastError();
 }
 
 template <typename T, int L>
 cudaError_t dv_t(const void *q, const void *k, const void *dh, const float *invD, const float *gb, const float *gx,
                  const float *gu, const float *cm, const float *Gs, int P, int S, int DQK, int DV, void *dv,
-                 const float *yv, cudaStream_t stream) {
+                 const float *yv, const float *pm, cudaStream_t stream) {
   auto kern = bwd_dv_kernel<T, L>;
   const size_t smem = chunk_smem<L>(4);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<dim3(S / L, DV / kCols, P), 256, smem, stream>>>((const T *)q, (const T *)k, (const T *)dh, invD, gb, gx,
-                                                          gu, cm, Gs, S, DQK, DV, (T *)dv, yv);
+                                                          gu, cm, Gs, S, DQK, DV, (T *)dv, yv, pm);
   return cudaGetLastError();
 }
 }  // namespace
@@ -566,11 +703,12 @@ cudaError_t launch_bwd_dqdk(const void *q, const void *k, const void *v, const v
                             const float *invD, const float *cc, const float *gb, const float *gx, const float *gu,
                             const float *cm, const float *Cs, const float *ns, const float *Gs, const float *Ns,
                             int P, int S, int L, int DQK, int DV, void *dq, void *dk, float *part_q,
-                            float *part_k, cudaStream_t stream, const float *yq, const float *yk) {
+                            float *part_k, cudaStream_t stream, const float *yq, const float *yk,
+                            const float *m1) {
   if (P == 0 || S == 0) return cudaSuccess;
 #define MLSTM_BWD_DQDK(T_, L_)                                                                                   \
   return dqdk_t<T_, L_>(q, k, v, dh, invD, cc, gb, gx, gu, cm, Cs, ns, Gs, Ns, P, S, DQK, DV, dq, dk, part_q, \
-                        part_k, yq, yk, stream)
+                        part_k, yq, yk, m1, stream)
   if (bf16) {
     switch (L) {
       case 16: MLSTM_BWD_DQDK(__nv_bfloat16, 16);
@@ -592,9 +730,10 @@ cudaError_t launch_bwd_dqdk(const void *q, const void *k, const void *v, const v
 
 cudaError_t launch_bwd_dv(const void *q, const void *k, const void *dh, bool bf16, const float *invD,
                           const float *gb, const float *gx, const float *gu, const float *cm, const float *Gs,
-                          int P, int S, int L, int DQK, int DV, void *dv, cudaStream_t stream, const float *yv) {
+                          int P, int S, int L, int DQK, int DV, void *dv, cudaStream_t stream, const float *yv,
+                          const float *pm) {
   if (P == 0 || S == 0) return cudaSuccess;
-#define MLSTM_BWD_DV(T_, L_) return dv_t<T_, L_>(q, k, dh, invD, gb, gx, gu, cm, Gs, P, S, DQK, DV, dv, yv, stream)
+#define MLSTM_BWD_DV(T_, L_) return dv_t<T_, L_>(q, k, dh, invD, gb, gx, gu, cm, Gs, P, S, DQK, DV, dv, yv, pm, stream)
   if (bf16) {
     switch (L) {
       case 16: MLSTM_BWD_DV(__nv_bfloat16, 16);

@@ -476,7 +476,7 @@ mlstm_status mlstm_wait_selftest(void *workspace, size_t ws_bytes, int B, int NH
 namespace {
 struct BwdLayout {
   size_t gb, gx, gu, cm, Cs, ns, Gs, Ns, h32, den, invD, cc, pq, pk, wx, wn, al, sc;
-  size_t Cst, Gst, q32, k32, v32, dh32, xq, yq, yk, yv, total;
+  size_t Cst, Gst, q32, k32, v32, dh32, xq, yq, yk, yv, pm, m1, nq, total;
   bool tc_states, tc_prod;  // state walks / state products on tensor cores
 };
 
@@ -520,6 +520,9 @@ BwdLayout bwd_layout(int B, int NH, int S, int DQK, int DV, int chunk, bool bf16
   take(L.yq, TQ);
   take(L.yk, TQ);
   take(L.yv, TV);
+  take(L.pm, P * NC * chunk * chunk);  // each chunk's L x L matrices, formed once
+  take(L.m1, P * NC * chunk * chunk);
+  take(L.nq, PS);
   L.total = off;
   return L;
 }
@@ -604,14 +607,23 @@ mlstm_status mlstm_bwd_chunkwise(const void *q, const void *k, const void *v, co
     ++kernels;
   }
   if (e == cudaSuccess && S > 0) {
-    e = launch_output_simt(q, k, v, bf16, false, F(Lw.gb), F(Lw.gx), F(Lw.gu), F(Lw.cm), F(Lw.Cs), F(Lw.ns), P, S,
-                           chunk, DQK, DV, F(Lw.h32), s, F(Lw.den), tc_prod ? F(Lw.xq) : nullptr);
-    ++kernels;
+    // each chunk's decay-weighted scores P (also the dv kernel's matrix) and n^(k) . q_t, once
+    e = launch_bwd_mat(0, q, k, bf16, DQK, nullptr, nullptr, F(Lw.gx), F(Lw.gu), F(Lw.cm), F(Lw.ns), P, S, chunk, DQK,
+                       F(Lw.pm), F(Lw.nq), s);
+    if (e == cudaSuccess)
+      e = launch_output_simt(q, k, v, bf16, false, F(Lw.gb), F(Lw.gx), F(Lw.gu), F(Lw.cm), F(Lw.Cs), F(Lw.ns), P, S,
+                             chunk, DQK, DV, F(Lw.h32), s, F(Lw.den), tc_prod ? F(Lw.xq) : nullptr, F(Lw.pm),
+                             F(Lw.nq));
+    kernels += 2;
   }
   if (e == cudaSuccess && S > 0) {
     e = launch_bwd_prep(dh, bf16, F(Lw.h32), F(Lw.den), F(Lw.gb), F(Lw.gu), F(Lw.cm), P, S, chunk, DV, F(Lw.invD),
                         F(Lw.cc), s);
-    ++kernels;
+    // each chunk's M1 = E (g v^T + c), once
+    if (e == cudaSuccess)
+      e = launch_bwd_mat(1, dh, v, bf16, DV, F(Lw.invD), F(Lw.cc), F(Lw.gx), F(Lw.gu), F(Lw.cm), F(Lw.ns), P, S,
+                         chunk, DQK, F(Lw.m1), nullptr, s);
+    kernels += 2;
   }
   if (e == cudaSuccess && tc_states) {
     e = launch_state_weights(1, F(Lw.gb), F(Lw.gx), F(Lw.gu), F(Lw.cm), F(Lw.invD), F(Lw.cc), P, S, chunk, DQK,
@@ -638,12 +650,12 @@ mlstm_status mlstm_bwd_chunkwise(const void *q, const void *k, const void *v, co
   if (e == cudaSuccess && S > 0) {
     e = launch_bwd_dqdk(q, k, v, dh, bf16, F(Lw.invD), F(Lw.cc), F(Lw.gb), F(Lw.gx), F(Lw.gu), F(Lw.cm), F(Lw.Cs),
                         F(Lw.ns), F(Lw.Gs), F(Lw.Ns), P, S, chunk, DQK, DV, dq, dk, F(Lw.pq), F(Lw.pk), s,
-                        tc_prod ? F(Lw.yq) : nullptr, tc_prod ? F(Lw.yk) : nullptr);
+                        tc_prod ? F(Lw.yq) : nullptr, tc_prod ? F(Lw.yk) : nullptr, F(Lw.m1));
     ++kernels;
   }
   if (e == cudaSuccess && S > 0) {
     e = launch_bwd_dv(q, k, dh, bf16, F(Lw.invD), F(Lw.gb), F(Lw.gx), F(Lw.gu), F(Lw.cm), F(Lw.Gs), P, S, chunk,
-                      DQK, DV, dv, s, tc_prod ? F(Lw.yv) : nullptr);
+                      DQK, DV, dv, s, tc_prod ? F(Lw.yv) : nullptr, F(Lw.pm));
     ++kernels;
   }
   if (e == cudaSuccess) {

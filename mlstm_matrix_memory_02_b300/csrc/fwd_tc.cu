@@ -597,7 +597,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(
     float sig_last = 0.f;
     bool ok = true;
     for (int k = 0; k < NC; ++k) {
-      const int s = k & 1;
       if (!mbar_wait(&sm.g_full[k & 3], (k >> 2) & 1, err, 40, abort_ptr)) { ok = false; break; }
       // U_{k-1} and X_{k-1} (which reads C16) are done
       if (k >= 1 && !mbar_wait(&sm.bar_X, (k - 1) & 1, err, 32, abort_ptr)) { ok = false; break; }

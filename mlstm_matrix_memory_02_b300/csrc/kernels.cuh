@@ -28,7 +28,8 @@ cudaError_t launch_states_simt(const void *k, const void *v, bool bf16, const fl
 cudaError_t launch_output_simt(const void *q, const void *k, const void *v, bool bf16, bool out_bf16,
                                const float *gb, const float *gx, const float *gu, const float *cm,
                                const float *Cs, const float *ns, int P, int S, int L, int DQK, int DV,
-                               void *h, cudaStream_t stream, float *den_out = nullptr, const float *xq = nullptr);
+                               void *h, cudaStream_t stream, float *den_out = nullptr, const float *xq = nullptr,
+                               const float *pm = nullptr, const float *nq = nullptr);
 
 // Backward of the chunkwise forward on CUDA cores (bwd_simt.cu), after the gate kernel, the
 // boundary states (Cs, ns) and the output kernel (h in fp32 and den) have run for chunk L:
@@ -50,11 +51,18 @@ cudaError_t launch_bwd_dqdk(const void *q, const void *k, const void *v, const v
                             const float *cm, const float *Cs, const float *ns, const float *Gs, const float *Ns,
                             int P, int S, int L, int DQK, int DV, void *dq, void *dk, float *part_q,
                             float *part_k, cudaStream_t stream, const float *yq = nullptr,
-                            const float *yk = nullptr);
+                            const float *yk = nullptr, const float *m1 = nullptr);
 cudaError_t launch_bwd_dv(const void *q, const void *k, const void *dh, bool bf16, const float *invD,
                           const float *gb, const float *gx, const float *gu, const float *cm, const float *Gs,
                           int P, int S, int L, int DQK, int DV, void *dv, cudaStream_t stream,
-                          const float *yv = nullptr);
+                          const float *yv = nullptr, const float *pm = nullptr);
+// A chunk's L x L matrices, formed once per (chunk, head) for the kernels above ([P, NC, L, L]):
+// mode 0, x = q, y = k, K = DQK: P_ut = E_ut (q_u . khat_t), and nq = n^(k) . q_u per token;
+// mode 1, x = dh, y = v, K = DV: M1_ut = E_ut (dh_u . v_t / D_u + c_u).  (pm, m1 and nq also
+// feed launch_output_simt, launch_bwd_dqdk and launch_bwd_dv.)
+cudaError_t launch_bwd_mat(int mode, const void *x, const void *y, bool bf16, int K, const float *invD,
+                           const float *cc, const float *gx, const float *gu, const float *cm, const float *ns, int P,
+                           int S, int L, int DQK, float *out, float *nq, cudaStream_t stream);
 // Chunk-boundary states on tensor cores (states_tc.cu): bf16 X [P, S, DV] and Y [P, S, DQK],
 // L a multiple of 64 up to 128, DQK in {64, 128, 256, 512}, DV a multiple of 128, S > 0.  The
 // weights come from launch_state_weights (mode 0: the forward state with X = v, Y = k; mode 1:
@@ -79,7 +87,7 @@ cudaError_t launch_states_tc(const void *X, const void *Y, const float *wx, cons
 bool state_prod_supported(int L, int DQK, int DV);
 cudaError_t launch_state_prod(const float *A, int MA, int K, int bshift, const float *Y, const float *tok_scale,
                               float scale, int P, int S, int L, float *out, int *err, cudaStream_t stream);
-// bf16 or fp32 elements to fp32.
+// bf16 or fp32 elements to fp32 (n a multiple of 8, pointers 16-byte aligned).
 cudaError_t launch_to_f32(const void *src, bool bf16, float *dst, size_t n, cudaStream_t stream);
 cudaError_t launch_bwd_gates(const float *fg, bool exp_fg, const float *part_q, const float *part_k, int P, int S,
                              int ntiles, const float *Gs0, const float *Ns0, size_t gs_stride, size_t ns_stride,

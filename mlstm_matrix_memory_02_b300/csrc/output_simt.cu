@@ -31,7 +31,8 @@ __global__ void __launch_bounds__(256) output_simt_kernel(
     const T *__restrict__ qin, const T *__restrict__ kin, const T *__restrict__ vin,
     const float *__restrict__ gb, const float *__restrict__ gx, const float *__restrict__ gu,
     const float *__restrict__ cm, const float *__restrict__ Cs, const float *__restrict__ ns,
-    int S, int DQK, int DV, TO *__restrict__ h, float *__restrict__ den_out, const float *__restrict__ xq) {
+    int S, int DQK, int DV, TO *__restrict__ h, float *__restrict__ den_out, const float *__restrict__ xq,
+    const float *__restrict__ pm, const float *__restrict__ nq) {
   constexpr int RB = L / 16;  // S-tile rows/cols per thread (16 x 16 thread grid)
   extern __shared__ float smem[];
   float *sP = smem;                        // [L][L+1]   S, then P = S o D
@@ -54,7 +55,7 @@ __global__ void __launch_bounds__(256) output_simt_kernel(
 
   if (tid < L) {
     sMr[tid] = fmaxf(m_in, gu[tbase + tid]);
-    sDenX[tid] = 0.f;
+    sDenX[tid] = pm != nullptr ? nq[tbase + tid] : 0.f;
   }
 
   // ---- S = Q K^T over d_qk in slabs; thread (ty, tx) owns rows ty + 16 i, cols tx + 16 j
@@ -64,7 +65,7 @@ __global__ void __launch_bounds__(256) output_simt_kernel(
   for (int i = 0; i < RB; ++i)
 #pragma unroll
     for (int j = 0; j < RB; ++j) s[i][j] = 0.f;
-  for (int c0 = 0; c0 < DQK; c0 += kSlab) {
+  for (int c0 = 0; c0 < DQK && pm == nullptr; c0 += kSlab) {
     __syncthreads();
     for (int e = tid; e < L * kSlab; e += blockDim.x) {
       const int r = e / kSlab, c = e - r * kSlab;
@@ -94,16 +95,22 @@ __global__ void __launch_bounds__(256) output_simt_kernel(
       }
     }
   }
-  // ---- P = S o D (causal), fp32; row sums give the intra-chunk denominator
+  // ---- P = S o D (causal), fp32 (or the chunk's P formed once elsewhere); row sums give the
+  // intra-chunk denominator
+  if (pm != nullptr) {
+    const float *pc = pm + ((size_t)p * NC + kc) * L * L;
+    for (int e = tid; e < L * L; e += blockDim.x) sP[(e / L) * (L + 1) + e % L] = pc[e];
+  } else {
 #pragma unroll
-  for (int i = 0; i < RB; ++i) {
-    const int r = ty + 16 * i;
+    for (int i = 0; i < RB; ++i) {
+      const int r = ty + 16 * i;
 #pragma unroll
-    for (int j = 0; j < RB; ++j) {
-      const int jj = tx + 16 * j;
-      float pv = 0.f;
-      if (jj <= r) pv = s[i][j] * scale * expf(gx[tbase + jj] - sMr[r]);
-      sP[r * (L + 1) + jj] = pv;
+      for (int j = 0; j < RB; ++j) {
+        const int jj = tx + 16 * j;
+        float pv = 0.f;
+        if (jj <= r) pv = s[i][j] * scale * expf(gx[tbase + jj] - sMr[r]);
+        sP[r * (L + 1) + jj] = pv;
+      }
     }
   }
   __syncthreads();
@@ -165,7 +172,8 @@ template <typename T, typename TO, int L>
 static cudaError_t launch_output_simt_t(const void *q, const void *k, const void *v, const float *gb,
                                         const float *gx, const float *gu, const float *cm,
                                         const float *Cs, const float *ns, int P, int S, int DQK,
-                                        int DV, void *h, float *den_out, const float *xq, cudaStream_t stream) {
+                                        int DV, void *h, float *den_out, const float *xq, const float *pm,
+                                        const float *nq, cudaStream_t stream) {
   constexpr int KR = L > kCols ? L : kCols;
   const size_t smem = sizeof(float) * ((size_t)L * (L + 1) + (size_t)(L + KR) * (kSlab + 1) +
                                        (size_t)L * kCols + 3 * (size_t)L);
@@ -174,7 +182,7 @@ static cudaError_t launch_output_simt_t(const void *q, const void *k, const void
   if (err != cudaSuccess) return err;
   dim3 grid(S / L, DV / kCols, P);
   kern<<<grid, 256, smem, stream>>>((const T *)q, (const T *)k, (const T *)v, gb, gx, gu, cm, Cs,
-                                    ns, S, DQK, DV, (TO *)h, den_out, xq);
+                                    ns, S, DQK, DV, (TO *)h, den_out, xq, pm, nq);
   return cudaGetLastError();
 }
 
@@ -182,12 +190,12 @@ template <typename T, typename TO>
 static cudaError_t dispatch_L(int L, const void *q, const void *k, const void *v, const float *gb,
                               const float *gx, const float *gu, const float *cm, const float *Cs,
                               const float *ns, int P, int S, int DQK, int DV, void *h,
-                              float *den, const float *xq, cudaStream_t st) {
+                              float *den, const float *xq, const float *pm, const float *nq, cudaStream_t st) {
   switch (L) {
-    case 16: return launch_output_simt_t<T, TO, 16>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den, xq, st);
-    case 32: return launch_output_simt_t<T, TO, 32>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den, xq, st);
-    case 64: return launch_output_simt_t<T, TO, 64>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den, xq, st);
-    case 128: return launch_output_simt_t<T, TO, 128>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den, xq, st);
+    case 16: return launch_output_simt_t<T, TO, 16>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den, xq, pm, nq, st);
+    case 32: return launch_output_simt_t<T, TO, 32>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den, xq, pm, nq, st);
+    case 64: return launch_output_simt_t<T, TO, 64>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den, xq, pm, nq, st);
+    case 128: return launch_output_simt_t<T, TO, 128>(q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den, xq, pm, nq, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -195,16 +203,17 @@ static cudaError_t dispatch_L(int L, const void *q, const void *k, const void *v
 cudaError_t launch_output_simt(const void *q, const void *k, const void *v, bool bf16, bool out_bf16,
                                const float *gb, const float *gx, const float *gu, const float *cm,
                                const float *Cs, const float *ns, int P, int S, int L, int DQK, int DV,
-                               void *h, cudaStream_t stream, float *den_out, const float *xq) {
+                               void *h, cudaStream_t stream, float *den_out, const float *xq, const float *pm,
+                               const float *nq) {
   if (P == 0 || S == 0) return cudaSuccess;
   if (bf16) {
     if (out_bf16)
-      return dispatch_L<__nv_bfloat16, __nv_bfloat16>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den_out, xq, stream);
-    return dispatch_L<__nv_bfloat16, float>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den_out, xq, stream);
+      return dispatch_L<__nv_bfloat16, __nv_bfloat16>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den_out, xq, pm, nq, stream);
+    return dispatch_L<__nv_bfloat16, float>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den_out, xq, pm, nq, stream);
   }
   if (out_bf16)
-    return dispatch_L<float, __nv_bfloat16>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den_out, xq, stream);
-  return dispatch_L<float, float>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den_out, xq, stream);
+    return dispatch_L<float, __nv_bfloat16>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den_out, xq, pm, nq, stream);
+  return dispatch_L<float, float>(L, q, k, v, gb, gx, gu, cm, Cs, ns, P, S, DQK, DV, h, den_out, xq, pm, nq, stream);
 }
 
 }  // namespace mlstm

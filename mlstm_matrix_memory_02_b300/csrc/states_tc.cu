@@ -44,6 +44,7 @@ template <int NQ>  // DQK / 64
 struct alignas(1024) StatesSmem {
   static constexpr int ST = stages_for<NQ>();
   unsigned char tile[ST][(2 + NQ) * 8192];  // X boxes 0, 1 then NQ Y boxes, 64 x 128 B each
+  float stage_out[4][32][33];  // per epilogue warp: its 32 rows x 32 columns, transposed for the stores
   uint64_t full[ST], conv[ST], empty[ST];
   uint64_t mma_done, epi_ready, fin;
   float wx[ST][64];  // the slab's X weights
@@ -51,6 +52,7 @@ struct alignas(1024) StatesSmem {
   uint32_t tmem_base;
   int abort_flag;
   int conv_fail;  // written by the conversion warps only, read by them after a barrier
+  int epi_fail;   // the epilogue warps' first failed chunk (-1: none), read by them after a barrier
 };
 
 __device__ __forceinline__ bool st_aborted(const int *f) { return *(const volatile int *)f != 0; }
@@ -66,7 +68,10 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
   constexpr int DQK = 64 * NQ;
   constexpr int NN = DQK > 256 ? 2 : 1;  // MMAs per K step (N <= 256 each)
   constexpr int NB = DQK / NN;           // N of each
-  constexpr uint32_t kCols = DQK < 32 ? 32 : DQK;
+  // two state buffers where tensor memory has room (d_qk <= 256): the products of chunk k then
+  // accumulate into one while the epilogue stores the state held in the other
+  constexpr bool PP = 2 * DQK <= 512;
+  constexpr uint32_t kCols = PP ? 2 * DQK : DQK;
   constexpr int ST = stages_for<NQ>();
   extern __shared__ unsigned char st_raw[];
   StatesSmem<NQ> &sm = *reinterpret_cast<StatesSmem<NQ> *>(
@@ -96,6 +101,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
     mbar_init(&sm.fin, 1);
     sm.abort_flag = 0;
     sm.conv_fail = 0;
+    sm.epi_fail = -1;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -152,7 +158,8 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
           for (int ks = 0; ks < 4; ++ks)
 #pragma unroll
             for (int h = 0; h < NN; ++h)
-              mma_f16_ss(tm + h * NB, dx + (uint64_t)(ks * 2048 >> 4),
+              mma_f16_ss(tm + (PP && !final_only ? (uint32_t)(((i + 1) & 1) * DQK) : 0u) + h * NB,
+                         dx + (uint64_t)(ks * 2048 >> 4),
                          dy + (uint64_t)((ks * 2048 + h * (NB / 64) * 8192) >> 4), id,
                          final_only ? ((j | ks) != 0) : 1);
           mma_commit(&sm.empty[s]);
@@ -168,8 +175,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
     // ------------------------------------------------------------------ epilogue
     const int row = 32 * (warp & 3) + lane;  // the tensor-memory lane this thread may access
     const uint32_t trow = tm + ((uint32_t)(32 * (warp & 3)) << 16);
-    float *Crow_states = states ? states + ((size_t)p * (NC + 1)) * DV * DQK + (size_t)(a0 + row) * DQK : nullptr;
-    auto boundary_row = [&](int b) { return Crow_states + (size_t)b * DV * DQK; };
+    float(*wbuf)[33] = sm.stage_out[warp & 3];
     float s_prev = 1.f;
     bool ok = true;
     if (final_only) {
@@ -202,41 +208,64 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
         s_nxt = sc[(size_t)p * NC + kc_of(i + 1)];
       }
       if (i > 0) {
-        // the whole warp takes the same branch before its collective tensor-memory loads
+        // all four warps take the same branch (they meet at named barriers below), each warp as a
+        // whole before its collective tensor-memory loads
         const bool got = __all_sync(0xffffffffu, mbar_wait(&sm.mma_done, (i - 1) & 1, err, 44, abort_ptr));
-        if (!got) {
+        // (the chunk index, not a flag: a warp that fails at chunk i + 1 before a slower warp has
+        // read the word for chunk i must not stop that warp one chunk early)
+        if (!got) atomicCAS(&sm.epi_fail, -1, i);
+        named_barrier_sync(2, 128);
+        const int failed = *(volatile int *)&sm.epi_fail;
+        if (failed >= 0 && failed <= i) {
           ok = false;
           break;
         }
         tc_fence_after();
       }
-      for (int c0 = 0; c0 < DQK; c0 += 32) {
-        uint32_t r[32];
-        float v[32];
+      // buffers: the state entering chunk i sits in buffer i % 2, the products of chunk i go into
+      // the other (one buffer without room for two)
+      const uint32_t tcur = trow + (PP ? (uint32_t)((i & 1) * DQK) : 0u);
+      const uint32_t tnxt = trow + (PP ? (uint32_t)(((i + 1) & 1) * DQK) : 0u);
+      // the state at boundary b_in, 32 columns at a time (in its own stabiliser frame)
+      auto state_piece = [&](int c0, float (&v)[32]) {
         if (i == 0) {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             v[e] = C0 ? C0[((size_t)p * DV + a0 + row) * DQK + c0 + e] : 0.f;
         } else {
-          tmem_ld32(trow + c0, r);
+          uint32_t r[32];
+          tmem_ld32(tcur + c0, r);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]) * s_prev;
         }
-        // the state at boundary b_in (in its own stabiliser frame)
-        float *dst = nullptr;
-        if (states) dst = boundary_row(b_in) + c0;
-        if (i == NC && C_fin) dst = C_fin + ((size_t)p * DV + a0 + row) * DQK + c0;
-        if (dst) {
+      };
+      // T for the next chunk: alpha_k times the state, in units of s_k
+      auto rescale_piece = [&](int c0, const float (&v)[32]) {
+        uint32_t r[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(v[e] * (a_cur / s_cur));
+        tmem_st16(tnxt + c0, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
+        tmem_st16(tnxt + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
+      };
+      auto store_piece = [&](int c0, const float (&v)[32]) {
+        if (states) {
+          // each thread holds 32 columns of its own row, and rows are 1 KB apart in global memory:
+          // the warp turns its 32 x 32 block around in shared memory (rows padded to 33 words, no
+          // bank conflicts) so that each store instruction writes one row's 128 contiguous bytes
+#pragma unroll
+          for (int e = 0; e < 32; ++e) wbuf[lane][e] = v[e];
+          __syncwarp();
+          float *base = states + ((size_t)(p * (NC + 1) + b_in) * DV + a0 + 32 * (warp & 3)) * DQK + c0 + lane;
+#pragma unroll 8
+          for (int rr = 0; rr < 32; ++rr) base[(size_t)rr * DQK] = wbuf[rr][lane];
+          __syncwarp();
+        }
+        if (i == NC && C_fin) {
+          float *dst = C_fin + ((size_t)p * DV + a0 + row) * DQK + c0;
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<float4 *>(dst + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-          if (i == NC && C_fin && states) {
-            float *d2 = boundary_row(b_in) + c0;
-#pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<float4 *>(d2 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-          }
         }
         if (states_t) {
           // the transposed state [DQK][DV]: for each column the warp's 32 rows are contiguous
@@ -244,18 +273,38 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
 #pragma unroll
           for (int e = 0; e < 32; ++e) dt[(size_t)e * DV] = v[e];
         }
+      };
+      if (PP) {
+        // the next chunk's T first, so that its products start while this state is stored
         if (i < NC) {
-          // T for the next chunk: alpha_k times the state, in units of s_k
-#pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(v[e] * (a_cur / s_cur));
-          tmem_st16(trow + c0, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
-          tmem_st16(trow + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
+          for (int c0 = 0; c0 < DQK; c0 += 32) {
+            float v[32];
+            state_piece(c0, v);
+            rescale_piece(c0, v);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&sm.epi_ready);
+        }
+        for (int c0 = 0; c0 < DQK; c0 += 32) {
+          float v[32];
+          state_piece(c0, v);
+          store_piece(c0, v);
+        }
+      } else {
+        for (int c0 = 0; c0 < DQK; c0 += 32) {
+          float v[32];
+          state_piece(c0, v);
+          store_piece(c0, v);
+          if (i < NC) rescale_piece(c0, v);
         }
       }
       if (i < NC) {
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&sm.epi_ready);
+        if (!PP) {
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&sm.epi_ready);
+        }
         s_prev = s_cur;
       }
     }

@@ -137,18 +137,29 @@ __global__ void __launch_bounds__(kThreads) step_multi_kernel(
   float4 *C4 = reinterpret_cast<float4 *>(C + (size_t)p * DV * DQK);
   const float4 *sq4 = reinterpret_cast<const float4 *>(sq);
   const float4 *sk4 = reinterpret_cast<const float4 *>(sk);
-  for (int a0 = warp * RIF; a0 < DV; a0 += (kThreads / 32) * RIF) {
-    float4 x[RIF][PL];
+  // the rows of the next pass are requested before this pass's arithmetic
+  auto load_rows = [&](int b0, float4 (&y)[RIF][PL]) {
 #pragma unroll
     for (int i = 0; i < RIF; ++i) {
-      const int a = a0 + i;
+      const int a = b0 + i;
 #pragma unroll
       for (int j = 0; j < PL; ++j) {
         const int c4 = lane + 32 * j;
-        if (a < DV && c4 < nv4) x[i][j] = __ldcs(&C4[(size_t)a * nv4 + c4]);
-        else x[i][j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a < DV && c4 < nv4) y[i][j] = __ldcs(&C4[(size_t)a * nv4 + c4]);
+        else y[i][j] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
+  };
+  constexpr int kPass = (kThreads / 32) * RIF;  // rows per pass of the CTA
+  float4 xn[RIF][PL];
+  load_rows(warp * RIF, xn);
+  for (int a0 = warp * RIF; a0 < DV; a0 += kPass) {
+    float4 x[RIF][PL];
+#pragma unroll
+    for (int i = 0; i < RIF; ++i)
+#pragma unroll
+      for (int j = 0; j < PL; ++j) x[i][j] = xn[i][j];
+    if (a0 + kPass < DV) load_rows(a0 + kPass, xn);
     if (BUTTERFLY) {
       // the RIF NT dot products of these rows (slot i kMaxT + t) are reduced together at the end,
       // 32 slots per butterfly
@@ -172,7 +183,8 @@ __global__ void __launch_bounds__(kThreads) step_multi_kernel(
           for (int i = 0; i < RIF; ++i) {
             const int a = a0 + i;
             const float va = a < DV ? sv[t * DV + a] : 0.f;
-            float dot = 0.f;
+            // four partial sums (one per float4 component): dependent chains of PL, not 4 PL
+            float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
 #pragma unroll
             for (int j = 0; j < PL; ++j) {
               float4 y = x[i][j];
@@ -181,12 +193,12 @@ __global__ void __launch_bounds__(kThreads) step_multi_kernel(
               y.z = fmaf(al, y.z, va * kv[j].z);
               y.w = fmaf(al, y.w, va * kv[j].w);
               x[i][j] = y;
-              dot = fmaf(y.x, qv[j].x, dot);
-              dot = fmaf(y.y, qv[j].y, dot);
-              dot = fmaf(y.z, qv[j].z, dot);
-              dot = fmaf(y.w, qv[j].w, dot);
+              d0 = fmaf(y.x, qv[j].x, d0);
+              d1 = fmaf(y.y, qv[j].y, d1);
+              d2 = fmaf(y.z, qv[j].z, d2);
+              d3 = fmaf(y.w, qv[j].w, d3);
             }
-            dots[(i * kMaxT + t) / 32][(i * kMaxT + t) % 32] = dot;
+            dots[(i * kMaxT + t) / 32][(i * kMaxT + t) % 32] = (d0 + d1) + (d2 + d3);
           }
         }
       }
@@ -210,7 +222,7 @@ __global__ void __launch_bounds__(kThreads) step_multi_kernel(
         for (int i = 0; i < RIF; ++i) {
           const int a = a0 + i;
           const float va = a < DV ? sv[t * DV + a] : 0.f;
-          float dot = 0.f;
+          float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
 #pragma unroll
           for (int j = 0; j < PL; ++j) {
             float4 y = x[i][j];
@@ -219,12 +231,12 @@ __global__ void __launch_bounds__(kThreads) step_multi_kernel(
             y.z = fmaf(al, y.z, va * kv[j].z);
             y.w = fmaf(al, y.w, va * kv[j].w);
             x[i][j] = y;
-            dot = fmaf(y.x, qv[j].x, dot);
-            dot = fmaf(y.y, qv[j].y, dot);
-            dot = fmaf(y.z, qv[j].z, dot);
-            dot = fmaf(y.w, qv[j].w, dot);
+            d0 = fmaf(y.x, qv[j].x, d0);
+            d1 = fmaf(y.y, qv[j].y, d1);
+            d2 = fmaf(y.z, qv[j].z, d2);
+            d3 = fmaf(y.w, qv[j].w, d3);
           }
-          dot = warp_sum(dot);
+          const float dot = warp_sum((d0 + d1) + (d2 + d3));
           if (lane == 0 && a < DV) h[((size_t)p * NT + t) * DV + a] = from_f32<TO>(dot * inv);
         }
       }
