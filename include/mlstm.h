@@ -258,8 +258,14 @@ mlstm_status mlstm_groupnorm_gate(const void *h, const void *o_pre, const float 
  *   dh [B,NH,S,DV] (dt): dL/dh.  Other inputs as for mlstm_fwd_chunkwise (same chunk rules).
  * Where |n_t . q_t| equals exp(-m_t) exactly, h has a kink; the derivative taken there treats
  * the floor as the active branch.  The forward is recomputed inside (gate preprocessing,
- * boundary states, per-token denominators), so no forward output is needed.  Runs on CUDA
- * cores in fp32 whatever dt.  workspace: at least mlstm_bwd_workspace_bytes(...) bytes. */
+ * boundary states, per-token denominators), so no forward output is needed.  For bf16 inputs
+ * with chunk 64 or 128, d_qk in {64, 128, 256, 512} and d_v a multiple of 128, the boundary and
+ * adjoint state walks run on tensor cores (fp16 operands, fp32 accumulation) and, with d_qk a
+ * multiple of 128 too, so do the products of the tokens with those states (tf32); the chunk-local
+ * L x L work runs on CUDA cores in fp32, as does everything for other sizes.  The tensor-core
+ * kernels' bounded device-side waits record into the error word at offset 0 of the workspace,
+ * which mlstm_fwd_check reads (pass the backward's workspace and sizes).
+ * workspace: at least mlstm_bwd_workspace_bytes(...) bytes. */
 size_t mlstm_bwd_workspace_bytes(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt);
 mlstm_status mlstm_bwd_chunkwise(const void *q, const void *k, const void *v,
                                  const float *igate_pre, const float *fgate_pre, const void *dh,
