@@ -10,7 +10,8 @@
 // inter-chunk recurrence (the boundary states C^(k), n^(k)); walked backwards with X = dh, Y = q
 // and the backward's weights it is the adjoint recurrence (G^(k), N^(k)).
 //
-// One CTA per (128 rows of DV, head): T lives in tensor memory (128 lanes x DQK fp32 columns),
+// One CTA per (128 rows of DV, half of DQK when DQK >= 128, head): T lives in tensor memory
+// (128 lanes x the CTA's DQK fp32 columns, twice where it fits),
 // each 64-token slab of X and Y arrives by TMA, is converted in place to fp16 (X scaled by its
 // token's weight) and enters T with four K = 16 tcgen05 MMAs per 128 x min(DQK, 256) block.
 // At every chunk boundary the epilogue warps read T, store the boundary state and write back
@@ -35,16 +36,17 @@ constexpr int kTileM = 128;   // rows of DV per CTA (tensor-memory lanes)
 // slabs in flight: four (two chunks of 128 tokens) where shared memory allows, else two
 template <int NQ>
 __host__ __device__ constexpr int stages_for() { return NQ <= 4 ? 4 : 2; }
-constexpr int kConvT = 256;  // conversion threads (warps 6-13)
-constexpr int kThreadsT = 192 + kConvT;
-// warp 0: TMA loads; warp 1: tensor-memory allocation and MMA issue; warps 2-5: epilogue
-// (tensor-memory lanes 32 (w % 4) .. + 31); warps 6-13: conversion and the n vector.
+constexpr int kEpiT = 256;   // epilogue threads (warps 2-9)
+constexpr int kConvT = 128;  // conversion threads (warps 10-13)
+constexpr int kThreadsT = 64 + kEpiT + kConvT;
+// warp 0: TMA loads; warp 1: tensor-memory allocation and MMA issue; warps 2-9: epilogue (warp
+// w reads tensor-memory lanes 32 (w % 4) .. + 31, warps w and w + 4 taking alternate 32-column
+// blocks, so that two warps share each quarter's state stores); warps 10-13: conversion and n.
 
-template <int NQ>  // DQK / 64
+template <int NQ>  // the CTA's columns of d_qk / 64
 struct alignas(1024) StatesSmem {
   static constexpr int ST = stages_for<NQ>();
   unsigned char tile[ST][(2 + NQ) * 8192];  // X boxes 0, 1 then NQ Y boxes, 64 x 128 B each
-  float stage_out[4][32][33];  // per epilogue warp: its 32 rows x 32 columns, transposed for the stores
   uint64_t full[ST], conv[ST], empty[ST];
   uint64_t mma_done, epi_ready, fin;
   float wx[ST][64];  // the slab's X weights
@@ -64,8 +66,8 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
     const float *__restrict__ wn, const float *__restrict__ alpha, const float *__restrict__ sc, int S, int L,
     int DV, int reverse, const float *__restrict__ C0, const float *__restrict__ n0, float *__restrict__ states,
     float *__restrict__ nstates, float *__restrict__ C_fin, float *__restrict__ n_fin, int *__restrict__ err,
-    float *__restrict__ states_t) {
-  constexpr int DQK = 64 * NQ;
+    float *__restrict__ states_t, int DQKt, int CS) {
+  constexpr int DQK = 64 * NQ;  // this CTA's columns: [cb, cb + DQK) of the state's DQKt
   constexpr int NN = DQK > 256 ? 2 : 1;  // MMAs per K step (N <= 256 each)
   constexpr int NB = DQK / NN;           // N of each
   // two state buffers where tensor memory has room (d_qk <= 256): the products of chunk k then
@@ -77,7 +79,8 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
   StatesSmem<NQ> &sm = *reinterpret_cast<StatesSmem<NQ> *>(
       (reinterpret_cast<uintptr_t>(st_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int p = blockIdx.y, a0 = blockIdx.x * kTileM;
+  // CTA = (128 rows of DV, one of CS column blocks, head)
+  const int p = blockIdx.y, a0 = (blockIdx.x / CS) * kTileM, cb = (blockIdx.x % CS) * DQK;
   const int NC = S / L, SUB = L / kSub, NS = S / kSub;
   // without per-chunk factors the walk keeps only the final state: the weights already carry
   // each token's decay to the end of the sequence (no rescaling between chunks, no stores)
@@ -97,7 +100,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
       mbar_init(&sm.empty[s], 1);
     }
     mbar_init(&sm.mma_done, 1);
-    mbar_init(&sm.epi_ready, 128);
+    mbar_init(&sm.epi_ready, kEpiT);
     mbar_init(&sm.fin, 1);
     sm.abort_flag = 0;
     sm.conv_fail = 0;
@@ -127,7 +130,8 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
         mbar_arrive_expect_tx(&sm.full[s], (uint32_t)(2 + NQ) * 8192u);
         tma_load_2d(sm.tile[s], &mapX, a0, row, &sm.full[s]);
         tma_load_2d(sm.tile[s] + 8192, &mapX, a0 + 64, row, &sm.full[s]);
-        for (int q = 0; q < NQ; ++q) tma_load_2d(sm.tile[s] + (2 + q) * 8192, &mapY, 64 * q, row, &sm.full[s]);
+        for (int q = 0; q < NQ; ++q)
+          tma_load_2d(sm.tile[s] + (2 + q) * 8192, &mapY, cb + 64 * q, row, &sm.full[s]);
         issued = j + 1;
       }
       // nothing may leave while loads it issued are still landing
@@ -171,11 +175,11 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
       mma_commit(&sm.fin);  // completes once every MMA issued above has finished
       mbar_wait(&sm.fin, 0, err, 48);
     }
-  } else if (warp < 6) {
+  } else if (warp < 2 + kEpiT / 32) {
     // ------------------------------------------------------------------ epilogue
     const int row = 32 * (warp & 3) + lane;  // the tensor-memory lane this thread may access
     const uint32_t trow = tm + ((uint32_t)(32 * (warp & 3)) << 16);
-    float(*wbuf)[33] = sm.stage_out[warp & 3];
+    const int cfirst = 32 * ((warp - 2) >> 2);  // this warp's first 32-column block; step 64
     float s_prev = 1.f;
     bool ok = true;
     if (final_only) {
@@ -183,11 +187,11 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
       const bool got = __all_sync(0xffffffffu, mbar_wait(&sm.mma_done, 0, err, 44, abort_ptr));
       if (got) {
         tc_fence_after();
-        for (int c0 = 0; c0 < DQK; c0 += 32) {
+        for (int c0 = cfirst; c0 < DQK; c0 += 64) {
           uint32_t r[32];
           tmem_ld32(trow + c0, r);
           tmem_wait_ld();
-          float *dst = C_fin + ((size_t)p * DV + a0 + row) * DQK + c0;
+          float *dst = C_fin + ((size_t)p * DV + a0 + row) * DQKt + cb + c0;
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<float4 *>(dst + e) = make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
@@ -214,7 +218,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
         // (the chunk index, not a flag: a warp that fails at chunk i + 1 before a slower warp has
         // read the word for chunk i must not stop that warp one chunk early)
         if (!got) atomicCAS(&sm.epi_fail, -1, i);
-        named_barrier_sync(2, 128);
+        named_barrier_sync(2, kEpiT);
         const int failed = *(volatile int *)&sm.epi_fail;
         if (failed >= 0 && failed <= i) {
           ok = false;
@@ -231,7 +235,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
         if (i == 0) {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            v[e] = C0 ? C0[((size_t)p * DV + a0 + row) * DQK + c0 + e] : 0.f;
+            v[e] = C0 ? C0[((size_t)p * DV + a0 + row) * DQKt + cb + c0 + e] : 0.f;
         } else {
           uint32_t r[32];
           tmem_ld32(tcur + c0, r);
@@ -250,26 +254,20 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
       };
       auto store_piece = [&](int c0, const float (&v)[32]) {
         if (states) {
-          // each thread holds 32 columns of its own row, and rows are 1 KB apart in global memory:
-          // the warp turns its 32 x 32 block around in shared memory (rows padded to 33 words, no
-          // bank conflicts) so that each store instruction writes one row's 128 contiguous bytes
+          float *dst = states + ((size_t)(p * (NC + 1) + b_in) * DV + a0 + row) * DQKt + cb + c0;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) wbuf[lane][e] = v[e];
-          __syncwarp();
-          float *base = states + ((size_t)(p * (NC + 1) + b_in) * DV + a0 + 32 * (warp & 3)) * DQK + c0 + lane;
-#pragma unroll 8
-          for (int rr = 0; rr < 32; ++rr) base[(size_t)rr * DQK] = wbuf[rr][lane];
-          __syncwarp();
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4 *>(dst + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
         }
         if (i == NC && C_fin) {
-          float *dst = C_fin + ((size_t)p * DV + a0 + row) * DQK + c0;
+          float *dst = C_fin + ((size_t)p * DV + a0 + row) * DQKt + cb + c0;
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<float4 *>(dst + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
         }
         if (states_t) {
           // the transposed state [DQK][DV]: for each column the warp's 32 rows are contiguous
-          float *dt = states_t + ((size_t)p * (NC + 1) + b_in) * (size_t)DQK * DV + (size_t)c0 * DV + a0 + row;
+          float *dt = states_t + ((size_t)p * (NC + 1) + b_in) * (size_t)DQKt * DV + (size_t)(cb + c0) * DV + a0 + row;
 #pragma unroll
           for (int e = 0; e < 32; ++e) dt[(size_t)e * DV] = v[e];
         }
@@ -277,7 +275,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
       if (PP) {
         // the next chunk's T first, so that its products start while this state is stored
         if (i < NC) {
-          for (int c0 = 0; c0 < DQK; c0 += 32) {
+          for (int c0 = cfirst; c0 < DQK; c0 += 64) {
             float v[32];
             state_piece(c0, v);
             rescale_piece(c0, v);
@@ -286,13 +284,13 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
           tc_fence_before();
           mbar_arrive(&sm.epi_ready);
         }
-        for (int c0 = 0; c0 < DQK; c0 += 32) {
+        for (int c0 = cfirst; c0 < DQK; c0 += 64) {
           float v[32];
           state_piece(c0, v);
           store_piece(c0, v);
         }
       } else {
-        for (int c0 = 0; c0 < DQK; c0 += 32) {
+        for (int c0 = cfirst; c0 < DQK; c0 += 64) {
           float v[32];
           state_piece(c0, v);
           store_piece(c0, v);
@@ -311,14 +309,14 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
     if (!ok) st_set_abort(abort_ptr);
   } else {
     // ------------------------------------------------------------------ conversion and n
-    const int ct = threadIdx.x - 192;  // 0 .. kConvT - 1
-    const bool do_n = blockIdx.x == 0 && (nstates != nullptr || n_fin != nullptr);
+    const int ct = threadIdx.x - 64 - kEpiT;  // 0 .. kConvT - 1
+    const bool do_n = blockIdx.x < CS && (nstates != nullptr || n_fin != nullptr);  // the first rows' CTAs
     constexpr int NPT = (DQK + kConvT - 1) / kConvT;  // n columns per thread
     float nacc[NPT];
 #pragma unroll
     for (int u = 0; u < NPT; ++u) {
       const int c = ct + kConvT * u;
-      nacc[u] = (n0 != nullptr && c < DQK) ? n0[(size_t)p * DQK + c] : 0.f;
+      nacc[u] = (n0 != nullptr && c < DQK) ? n0[(size_t)p * DQKt + cb + c] : 0.f;
     }
     auto store_n = [&](int b) {
       if (!do_n) return;
@@ -326,7 +324,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
       for (int u = 0; u < NPT; ++u) {
         const int c = ct + kConvT * u;
         if (c < DQK) {
-          if (nstates) nstates[((size_t)p * (NC + 1) + b) * DQK + c] = nacc[u];
+          if (nstates) nstates[((size_t)p * (NC + 1) + b) * DQKt + cb + c] = nacc[u];
         }
       }
     };
@@ -421,7 +419,7 @@ __global__ void __launch_bounds__(kThreadsT, 1) states_tc_kernel(
 #pragma unroll
         for (int u = 0; u < NPT; ++u) {
           const int c = ct + kConvT * u;
-          if (c < DQK) n_fin[(size_t)p * DQK + c] = nacc[u];
+          if (c < DQK) n_fin[(size_t)p * DQKt + cb + c] = nacc[u];
         }
       }
     }
@@ -501,13 +499,14 @@ template <int NQ>
 cudaError_t states_tc_t(const CUtensorMap &mx, const CUtensorMap &my, const float *wx, const float *wn,
                         const float *alpha, const float *sc, int P, int S, int L, int DV, bool reverse,
                         const float *C0, const float *n0, float *states, float *nstates, float *C_fin, float *n_fin,
-                        int *err, float *states_t, cudaStream_t stream) {
+                        int *err, float *states_t, int DQKt, int CS, cudaStream_t stream) {
   auto kern = states_tc_kernel<NQ>;
   const size_t smem = sizeof(StatesSmem<NQ>) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(DV / kTileM, P), kThreadsT, smem, stream>>>(mx, my, wx, wn, alpha, sc, S, L, DV, reverse ? 1 : 0, C0,
-                                                          n0, states, nstates, C_fin, n_fin, err, states_t);
+  kern<<<dim3(DV / kTileM * CS, P), kThreadsT, smem, stream>>>(mx, my, wx, wn, alpha, sc, S, L, DV, reverse ? 1 : 0,
+                                                               C0, n0, states, nstates, C_fin, n_fin, err, states_t,
+                                                               DQKt, CS);
   return cudaGetLastError();
 }
 
@@ -536,11 +535,15 @@ cudaError_t launch_states_tc(const void *X, const void *Y, const float *wx, cons
   const uint64_t rows = (uint64_t)P * S;
   if (!make_tmap_2d_b16(&mx, X, true, rows, DV, DV, 64, kSub)) return cudaErrorInvalidValue;
   if (!make_tmap_2d_b16(&my, Y, true, rows, DQK, DQK, 64, kSub)) return cudaErrorInvalidValue;
-  switch (DQK) {
-    case 64: return states_tc_t<1>(mx, my, wx, wn, alpha, sc, P, S, L, DV, reverse, C0, n0, states, nstates, C_fin, n_fin, err, states_t, stream);
-    case 128: return states_tc_t<2>(mx, my, wx, wn, alpha, sc, P, S, L, DV, reverse, C0, n0, states, nstates, C_fin, n_fin, err, states_t, stream);
-    case 256: return states_tc_t<4>(mx, my, wx, wn, alpha, sc, P, S, L, DV, reverse, C0, n0, states, nstates, C_fin, n_fin, err, states_t, stream);
-    case 512: return states_tc_t<8>(mx, my, wx, wn, alpha, sc, P, S, L, DV, reverse, C0, n0, states, nstates, C_fin, n_fin, err, states_t, stream);
+  // with every boundary stored, d_qk of 128 and more is split over two CTAs per 128 rows: twice
+  // the SMs share the boundary states' stores, and each CTA holds two state buffers in tensor
+  // memory (the final-state walk stores once and keeps its grid)
+  const int CS = DQK >= 128 && alpha != nullptr ? 2 : 1;
+  switch (DQK / CS) {
+    case 64: return states_tc_t<1>(mx, my, wx, wn, alpha, sc, P, S, L, DV, reverse, C0, n0, states, nstates, C_fin, n_fin, err, states_t, DQK, CS, stream);
+    case 128: return states_tc_t<2>(mx, my, wx, wn, alpha, sc, P, S, L, DV, reverse, C0, n0, states, nstates, C_fin, n_fin, err, states_t, DQK, CS, stream);
+    case 256: return states_tc_t<4>(mx, my, wx, wn, alpha, sc, P, S, L, DV, reverse, C0, n0, states, nstates, C_fin, n_fin, err, states_t, DQK, CS, stream);
+    case 512: return states_tc_t<8>(mx, my, wx, wn, alpha, sc, P, S, L, DV, reverse, C0, n0, states, nstates, C_fin, n_fin, err, states_t, DQK, CS, stream);
   }
   return cudaErrorInvalidValue;
 }
