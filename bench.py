@@ -450,13 +450,37 @@ def run_ours(args, rank, local, world):
 
     flops = fwd_flops(w)
     path = B.mlstm_fwd_path(w.B, w.NH, w.S, w.DQK, w.DV, w.chunk)
+    per_step = launches_fwd / max(args.steps, 1)
+    five = path >= 1 and round(per_step) == 5  # gate chain, pre-pass, n chain, denominators, state walk
     achieved_tf = flops / (ms * 1e-3) / 1e12
+    # the same forward through the single fused kernel (the least workspace selects it), for context
+    ws_least = torch.empty(B.mlstm_fwd_workspace_min_bytes(w.B, w.NH, w.S, w.DQK, w.DV, w.chunk),
+                           dtype=torch.uint8, device=dev)
+    fused_ms = None
+    if five:
+        for _ in range(3):
+            B.mlstm_fwd_chunkwise(q, k, v, ig, fg, w.chunk, h_dtype=torch.float32, out=(h, C, n, m),
+                                  workspace=ws_least)
+        fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
+        for a_, b_ in fev:
+            flush.zero_()
+            a_.record(stream)
+            B.mlstm_fwd_chunkwise(q, k, v, ig, fg, w.chunk, h_dtype=torch.float32, out=(h, C, n, m),
+                                  workspace=ws_least)
+            b_.record(stream)
+        torch.cuda.synchronize()
+        fused_ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in fev)
     roofline = {"bound": "tensor", "achieved": achieved_tf, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": achieved_tf / peaks["bf16_tflops"],
                 # the committed capture is of the 1.3B-style layer: other workloads report none
-                "traffic": captured_traffic("fwd_tc_kernel") if path >= 1 and w is W.LAYER_1P3B else None,
-                "kernel": ("fwd_tc_kernel (the whole forward: one launch)" if path >= 1
+                "traffic": (captured_traffic("forward@1p3b" if five else "fwd_tc_kernel")
+                            if path >= 1 and w is W.LAYER_1P3B else None),
+                "kernel": ("the whole forward call, five launches: gate chain, pre-pass (Q K^T on tensor "
+                           "cores, P, beta q, w k), n chain, denominators, state walk (U, X, P V on tensor "
+                           "cores; the largest share)" if five else
+                           "fwd_tc_kernel (the whole forward: one launch)" if path >= 1
                            else "gates + states + output kernels"),
+                "fused_single_kernel_ms": fused_ms,
                 "algorithmic_flops_per_launch": flops, "ms_per_launch": ms,
                 "peak_source": f"{peaks['source']} bf16 dense (burst); fp16 operands run at the same rate",
                 "frac_of_sustained": achieved_tf / peaks["bf16_tflops_sustained"]

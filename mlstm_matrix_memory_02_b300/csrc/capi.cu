@@ -32,10 +32,21 @@ struct Layout {
   // the sequence-parallel forward's buffers (G segments per head, the fused path only), after
   // `total`: per (head, segment) the sum of log f, the segment's own state and stabiliser, and
   // its entering state
-  size_t Bg, Cseg, nseg, mseg, Cin, nin, min, m1, cmseg, wx, wn, split_total;
+  size_t Bg, Cseg, nseg, mseg, Cin, nin, min, m1, cmseg, wx, wn;
+  // the three-kernel forward's buffers (per-chunk operands prepared ahead of the state walk)
+  size_t qb, kw, pm, pden, pinv, pdn, ptok4, ptok2, pcdat;
+  size_t split_total;  // the end of the optional buffers: the size mlstm_fwd_workspace_bytes reports
   int G, G1, Ls;  // segments per head (second pass, first pass); the first pass's chunk
   bool tc;  // the forward runs on the fused tensor-core kernel (no materialised states)
+  bool pre;  // the sizes suit the three-kernel forward (used when the workspace holds its buffers)
 };
+
+// The three-kernel forward (pre-pass, n chain, state walk) instead of the single fused kernel:
+// for heads split over a CTA pair, where the per-chunk work it does once per head would
+// otherwise be repeated by each d_v tile, and for sequences of at most 64 chunks of 64 tokens.
+bool use_prepass(int P, int S, int DQK, int DV) {
+  return fwd_prep_supported(S, DQK) && fwd_tc_pair(P, DQK, DV) && DQK == 512;
+}
 
 bool use_tc(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) {
   return fwd_tc_supported(S, chunk, DQK, DV, dt == MLSTM_BF16) && (long long)B * NH * S < (1LL << 31);
@@ -96,6 +107,17 @@ Layout layout(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) 
   L.cmseg = off; off = round_up(off + (NC1 + PG1) * sizeof(float));  // PG1 chains of S / (G1 Ls) + 1
   L.wx = off; off = round_up(off + PS1 * sizeof(float));
   L.wn = off; off = round_up(off + PS1 * sizeof(float));
+  L.pre = L.tc && L.G == 1 && use_prepass((int)P, S, DQK, DV);
+  const size_t PSp = L.pre ? P * (size_t)S : 0, PNCp = L.pre ? P * (size_t)(S / 64) : 0;
+  L.qb = off; off = round_up(off + PSp * DQK * 2);
+  L.kw = off; off = round_up(off + PSp * DQK * 2);
+  L.pm = off; off = round_up(off + PSp * 64 * 2);
+  L.pden = off; off = round_up(off + PSp * sizeof(float));
+  L.pinv = off; off = round_up(off + PSp * sizeof(float));
+  L.ptok4 = off; off = round_up(off + PSp * 4 * sizeof(float));
+  L.ptok2 = off; off = round_up(off + PSp * 2 * sizeof(float));
+  L.pdn = off; off = round_up(off + PNCp * DQK * sizeof(float));
+  L.pcdat = off; off = round_up(off + PNCp * 2 * 4 * sizeof(float));
   L.split_total = off;
   return L;
 }
@@ -287,6 +309,37 @@ static mlstm_status run_segments(const void *q, const void *k, const void *v, co
                                      exp_fg, P));
 }
 
+// The forward in three kernels: the pre-pass (per head and chunk: Q K^T on tensor cores, P,
+// beta q, w k, the n increment, the chunk's stabiliser and frame), the n chain with every token's
+// 1/den, and the state walk (U, X and P V on tensor cores).  n_init is read by every chunk's CTA
+// of the second kernel while one of them writes n_last, which may alias it: a copy is read.
+static mlstm_status run_prepass(const void *q, const void *k, const void *v, const Layout &Lw, int P, int S, int DQK,
+                                int DV, const float *C_init, const float *n_init, const float *m_init, const float *ig,
+                                const float *fg, bool exp_fg, void *h, mlstm_dtype h_dt, float *C_last,
+                                float *n_last, float *m_last, char *ws, cudaStream_t s) {
+  PrepBuffers b;
+  b.qb = (__half *)(ws + Lw.qb);
+  b.kw = (__half *)(ws + Lw.kw);
+  b.pm = (__half *)(ws + Lw.pm);
+  b.den = (float *)(ws + Lw.pden);
+  b.inv = (float *)(ws + Lw.pinv);
+  b.dn = (float *)(ws + Lw.pdn);
+  b.tok4 = (float4 *)(ws + Lw.ptok4);
+  b.tok2 = (float2 *)(ws + Lw.ptok2);
+  b.cdat = (float4 *)(ws + Lw.pcdat);
+  int *err = (int *)(ws + Lw.err);
+  if (n_init) {
+    float *ncopy = (float *)(ws + Lw.ncopy);
+    if (cudaMemcpyAsync(ncopy, n_init, sizeof(float) * (size_t)P * DQK, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return launch_status(cudaGetLastError());
+    n_init = ncopy;
+  }
+  if (mlstm_status st = launch_status(
+          launch_fwd_prep(q, k, ig, fg, m_init, P, S, DQK, exp_fg, b, n_init, n_last, m_last, err, s), 4))
+    return st;
+  return launch_status(launch_fwd_state(b, v, h_dt == MLSTM_BF16, P, S, DQK, DV, C_init, h, C_last, err, s));
+}
+
 // Everything after kernel (a), on a workspace that kernel (a) has filled for these sizes -- or,
 // on the tensor-core path when ig is given, from the raw gate pre-activations (ig, fg, m_init),
 // whose preprocessing the fused kernel then does itself.
@@ -309,6 +362,9 @@ static mlstm_status run_from_gates(const void *q, const void *k, const void *v, 
   if (Lw.tc && ig != nullptr && Lw.G > 1 && ws_bytes >= Lw.split_total)
     return run_segments(q, k, v, Lw, P, S, DQK, DV, C_init, n_init, m_init, ig, fg, exp_fg, h, h_dt, C_last,
                         n_last, m_last, ws, s);
+  if (Lw.tc && ig != nullptr && Lw.pre && ws_bytes >= Lw.split_total)
+    return run_prepass(q, k, v, Lw, P, S, DQK, DV, C_init, n_init, m_init, ig, fg, exp_fg, h, h_dt, C_last, n_last,
+                       m_last, ws, s);
   if (Lw.tc) {
     if (n_init) {
       float *ncopy = (float *)(ws + Lw.ncopy);

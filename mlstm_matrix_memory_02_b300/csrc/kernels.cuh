@@ -1,6 +1,7 @@
 // kernels.cuh -- launch wrappers of the mLSTM kernels (internal to the library).
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace mlstm {
@@ -112,6 +113,23 @@ cudaError_t launch_fwd_tc(const void *q, const void *k, const void *v, bool out_
                           const float *m_init, int P, int S, int D, int DV, const float *C_init,
                           const float *n_init, void *h, float *C_last, float *n_last, float *m_last, int *err,
                           cudaStream_t stream, bool exp_fg = false, int pair_heads = 0);
+// The forward in three kernels (fwd_prep.cu, fwd_state.cu) for bf16 heads of d_qk 256 or 512
+// split over a CTA pair: per (head, chunk) the state-independent work once (P, its row sums,
+// beta q and w k in fp16, the n increment, the chunk's stabiliser and frame), then n over the
+// chunks and every token's 1/den, then the state walk with the products U, X and P V only.
+struct PrepBuffers {
+  __half *qb, *kw, *pm;  // beta q, w k [P*S][D]; P [P*NC][64][64]
+  float *den, *inv, *dn;  // [P*S], [P*S], [P*NC][D] (the n increments, then n entering each chunk)
+  float4 *tok4;          // per token (x, mr, beta, w in the walk's frame / sqrt(d))
+  float2 *tok2;          // per token (w / sqrt(d), exp(-m))
+  float4 *cdat;          // per chunk: (m_in, m_out, alpha, frame after), (exp(frame), exp(frame) alpha, lazy, 0)
+};
+bool fwd_prep_supported(int S, int D);
+cudaError_t launch_fwd_prep(const void *q, const void *k, const float *ig, const float *fg, const float *m_init,
+                            int P, int S, int D, bool exp_fg, const PrepBuffers &b, const float *n_init,
+                            float *n_last, float *m_last, int *err, cudaStream_t stream);
+cudaError_t launch_fwd_state(const PrepBuffers &b, const void *v, bool out_bf16, int P, int S, int D, int DV,
+                             const float *C_init, void *h, float *C_last, int *err, cudaStream_t stream);
 // The sequence-parallel forward's helpers (seq_split.cu), for G segments of Sg tokens per head:
 // every segment's sum of log f (Bg, P*G floats) and m = -inf as its first-pass entering
 // stabiliser (min) ...

@@ -91,6 +91,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *e
   return mbar_wait_slow(bar, parity, err, code, abort);
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// A kernel launched with the programmatic-serialisation attribute may start while the previous
+// kernel in the stream is still running: pdl_wait blocks the calling thread until that kernel
+// has completed and its memory writes are visible (a no-op for a plain launch); pdl_trigger lets
+// the next such kernel be scheduled once every CTA of this one has issued it.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- clusters / distributed smem
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

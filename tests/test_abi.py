@@ -61,9 +61,13 @@ def test_workspace_bytes(lib):
     # (P x (NC+1) x DV x DQK fp32)
     need = gates + P * (NC + 1) * 512 * 512 * 4 + P * (NC + 1) * 512 * 4
     assert ws(4, 4, 2048, 512, 512, 64, 0) >= need
-    # tensor-core path (bf16, chunk 64): gate arrays, chunk m and a copy of n_init; no states
+    # tensor-core path (bf16, chunk 64): gate arrays, chunk m and a copy of n_init; no states.
+    # The full size adds the three-kernel forward's per-chunk operands (beta q and w k in fp16,
+    # P in fp16, per-token and per-chunk floats)
     assert lib.mlstm_fwd_path(4, 4, 2048, 512, 512, 64, 1) == 2  # d_qk = 512: CTA pair
-    assert gates + P * 512 * 4 <= ws(4, 4, 2048, 512, 512, 64, 1) < need // 100
+    least = lib.mlstm_fwd_workspace_min_bytes(4, 4, 2048, 512, 512, 64, 1)
+    assert gates + P * 512 * 4 <= least < need // 100
+    assert least + _prepass_bytes(P, S, 512) <= ws(4, 4, 2048, 512, 512, 64, 1) < need // 5
     assert ws(1, 1, 100, 64, 64, 64, 1) == 0      # S % chunk != 0
     assert ws(1, 1, 128, 48, 64, 64, 1) == 0      # DQK not a multiple of 32
     assert ws(1, 1, 128, 64, 1024, 64, 1) == 0    # DV above 512
@@ -84,6 +88,20 @@ def test_workspace_bytes_follow_the_path_that_runs(lib):
     assert gates128 <= ws_min(1, 8, S, 256, 256, 128, 1) < 4 << 20
     assert ws(1, 8, S, 256, 256, 128, 0) > P * (S // 128) * 256 * 256 * 4
     assert ws_min(1, 8, S, 256, 256, 128, 0) == ws(1, 8, S, 256, 256, 128, 0)
+
+
+def _prepass_bytes(P, S, D):
+    """Workspace of the three-kernel forward, restated: beta q and w k (fp16, D per token), P
+    (fp16, 64 per token), den, 1/den and six gate factors per token (eight floats), the n
+    increment (D floats) and two float4 per chunk."""
+    NC = S // 64
+    return 2 * P * S * D * 2 + P * S * 64 * 2 + P * S * 8 * 4 + P * NC * D * 4 + P * NC * 32
+
+
+def _prepass_expected(P, S, D):
+    """Where the three-kernel forward applies: d_qk = 512 (always a CTA pair), at most 64
+    chunks of 64 tokens, and no sequence segments."""
+    return D == 512 and 64 <= S <= 4096 and S % 64 == 0
 
 
 def _sms():
@@ -127,6 +145,9 @@ def test_sequence_parallel_selection(lib, b, nh, s, dqk, dv):
         least_extra = b * nh * ((G + G1) * per_state + s * per_token)
         slack = b * nh * (3 * 4 * G1 + 4 * G + 4 * (s // 64)) + 14 * 256  # B, m1, chains, round-ups
         assert least_extra <= full - least <= least_extra + slack
+    elif _prepass_expected(b * nh, s, dqk):
+        extra = _prepass_bytes(b * nh, s, dqk)
+        assert extra <= full - least <= extra + 24 * 256  # round-ups
     else:
         assert full == least
     assert seg(1, 2, 100, 64, 64, 64, 1, 1 << 30) == -1  # S % chunk != 0

@@ -877,3 +877,78 @@ def test_tensor_core_in_place_state_update(B, dqk):
                           n_init=n, m_init=m, out=(h, C, n, m))
     torch.cuda.synchronize()
     assert torch.equal(h, h_ref) and torch.equal(C, C_ref) and torch.equal(n, n_ref) and torch.equal(m, m_ref)
+
+
+# ----------------------------------------------------------------------------- d_qk = 512 in five kernels
+THREE_KERNEL_CASES = [
+    # (B, NH, S, DV, gates, init, forget, h dtype)
+    (1, 2, 256, 256, "layer", True, "sigmoid", torch.float32),
+    (1, 2, 192, 256, "stress", False, "sigmoid", torch.float32),
+    (1, 2, 320, 256, "layer", False, "exp", torch.bfloat16),
+    # 64 chunks, the longest sequence this path takes, with enough heads (80 CTA pairs) that the
+    # sequence is not cut into segments; the oracle checks two sampled heads
+    (2, 20, 4096, 128, "stress", True, "sigmoid", torch.float32),
+]
+
+
+@pytest.mark.parametrize("b,nh,s,dv,gates,init,forget,hdt", THREE_KERNEL_CASES)
+def test_three_kernel_forward(B, b, nh, s, dv, gates, init, forget, hdt):
+    """d_qk = 512 heads (CTA pairs) with the full workspace run as gate chain, pre-pass (Q K^T on
+    tensor cores, P, beta q, w k, the n increments), n chain, denominators and state walk; with
+    the least workspace as the single fused kernel.  Each against the oracle (the conditioned
+    bound of the tensor-core path), and the two against each other: the same state recurrence,
+    so the final states agree to fp32 rounding."""
+    dqk = 512
+    assert B.mlstm_fwd_segments(b, nh, s, dqk, dv, 64) == 1
+    w = W.LAYER_350M.with_(B=b, NH=nh, S=s, DQK=dqk, DV=dv)
+    if gates == "stress":
+        w = w.with_(ig=("student_t", 4.0, 3.0), fg=("normal", 0.0, 2.0))
+    inp = W.make_inputs(w)
+    if forget == "exp":
+        inp = exp_forget_inputs(inp)
+    init_np, kw = None, {}
+    if init:
+        rng = np.random.default_rng(12)
+        init_np = ((0.3 * rng.standard_normal((b, nh, dv, dqk))).astype(np.float32),
+                   (0.3 * rng.standard_normal((b, nh, dqk))).astype(np.float32),
+                   rng.uniform(-2, 3, (b, nh)).astype(np.float32))
+        kw = dict(C_init=torch.from_numpy(init_np[0]).cuda(), n_init=torch.from_numpy(init_np[1]).cuda(),
+                  m_init=torch.from_numpy(init_np[2]).cuda())
+    # the oracle on every head, or on two sampled heads of a large batch
+    heads = [(i, j) for i in range(b) for j in range(nh)]
+    if len(heads) > 4:
+        heads = [heads[3], heads[-5]]
+    sl = lambda x, i, j: x[i:i + 1, j:j + 1]
+    oras = {}
+    for (i, j) in heads:
+        sub = {key: sl(val, i, j) for key, val in inp.items()}
+        okw = {} if init_np is None else dict(C0=sl(init_np[0], i, j), n0=sl(init_np[1], i, j),
+                                              m0=sl(init_np[2], i, j))
+        oras[(i, j)] = (sub, oracle.recurrent(**sub, **okw, forget=forget, want_m_tok=True, want_den=True))
+    d = dev(inp, torch.bfloat16)
+    full = B.alloc_workspace(b, nh, s, dqk, dv, 64)
+    least = torch.empty(B.mlstm_fwd_workspace_min_bytes(b, nh, s, dqk, dv, 64), dtype=torch.uint8, device="cuda")
+    assert full.numel() > least.numel()
+    outs = []
+    for ws in (full, least):
+        h, C, n, m = B.mlstm_fwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], 64, h_dtype=hdt,
+                                           workspace=ws, forget=forget, **kw)
+        B.mlstm_fwd_check(ws, b, nh, s, dqk, dv, 64)
+        h, C, n, m = npy(h), npy(C), npy(n), npy(m)
+        assert np.all(np.isfinite(h))
+        for (i, j), (sub, ora) in oras.items():
+            hh = sl(h, i, j)
+            if hdt == torch.bfloat16:
+                ok, worst = bf16_out_ok(hh, ora["h"])
+                assert ok, worst
+            else:
+                ok, worst, stats = conditioned_ok(hh, ora, sub["v"], TOL_BF16, u_tc(dqk), u_tc(dqk))
+                assert ok, (worst, stats)
+                assert stats["rel_err_kappa_le_100"] <= TOL_BF16, stats
+            eC, en, em = state_errs(sl(C, i, j), sl(n, i, j), sl(m, i, j), ora["C"], ora["n"], ora["m"])
+            assert eC <= TOL_BF16 and en <= TOL_BF16 and em <= 1e-4, (eC, en, em)
+        outs.append((h, C, n, m))
+    assert rel_err(outs[0][1], outs[1][1]) <= 1e-5 and rel_err(outs[0][2], outs[1][2]) <= 1e-5
+    assert np.array_equal(outs[0][3], outs[1][3])
+    if gates == "layer":
+        assert rel_err(outs[0][0], outs[1][0]) <= TOL_BF16
