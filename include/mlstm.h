@@ -102,13 +102,25 @@ int mlstm_fwd_path(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype
  * element type).  On the fused path, sizes whose grid would leave most SMs idle (long
  * sequences over few heads, see mlstm_fwd_segments) also get the sequence-parallel buffers:
  * per head and segment one float32 state C, n, m for the segment's own map and one for its
- * entering state (the long-context layer, B=1 NH=8 S=16384 d=256, about 18 MB in all). */
+ * entering state (the long-context layer, B=1 NH=8 S=16384 d=256, about 18 MB in all).
+ * bf16 heads with d_qk = 512 over at most 64 chunks of 64 tokens (and no sequence segments)
+ * also get the buffers of the forward in five kernels: per token beta q and w k in fp16 (2 x
+ * d_qk halves), a row of P in fp16 (64 halves) and eight floats, per chunk the n increment
+ * (d_qk floats) and eight floats -- about 74 MB for the 1.3B-style layer (B=4 NH=4 S=2048).
+ * With them the forward runs as: per head the gate prefix sums, stabiliser chain and token
+ * factors; per (head, chunk) Q K^T on tensor cores with P, its row sums, beta q, w k and the n
+ * increment (section 3 "The Parallel Dual Form": the in-chunk matrix and the chunk's state
+ * update operands, which every d_v tile of a head shares); n entering each chunk; every
+ * token's 1/den; then the state walk with the products U, X and P V only.  The result is the
+ * same function up to rounding (the same state recurrence: C, n, m agree with the single
+ * fused kernel to fp32 rounding). */
 size_t mlstm_fwd_workspace_bytes(int B, int NH, int S, int DQK, int DV, int chunk,
                                  mlstm_dtype dt);
 
 /* The least workspace mlstm_fwd_chunkwise accepts for these sizes (0 if unsupported): that of
- * mlstm_fwd_workspace_bytes without the sequence-parallel buffers.  A workspace between the
- * two runs the forward over whole sequences, one head at a time per CTA (or CTA pair). */
+ * mlstm_fwd_workspace_bytes without the sequence-parallel buffers or the five-kernel
+ * forward's buffers.  A workspace below mlstm_fwd_workspace_bytes runs the forward over whole
+ * sequences in the single fused kernel, one head at a time per CTA (or CTA pair). */
 size_t mlstm_fwd_workspace_min_bytes(int B, int NH, int S, int DQK, int DV, int chunk,
                                      mlstm_dtype dt);
 
@@ -140,7 +152,8 @@ int mlstm_fwd_segments(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_d
  *       after the last token (may alias C_init/n_init/m_init for an in-place update).
  *   workspace: at least mlstm_fwd_workspace_min_bytes(...) bytes of device memory;
  *       mlstm_fwd_workspace_bytes(...) bytes enable the sequence-parallel forward where it
- *       applies (mlstm_fwd_segments).
+ *       applies (mlstm_fwd_segments) and the five-kernel forward of d_qk = 512 heads (see
+ *       mlstm_fwd_workspace_bytes).
  * S == 0 copies the initial state to the outputs. */
 mlstm_status mlstm_fwd_chunkwise(const void *q, const void *k, const void *v,
                                  const float *igate_pre, const float *fgate_pre, int B, int NH,
