@@ -662,10 +662,19 @@ mlstm_status mlstm_bwd_chunkwise(const void *q, const void *k, const void *v, co
                            F(Lw.ns), nullptr, nullptr, s);
     ++kernels;
   }
+  // a chunk's L x L matrix (mode 0: E (q k^T) / sqrt(d) and n^(k) . q; mode 1: E (g v^T + c)): on
+  // tensor cores for bf16 chunks of 64, else on CUDA cores
+  auto chunk_mat = [&](int mode, const void *x, const void *y, int K, const float *invD, const float *cc, float *out,
+                       float *nq) {
+    if (bf16 && chunk_gram_tc_supported(chunk, K))
+      return launch_chunk_gram_tc(mode, x, y, K, invD, cc, F(Lw.gx), F(Lw.gu), F(Lw.cm), F(Lw.ns), P, S, DQK, out, nq,
+                                  err, s);
+    return launch_bwd_mat(mode, x, y, bf16, K, invD, cc, F(Lw.gx), F(Lw.gu), F(Lw.cm), F(Lw.ns), P, S, chunk, DQK, out,
+                          nq, s);
+  };
   if (e == cudaSuccess && S > 0) {
     // each chunk's decay-weighted scores P (also the dv kernel's matrix) and n^(k) . q_t, once
-    e = launch_bwd_mat(0, q, k, bf16, DQK, nullptr, nullptr, F(Lw.gx), F(Lw.gu), F(Lw.cm), F(Lw.ns), P, S, chunk, DQK,
-                       F(Lw.pm), F(Lw.nq), s);
+    e = chunk_mat(0, q, k, DQK, nullptr, nullptr, F(Lw.pm), F(Lw.nq));
     if (e == cudaSuccess)
       e = launch_output_simt(q, k, v, bf16, false, F(Lw.gb), F(Lw.gx), F(Lw.gu), F(Lw.cm), F(Lw.Cs), F(Lw.ns), P, S,
                              chunk, DQK, DV, F(Lw.h32), s, F(Lw.den), tc_prod ? F(Lw.xq) : nullptr, F(Lw.pm),
@@ -676,9 +685,7 @@ mlstm_status mlstm_bwd_chunkwise(const void *q, const void *k, const void *v, co
     e = launch_bwd_prep(dh, bf16, F(Lw.h32), F(Lw.den), F(Lw.gb), F(Lw.gu), F(Lw.cm), P, S, chunk, DV, F(Lw.invD),
                         F(Lw.cc), s);
     // each chunk's M1 = E (g v^T + c), once
-    if (e == cudaSuccess)
-      e = launch_bwd_mat(1, dh, v, bf16, DV, F(Lw.invD), F(Lw.cc), F(Lw.gx), F(Lw.gu), F(Lw.cm), F(Lw.ns), P, S,
-                         chunk, DQK, F(Lw.m1), nullptr, s);
+    if (e == cudaSuccess) e = chunk_mat(1, dh, v, DV, F(Lw.invD), F(Lw.cc), F(Lw.m1), nullptr);
     kernels += 2;
   }
   if (e == cudaSuccess && tc_states) {

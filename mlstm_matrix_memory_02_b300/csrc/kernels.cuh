@@ -61,6 +61,12 @@ cudaError_t launch_bwd_dv(const void *q, const void *k, const void *dh, bool bf1
 // mode 0, x = q, y = k, K = DQK: P_ut = E_ut (q_u . khat_t), and nq = n^(k) . q_u per token;
 // mode 1, x = dh, y = v, K = DV: M1_ut = E_ut (dh_u . v_t / D_u + c_u).  (pm, m1 and nq also
 // feed launch_output_simt, launch_bwd_dqdk and launch_bwd_dv.)
+// The same two matrices on tensor cores (chunk_gram_tc.cu) for bf16 inputs, chunks of 64 and K in
+// {64, 128, 256, 512}: the raw products bf16 x bf16 with fp32 sums, the factors applied in fp32.
+bool chunk_gram_tc_supported(int L, int K);
+cudaError_t launch_chunk_gram_tc(int mode, const void *x, const void *y, int K, const float *invD, const float *cc,
+                                 const float *gx, const float *gu, const float *cm, const float *ns, int P, int S,
+                                 int DQK, float *out, float *nq, int *err, cudaStream_t stream);
 cudaError_t launch_bwd_mat(int mode, const void *x, const void *y, bool bf16, int K, const float *invD,
                            const float *cc, const float *gx, const float *gu, const float *cm, const float *ns, int P,
                            int S, int L, int DQK, float *out, float *nq, cudaStream_t stream);
