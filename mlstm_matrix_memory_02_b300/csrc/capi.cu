@@ -45,7 +45,7 @@ struct Layout {
 // for heads split over a CTA pair, where the per-chunk work it does once per head would
 // otherwise be repeated by each d_v tile, and for sequences of at most 64 chunks of 64 tokens.
 bool use_prepass(int P, int S, int DQK, int DV) {
-  return fwd_prep_supported(S, DQK) && fwd_tc_pair(P, DQK, DV) && DQK == 512;
+  return fwd_prep_supported(S, DQK) && fwd_tc_pair(P, DQK, DV);
 }
 
 bool use_tc(int B, int NH, int S, int DQK, int DV, int chunk, mlstm_dtype dt) {

@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kStThreads, 1) fwd_state_kernel(
   using Lay = StLayout<DH>;
   constexpr int D = 2 * DH;
   constexpr uint32_t kColC16 = DH, kColH = DH + DH / 2;
-  static_assert(DH == 128 || DH == 256, "DH");
+  static_assert(DH == 256, "DH");
   static_assert(Lay::STAGE % 1024 == 0, "stage alignment");
   extern __shared__ uint8_t st_dyn[];
   __shared__ StSmem sm;
@@ -445,13 +445,9 @@ cudaError_t launch_fwd_state(const PrepBuffers &b, const void *v, bool out_bf16,
                              const float *C_init, void *h, float *C_last, int *err, cudaStream_t stream) {
   if (P == 0 || S == 0) return cudaSuccess;
   if (DV % kTileS != 0 || S % kLs != 0) return cudaErrorInvalidValue;
-  if (D == 512)
-    return out_bf16 ? launch_state_one<256, __nv_bfloat16>(b, v, P, S, DV, C_init, h, C_last, err, stream)
-                    : launch_state_one<256, float>(b, v, P, S, DV, C_init, h, C_last, err, stream);
-  if (D == 256)
-    return out_bf16 ? launch_state_one<128, __nv_bfloat16>(b, v, P, S, DV, C_init, h, C_last, err, stream)
-                    : launch_state_one<128, float>(b, v, P, S, DV, C_init, h, C_last, err, stream);
-  return cudaErrorInvalidValue;
+  if (D != 512) return cudaErrorInvalidValue;  // the sizes the pre-pass takes
+  return out_bf16 ? launch_state_one<256, __nv_bfloat16>(b, v, P, S, DV, C_init, h, C_last, err, stream)
+                  : launch_state_one<256, float>(b, v, P, S, DV, C_init, h, C_last, err, stream);
 }
 
 }  // namespace mlstm

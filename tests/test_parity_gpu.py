@@ -885,6 +885,7 @@ THREE_KERNEL_CASES = [
     (1, 2, 256, 256, "layer", True, "sigmoid", torch.float32),
     (1, 2, 192, 256, "stress", False, "sigmoid", torch.float32),
     (1, 2, 320, 256, "layer", False, "exp", torch.bfloat16),
+    (3, 1, 64, 128, "stress", True, "sigmoid", torch.float32),  # a single chunk
     # 64 chunks, the longest sequence this path takes, with enough heads (80 CTA pairs) that the
     # sequence is not cut into segments; the oracle checks two sampled heads
     (2, 20, 4096, 128, "stress", True, "sigmoid", torch.float32),
