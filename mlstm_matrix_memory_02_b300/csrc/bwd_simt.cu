@@ -248,12 +248,42 @@ __global__ void __launch_bounds__(256) bwd_dqdk_kernel(
     sB[r * (kSlab + 1) + c] = to_f32(kin[(tbase + r) * DQK + c0 + c]) * scale;
   }
   __syncthreads();
-  for (int t = 0; t < L; ++t) {
-    const float kt = sB[t * (kSlab + 1) + cx], qt = sA[t * (kSlab + 1) + cx];
+  {
+    // register tiles of L/16 rows x 2 columns (thread (rq, cq): rows RQ rq + i, columns 2 cq + j),
+    // so that each shared-memory read feeds two or more products
+    constexpr int RQ = L / 16;
+    const int cq = tid & 15, rq = tid >> 4;
+    float aq[RQ][2], ak[RQ][2];
+#pragma unroll
+    for (int i = 0; i < RQ; ++i) aq[i][0] = aq[i][1] = ak[i][0] = ak[i][1] = 0.f;
+#pragma unroll 4
+    for (int t = 0; t < L; ++t) {
+      const float k0 = sB[t * (kSlab + 1) + 2 * cq], k1 = sB[t * (kSlab + 1) + 2 * cq + 1];
+      const float q0 = sA[t * (kSlab + 1) + 2 * cq], q1 = sA[t * (kSlab + 1) + 2 * cq + 1];
+#pragma unroll
+      for (int i = 0; i < RQ; ++i) {
+        const float mr = sM[(RQ * rq + i) * (L + 1) + t];  // M1[u][t]: sum_t M1[u][t] khat_t
+        const float mc = sM[t * (L + 1) + RQ * rq + i];    // M1[t][u]: sum_t M1[t][u] q_t
+        aq[i][0] = fmaf(mr, k0, aq[i][0]);
+        aq[i][1] = fmaf(mr, k1, aq[i][1]);
+        ak[i][0] = fmaf(mc, q0, ak[i][0]);
+        ak[i][1] = fmaf(mc, q1, ak[i][1]);
+      }
+    }
+    // back to the row-per-thread layout of the rest of the kernel, through shared memory
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < RQ; ++i)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        sA[(RQ * rq + i) * (kSlab + 1) + 2 * cq + j] = aq[i][j];
+        sB[(RQ * rq + i) * (kSlab + 1) + 2 * cq + j] = ak[i][j];
+      }
+    __syncthreads();
 #pragma unroll
     for (int i = 0; i < RR; ++i) {
-      dq_in[i] = fmaf(sM[(ry + 8 * i) * (L + 1) + t], kt, dq_in[i]);  // sum_t M1[u][t] khat_t
-      dk_in[i] = fmaf(sM[t * (L + 1) + ry + 8 * i], qt, dk_in[i]);    // sum_u M1[u][t] q_u
+      dq_in[i] = sA[(ry + 8 * i) * (kSlab + 1) + cx];
+      dk_in[i] = sB[(ry + 8 * i) * (kSlab + 1) + cx];
     }
   }
 
@@ -394,10 +424,32 @@ __global__ void __launch_bounds__(256) bwd_dv_kernel(
     sA[r * (kSlab + 1) + a] = to_f32(dh[(tbase + r) * DV + a0 + a]) * sInv[r];
   }
   __syncthreads();
-  for (int u = 0; u < L; ++u) {
-    const float gu_a = sA[u * (kSlab + 1) + ax];
+  {
+    // register tiles of L/16 rows x 2 columns, as in the dq/dk kernel: sum_u M2[u][t] g_u
+    constexpr int RQ = L / 16;
+    const int cq = tid & 15, rq = tid >> 4;
+    float av[RQ][2];
 #pragma unroll
-    for (int i = 0; i < RR; ++i) dv_in[i] = fmaf(sM[u * (L + 1) + ry + 8 * i], gu_a, dv_in[i]);
+    for (int i = 0; i < RQ; ++i) av[i][0] = av[i][1] = 0.f;
+#pragma unroll 4
+    for (int u = 0; u < L; ++u) {
+      const float g0 = sA[u * (kSlab + 1) + 2 * cq], g1 = sA[u * (kSlab + 1) + 2 * cq + 1];
+#pragma unroll
+      for (int i = 0; i < RQ; ++i) {
+        const float mc = sM[u * (L + 1) + RQ * rq + i];
+        av[i][0] = fmaf(mc, g0, av[i][0]);
+        av[i][1] = fmaf(mc, g1, av[i][1]);
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < RQ; ++i)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) sB[(RQ * rq + i) * (kSlab + 1) + 2 * cq + j] = av[i][j];
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < RR; ++i) dv_in[i] = sB[(ry + 8 * i) * (kSlab + 1) + ax];
+    __syncthreads();  // the inter-chunk part below restages sA and sB
   }
   const float *Gk = Gs + ((size_t)p * (NC + 1) + kc + 1) * (size_t)DV * DQK;
   for (int c0 = 0; c0 < DQK && yv == nullptr; c0 += kSlab) {

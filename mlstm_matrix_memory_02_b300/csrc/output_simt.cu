@@ -131,10 +131,34 @@ __global__ void __launch_bounds__(256) output_simt_kernel(
     sV[r * kCols + a] = to_f32(vin[(tbase + r) * DV + a0 + a]);
   }
   __syncthreads();
-  for (int j = 0; j < L; ++j) {
-    const float vv = sV[j * kCols + ax];
+  {
+    // register tiles of L/16 rows x 2 columns (thread (rq, cq): rows RQ rq + i, columns 2 cq + j),
+    // so that each shared-memory read feeds two or more products; then back to the
+    // row-per-thread layout through shared memory
+    constexpr int RQ = L / 16;
+    const int cq = tid & 15, rq = tid >> 4;
+    float an[RQ][2];
 #pragma unroll
-    for (int i = 0; i < RR; ++i) num_in[i] = fmaf(sP[(ry + 8 * i) * (L + 1) + j], vv, num_in[i]);
+    for (int i = 0; i < RQ; ++i) an[i][0] = an[i][1] = 0.f;
+#pragma unroll 4
+    for (int j = 0; j < L; ++j) {
+      const float v0 = sV[j * kCols + 2 * cq], v1 = sV[j * kCols + 2 * cq + 1];
+#pragma unroll
+      for (int i = 0; i < RQ; ++i) {
+        const float pr = sP[(RQ * rq + i) * (L + 1) + j];
+        an[i][0] = fmaf(pr, v0, an[i][0]);
+        an[i][1] = fmaf(pr, v1, an[i][1]);
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < RQ; ++i) {
+      sV[(RQ * rq + i) * kCols + 2 * cq] = an[i][0];
+      sV[(RQ * rq + i) * kCols + 2 * cq + 1] = an[i][1];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < RR; ++i) num_in[i] = sV[(ry + 8 * i) * kCols + ax];
   }
   for (int c0 = 0; c0 < DQK && xq == nullptr; c0 += kSlab) {
     __syncthreads();
