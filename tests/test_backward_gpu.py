@@ -132,6 +132,31 @@ def test_backward_bf16_tensor_core_states(B, dqk, dv, s, chunk, init):
     run_case(B, W.LAYER_350M.with_(B=1, NH=2, S=s, DQK=dqk, DV=dv), chunk, init=init, conditioned=init)
 
 
+def test_backward_full_size_sampled_heads(B):
+    """The 350M-style layer at full size (B=8, NH=4, S=1024, d=256, chunk 64: the configuration
+    the benchmark times) through the tensor-core backward; two sampled heads against the fp64
+    oracle's backward of those heads alone (heads are independent)."""
+    w = W.LAYER_350M
+    inp = W.make_inputs(w)
+    dh = upstream(w)
+    d = {x: torch.from_numpy(inp[x]).cuda().to(torch.bfloat16).contiguous() for x in ("q", "k", "v")}
+    d.update({x: torch.from_numpy(inp[x]).cuda().contiguous() for x in ("ig", "fg")})
+    g = B.mlstm_bwd_chunkwise(d["q"], d["k"], d["v"], d["ig"], d["fg"], torch.from_numpy(dh).cuda().to(torch.bfloat16),
+                              w.chunk)
+    torch.cuda.synchronize()
+    for (i, j) in ((3, 1), (6, 2)):
+        sl = lambda x: x[i:i + 1, j:j + 1]
+        ora = oracle.recurrent_backward(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["ig"]), sl(inp["fg"]), sl(dh))
+        for name in ("dq", "dk", "dv", "dig", "dfg"):
+            x = sl(npy(g[name]))
+            assert np.all(np.isfinite(x)), name
+            if name in ("dq", "dk", "dv"):
+                ok, worst = bf16_out_ok(x, ora[name], TOL_BF16)
+                assert ok, (i, j, name, worst)
+            else:
+                assert rel_err(x, ora[name]) <= TOL_BF16, (i, j, name, rel_err(x, ora[name]))
+
+
 def test_backward_state_paths_agree(B):
     """The same bf16 inputs with chunk 32 (states on CUDA cores) and chunk 64 (states on tensor
     cores): the gradients agree to the bf16 tolerance."""
