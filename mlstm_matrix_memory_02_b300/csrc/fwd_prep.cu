@@ -17,11 +17,12 @@
 // instead of in each tile of the state walk (fwd_state.cu).  Four kernels, in stream order:
 //   gate chain  per head: the gate prefix sums of every chunk, the stabiliser chain and the
 //               frame of the state walk over the chunks, every token's factors
-//   pre-pass    per (chunk, head), three CTAs to an SM: q and k arrive by TMA in two halves of
-//               d_qk; for each half one thread issues its part of Q K^T on the tensor cores
-//               (M = 64, N = 64, bf16 in, fp32 accumulated in tensor memory) while every thread
-//               converts the half into the fp16 operands beta q and w k and sums the n increment;
-//               warps 0-3 then read S from tensor memory and write P (fp16) and its row sums
+//   pre-pass    per (chunk, head), four CTAs to an SM (the whole grid of the 1.3B layer resident
+//               at once): q and k arrive by TMA in four parts of d_qk; for each part one thread
+//               issues its share of Q K^T on the tensor cores (M = 64, N = 64, bf16 in, fp32
+//               accumulated in tensor memory) while every thread converts the part into the fp16
+//               operands beta q and w k and sums the n increment; warps 0-3 then read S from
+//               tensor memory and write P (fp16) and its row sums
 //   n chain     per head: n_{k+1} = alpha_k n_k + dn_k over the chunks (n entering each chunk)
 //   denominator per (chunk, head): 1 / max(|den_r + beta_r n_k . q_r|, exp(-m_r)) per token
 #include <cuda_bf16.h>
@@ -40,6 +41,7 @@ using namespace sm100;
 
 constexpr int kLp = 64;                  // chunk length
 constexpr int kPrepThreads = 256;
+constexpr int kPrepParts = 4;            // d_qk in four parts: 42 KB of shared memory, four CTAs per SM
 constexpr int kPrepMaxChunks = 64;       // chunks per head this path takes (S <= 4096)
 constexpr float kFrameLog = 5.545177444479562f;  // ln(2^8): largest lazy frame factor of the state walk
 
@@ -149,14 +151,15 @@ __global__ void __launch_bounds__(1024) fwd_gchain_kernel(const float *__restric
 }
 
 template <int D>
-__global__ void __launch_bounds__(kPrepThreads, 3) fwd_prep_kernel(
+__global__ void __launch_bounds__(kPrepThreads, 4) fwd_prep_kernel(
     const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
     const float4 *__restrict__ tok4, const float2 *__restrict__ tok2, int S, float scale, __half *__restrict__ qb,
     __half *__restrict__ kw, __half *__restrict__ pm, float *__restrict__ den, float *__restrict__ dn,
     int *__restrict__ err) {
-  constexpr int DH = D / 2;                // columns per half: q and k arrive half by half
+  constexpr int NP = kPrepParts;           // q and k arrive in NP parts of d_qk
+  constexpr int DH = D / NP;               // columns per part
   constexpr int HBYTES = DH * 128;         // a [64 x DH] 2-byte tile: DH / 64 swizzled blocks of 8 KB
-  constexpr int CPR = DH / 8;              // 16-byte chunks per row of a half
+  constexpr int CPR = DH / 8;              // 16-byte chunks per row of a part
   constexpr int RG = kPrepThreads / CPR;   // rows converted at once
   static_assert(DH % 64 == 0 && D <= 512 && kPrepThreads % CPR == 0, "D");
   extern __shared__ uint8_t prep_dyn[];
@@ -183,7 +186,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) fwd_prep_kernel(
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = sm.tmem_base;
-  // q and k columns [hf DH, hf DH + DH) of the chunk into the (single) half stage
+  // q and k columns [hf DH, hf DH + DH) of the chunk into the (single) stage
   auto load_half = [&](int hf) {
     mbar_arrive_expect_tx(&sm.full, 2u * HBYTES);
 #pragma unroll 1
@@ -211,11 +214,11 @@ __global__ void __launch_bounds__(kPrepThreads, 3) fwd_prep_kernel(
 
   bool ok = true;
 #pragma unroll 1
-  for (int hf = 0; hf < 2; ++hf) {
-    ok = __syncthreads_and(mbar_wait(&sm.full, hf, err, 101)) != 0;
+  for (int hf = 0; hf < NP; ++hf) {
+    ok = __syncthreads_and(mbar_wait(&sm.full, hf & 1, err, 101)) != 0;
     if (!ok) break;
     if (tid == 32) {
-      // S += Q K^T over this half's columns (M = 64, N = 64, K = DH)
+      // S += Q K^T over this part's columns (M = 64, N = 64, K = DH)
       tc_fence_after();
       const uint32_t id_S = idesc_f16(64, kLp, /*bf16*/ 1, 0, 0);
       const uint64_t dq = smem_desc(smem_u32(sq), 16, 1024, kSwizzle128B);
@@ -227,7 +230,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) fwd_prep_kernel(
       }
       mma_commit(&sm.done);
     }
-    // beta q and w k of this half into the 16-bit operands (global, row-major), and the partial
+    // beta q and w k of this part into the 16-bit operands (global, row-major), and the partial
     // sums of the n increment per row group: thread = (16-byte column chunk, row group)
     {
       const int ch = tid % CPR, rg = tid / CPR;
@@ -269,12 +272,12 @@ __global__ void __launch_bounds__(kPrepThreads, 3) fwd_prep_kernel(
       for (int g = 0; g < RG; ++g) a += spart[g * DH + c];
       dn[((size_t)p * NC + k) * D + hf * DH + c] = a;
     }
-    if (hf == 0) {
-      // the stage is reloaded once the products of the first half have read it (every thread
-      // has passed the conversion above, which read it last)
+    if (hf + 1 < NP) {
+      // the stage is reloaded once this part's products have read it (every thread has passed
+      // the conversion above, which read it last)
       if (tid == 0) {
-        ok = mbar_wait(&sm.done, 0, err, 104);
-        if (ok) load_half(1);
+        ok = mbar_wait(&sm.done, hf & 1, err, 104);
+        if (ok) load_half(hf + 1);
       }
       ok = __syncthreads_and(ok) != 0;
       if (!ok) break;
@@ -282,38 +285,40 @@ __global__ void __launch_bounds__(kPrepThreads, 3) fwd_prep_kernel(
   }
   // P and its row sums from S (M = 64 layout: row 16 w + l in lane l < 16 of warp w's quarter)
   if (ok && warp < 4) {
-    const bool got = __all_sync(0xffffffffu, mbar_wait(&sm.done, 1, err, 102));
+    const bool got = __all_sync(0xffffffffu, mbar_wait(&sm.done, (NP - 1) & 1, err, 102));
     if (got) {
       tc_fence_after();
-      uint32_t u[2][32];
       const uint32_t lb = (uint32_t)(warp * 32) << 16;
-      tmem_ld32(tm + lb, u[0]);
-      tmem_ld32(tm + lb + 32, u[1]);
-      tmem_wait_ld();
-      if (lane < 16) {
-        const int r = 16 * warp + lane;
-        const float mrr = sm.mr[r];
-        float d = 0.f;
-        uint4 *prow = reinterpret_cast<uint4 *>(pm + (((size_t)p * NC + k) * kLp + r) * kLp);
+      const int r = 16 * warp + (lane & 15);
+      const float mrr = sm.mr[r];
+      float d = 0.f;
+      uint4 *prow = reinterpret_cast<uint4 *>(pm + (((size_t)p * NC + k) * kLp + r) * kLp);
+      // 16 columns of S at a time (the loads are warp-wide; lanes 16-31 hold no row)
+#pragma unroll 1
+      for (int c16 = 0; c16 < kLp / 16; ++c16) {
+        uint32_t u[16];
+        tmem_ld16(tm + lb + 16 * c16, u);
+        tmem_wait_ld();
+        if (lane < 16) {
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          float pv[8];
+          for (int h8 = 0; h8 < 2; ++h8) {
+            float pv[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int j = 8 * c8 + e;
-            const float s = __uint_as_float(u[j >> 5][j & 31]);
-            pv[e] = j <= r ? s * scale * __expf(sm.x[j] - mrr) : 0.f;
-            d += pv[e];
+            for (int e = 0; e < 8; ++e) {
+              const int j = 16 * c16 + 8 * h8 + e;
+              pv[e] = j <= r ? __uint_as_float(u[8 * h8 + e]) * scale * __expf(sm.x[j] - mrr) : 0.f;
+              d += pv[e];
+            }
+            uint4 w4;
+            w4.x = pack_half2(pv[0], pv[1]);
+            w4.y = pack_half2(pv[2], pv[3]);
+            w4.z = pack_half2(pv[4], pv[5]);
+            w4.w = pack_half2(pv[6], pv[7]);
+            prow[2 * c16 + h8] = w4;
           }
-          uint4 w4;
-          w4.x = pack_half2(pv[0], pv[1]);
-          w4.y = pack_half2(pv[2], pv[3]);
-          w4.z = pack_half2(pv[4], pv[5]);
-          w4.w = pack_half2(pv[6], pv[7]);
-          prow[c8] = w4;
         }
-        den[tok0 + r] = d;
       }
+      if (lane < 16) den[tok0 + r] = d;
     }
   }
   if (!ok && tid == 0) {
@@ -451,8 +456,9 @@ cudaError_t launch_prep_d(const void *q, const void *k, const float *ig, const f
   fwd_gchain_kernel<<<P, 1024, 0, stream>>>(ig, fg, m_init, S, scale, exp_fg ? 1 : 0, b.tok4, b.tok2, b.cdat);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // one half stage of q and k, the row-group partial sums of a half, alignment slack
-  const size_t smem = (size_t)D * 128 + (size_t)(kPrepThreads / (D / 16)) * (D / 2) * 4 + 1024;
+  // one stage of q and k (a part of d_qk), the row-group partial sums of a part, alignment slack
+  constexpr int DP = D / kPrepParts;
+  const size_t smem = (size_t)2 * DP * 128 + (size_t)(kPrepThreads / (DP / 8)) * DP * 4 + 1024;
   auto kern = fwd_prep_kernel<D>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess)
