@@ -371,21 +371,28 @@ __global__ void __launch_bounds__(256) fwd_nchain_kernel(float *__restrict__ dn,
 // denominator cancels).  One CTA per (chunk, head), eight rows per warp, every row requested
 // before any is reduced.
 template <int D>
-__global__ void __launch_bounds__(256) fwd_ninv_kernel(const __nv_bfloat16 *__restrict__ q, const float *__restrict__ nk,
-                                                       const float4 *__restrict__ cdat, const float *__restrict__ den,
-                                                       const float4 *__restrict__ tok4, const float2 *__restrict__ tok2,
-                                                       int S, float *__restrict__ inv, float *__restrict__ m_last) {
+__global__ void __launch_bounds__(256, 4) fwd_ninv_kernel(const __nv_bfloat16 *__restrict__ q,
+                                                          const float *__restrict__ nk,
+                                                          const float4 *__restrict__ cdat,
+                                                          const float *__restrict__ den,
+                                                          const float4 *__restrict__ tok4,
+                                                          const float2 *__restrict__ tok2, int S,
+                                                          float *__restrict__ inv, float *__restrict__ m_last) {
   constexpr int PER = D / 32;  // elements of a row per lane
+  constexpr int RB = 4;        // rows of a warp requested at once (64 registers: four CTAs per SM)
   const int k = blockIdx.x, p = blockIdx.y, NC = S / kLp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t tok0 = (size_t)p * S + (size_t)k * kLp;
-  uint4 qv[8][PER / 8];
+  uint4 qv[RB][PER / 8];
+  auto load_rows = [&](int half) {
 #pragma unroll
-  for (int rr = 0; rr < 8; ++rr) {
-    const uint4 *qr = reinterpret_cast<const uint4 *>(q + (tok0 + warp + 8 * rr) * D + lane * PER);
+    for (int rr = 0; rr < RB; ++rr) {
+      const uint4 *qr = reinterpret_cast<const uint4 *>(q + (tok0 + warp + 8 * (RB * half + rr)) * D + lane * PER);
 #pragma unroll
-    for (int v8 = 0; v8 < PER / 8; ++v8) qv[rr][v8] = qr[v8];
-  }
+      for (int v8 = 0; v8 < PER / 8; ++v8) qv[rr][v8] = qr[v8];
+    }
+  };
+  load_rows(0);
   pdl_trigger();
   pdl_wait();  // n, den and the gate factors come from the previous kernels
   float nv[PER];
@@ -400,30 +407,34 @@ __global__ void __launch_bounds__(256) fwd_ninv_kernel(const __nv_bfloat16 *__re
   }
   // written here, after every CTA of the gate kernel has read m_init (which m_last may alias)
   if (k == NC - 1 && threadIdx.x == 0) m_last[p] = cdat[2 * ((size_t)p * NC + k)].y;
-  float dots[8];
+#pragma unroll 1
+  for (int half = 0; half < 8 / RB; ++half) {
+    if (half > 0) load_rows(half);
+    float dots[RB];
 #pragma unroll
-  for (int rr = 0; rr < 8; ++rr) {
-    float a = 0.f;
+    for (int rr = 0; rr < RB; ++rr) {
+      float a = 0.f;
 #pragma unroll
-    for (int v8 = 0; v8 < PER / 8; ++v8) {
-      const uint4 w = qv[rr][v8];
-      a += bf16_lo(w.x) * nv[8 * v8] + bf16_hi(w.x) * nv[8 * v8 + 1];
-      a += bf16_lo(w.y) * nv[8 * v8 + 2] + bf16_hi(w.y) * nv[8 * v8 + 3];
-      a += bf16_lo(w.z) * nv[8 * v8 + 4] + bf16_hi(w.z) * nv[8 * v8 + 5];
-      a += bf16_lo(w.w) * nv[8 * v8 + 6] + bf16_hi(w.w) * nv[8 * v8 + 7];
+      for (int v8 = 0; v8 < PER / 8; ++v8) {
+        const uint4 w = qv[rr][v8];
+        a += bf16_lo(w.x) * nv[8 * v8] + bf16_hi(w.x) * nv[8 * v8 + 1];
+        a += bf16_lo(w.y) * nv[8 * v8 + 2] + bf16_hi(w.y) * nv[8 * v8 + 3];
+        a += bf16_lo(w.z) * nv[8 * v8 + 4] + bf16_hi(w.z) * nv[8 * v8 + 5];
+        a += bf16_lo(w.w) * nv[8 * v8 + 6] + bf16_hi(w.w) * nv[8 * v8 + 7];
+      }
+      dots[rr] = a;
     }
-    dots[rr] = a;
-  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
+    for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-    for (int rr = 0; rr < 8; ++rr) dots[rr] += __shfl_xor_sync(0xffffffffu, dots[rr], o);
-  if (lane < 8) {
-    float a = dots[0];
+      for (int rr = 0; rr < RB; ++rr) dots[rr] += __shfl_xor_sync(0xffffffffu, dots[rr], o);
+    if (lane < RB) {
+      float a = dots[0];
 #pragma unroll
-    for (int rr = 1; rr < 8; ++rr) a = lane == rr ? dots[rr] : a;
-    const size_t t = tok0 + warp + 8 * lane;
-    inv[t] = 1.f / fmaxf(fabsf(den[t] + tok4[t].z * a), tok2[t].y);
+      for (int rr = 1; rr < RB; ++rr) a = lane == rr ? dots[rr] : a;
+      const size_t t = tok0 + warp + 8 * (RB * half + lane);
+      inv[t] = 1.f / fmaxf(fabsf(den[t] + tok4[t].z * a), tok2[t].y);
+    }
   }
 }
 
